@@ -1,0 +1,529 @@
+/*
+ * moe_oracle.c -- plain, slow, CPU reference of the token-choice top-k
+ * Mixture-of-Experts FFN layer forward.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package smoke check and
+ * the CPU-baseline leg of the benchmark may load this library.  The product
+ * (the CUDA library and its Python binding) never calls it, and it shares no
+ * code, header, table or constant with the CUDA path.
+ *
+ * Arithmetic is fp64 throughout, except where the pages fix fp32:
+ *   - router logits are stored as fp32 ("Mixture of Experts (MoE) From
+ *     Scratch to DeepSeek V3", stability tricks: the router is computed in
+ *     float32), and expert selection compares fp32 keys;
+ *   - the sigmoid selection key of DeepSeek-V3-style routing is an fp32
+ *     value (see orc_exp32 / orc_sigmoid32 below);
+ *   - the aux-loss-free bias b_i is an fp32 parameter updated in place.
+ * For bf16 layers the activation output H is rounded to bf16, because that
+ * is the storage precision of the layer's intermediate (a bf16 Linear ->
+ * activation -> Linear chain keeps H in bf16).
+ *
+ * Functions and the passages they follow:
+ *   orc_router_logits    "MoE Training: Mixture of Experts", Quick Start
+ *                        MoELayer (gate = nn.Linear(hidden, E) with bias);
+ *                        "...From Scratch to DeepSeek V3", routing formula
+ *                        h(x) = x . W_g.
+ *   orc_route            same pages: softmax -> top-k -> renormalise
+ *                        (MoELayer.forward; moe_code.py MixtureOfExperts
+ *                        steps 1-3); sigmoid scores with selection bias b_i
+ *                        (DeepSeek V3 page: sigmoid routing, aux-loss-free
+ *                        balancing, Score_i = x.e_i + b_i).
+ *   orc_capacity         "MoE Training Guide", Core MoE Parameters:
+ *                        capacity = tokens / num_experts x capacity_factor,
+ *                        min_capacity 4, drop_tokens.
+ *   orc_dispatch         same + DeepSeek V3 page "Token Dropping": slots
+ *                        beyond an expert's capacity are left unprocessed.
+ *   orc_forward_tokens   moe_code.py MixtureOfExperts.forward, the
+ *                        per-position loop  output[i] += p_j * E_j(x_i);
+ *                        experts: Quick Start Linear-GELU-Linear,
+ *                        moe_code.py Expert ReLU FFN (dropout = identity in
+ *                        a forward pass), SwiGLU (three-matrix expert of the
+ *                        Mixtral parameter arithmetic in the MoE technical
+ *                        survey page); shared expert and the "+ x" residual
+ *                        of the routing formula from the DeepSeek V3 page.
+ *   orc_dense_all        moe_code.py EfficientMoE.forward: every expert on
+ *                        every token, then gather and weight (brute force).
+ *   orc_stats            "MoE Training: Mixture of Experts", Load Balancing
+ *                        (auxiliary loss N * sum f_i P_i; router z-loss
+ *                        mean(logsumexp^2)); "MoE Training Guide",
+ *                        Monitoring (imbalance, utilisation, drop rate).
+ *   orc_bias_update      DeepSeek V3 page, aux-loss-free balancing: lower
+ *                        b_i for an overloaded expert, raise it for an idle
+ *                        one.
+ *   orc_param_counts     moe_code.py compare_moe_vs_dense; the Mixtral
+ *                        parameter arithmetic of the MoE technical survey.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* configuration and tensors (the oracle's own layout description)     */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    int64_t T;               /* tokens (batch * seq, flattened)          */
+    int32_t d, E, k, F;      /* d_model, routed experts, top_k, d_ff      */
+    int32_t score_fn;        /* 0 softmax, 1 sigmoid                     */
+    int32_t activation;      /* 0 GELU (erf), 1 ReLU, 2 SwiGLU           */
+    int32_t renormalize;     /* 1: gates renormalised over the top-k     */
+    int32_t drop_tokens;     /* 1: capacity limit applies                */
+    int32_t min_capacity;
+    int32_t num_shared;      /* always-on experts, weight 1              */
+    int32_t residual;        /* 1: output adds x                          */
+    int32_t dtype;           /* storage of x and all weights: 0 f32, 1 bf16 */
+    double capacity_factor;
+} orc_cfg;
+
+typedef struct {
+    const void *x;           /* [T, d]                                    */
+    const void *w_router;    /* [E, d]                                    */
+    const float *b_router;   /* [E] fp32, or NULL                         */
+    const float *sel_bias;   /* [E] fp32 (sigmoid routing), or NULL       */
+    const void *w1, *b1;     /* [E, F, d], [E, F] (b1 may be NULL)        */
+    const void *w3;          /* [E, F, d] (SwiGLU only)                   */
+    const void *w2, *b2;     /* [E, d, F], [E, d] (b2 may be NULL)        */
+    const void *sw1, *sw3, *sw2; /* shared experts: [S,F,d],[S,F,d],[S,d,F] */
+} orc_tensors;
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* storage decode: fp32 as is, bf16 = upper 16 bits of an fp32 (exact) */
+static double elem(const void *p, int dtype, int64_t i) {
+    if (dtype == 0) return (double)((const float *)p)[i];
+    uint32_t u = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static void decode_row(const void *p, int dtype, int64_t off, int64_t n, double *dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = elem(p, dtype, off + i);
+}
+
+static double dot_row(const void *p, int dtype, int64_t off, const double *v, int64_t n) {
+    double acc = 0.0;
+    if (dtype == 0) {
+        const float *q = (const float *)p + off;
+        for (int64_t i = 0; i < n; ++i) acc += (double)q[i] * v[i];
+    } else {
+        const uint16_t *q = (const uint16_t *)p + off;
+        for (int64_t i = 0; i < n; ++i) {
+            uint32_t u = (uint32_t)q[i] << 16;
+            float f;
+            memcpy(&f, &u, 4);
+            acc += (double)f * v[i];
+        }
+    }
+    return acc;
+}
+
+/* round an fp64 value to the nearest bf16 value (8 significant bits, ties to
+ * even), returned as fp64.  Used only to mirror bf16 storage of H. */
+double orc_round_bf16(double v) {
+    if (v == 0.0 || !isfinite(v)) return v;
+    int ex;
+    double m = frexp(v, &ex);          /* v = m * 2^ex, 0.5 <= |m| < 1 */
+    double q = nearbyint(m * 256.0);   /* 8 significant bits, ties-to-even */
+    return ldexp(q / 256.0, ex);
+}
+
+/* ------------------------------------------------------------------ */
+/* fp32 sigmoid key                                                      */
+/* ------------------------------------------------------------------ */
+/*
+ * The selection key of sigmoid routing is an fp32 number, and an integer
+ * decision (which experts) is taken on it, so both sides of a parity check
+ * must produce the same bits.  The key is therefore fixed by a written
+ * recipe built only from IEEE-754 correctly rounded fp32 operations:
+ *
+ *   exp32(a):  Cody-Waite argument reduction with ln 2 split in two
+ *              (hi part = ln 2 truncated to 16 bits, lo part = the fp32
+ *              remainder):  n = rint(a * log2e),  r = fma(-n, ln2_hi, a),
+ *              r = fma(-n, ln2_lo, r);  e^r by the degree-7 Taylor
+ *              polynomial sum r^i / i! in Horner form with fma;  result =
+ *              p * 2^n (one multiply by an exact power of two).
+ *              a > 88 gives +inf, a < -87 gives 0, NaN propagates.
+ *   sigmoid32(x) = 1 / (1 + exp32(-x))      (fp32 add and divide)
+ *   key         = sigmoid32(logit) + b_i     (fp32 add)
+ *
+ * Constants are the fp32 values nearest to log2(e), 1/i!, and the exact
+ * 16-bit head of ln 2 with its fp32 tail.
+ */
+static const float K_LOG2E = 0x1.715476p+0f;
+static const float K_LN2_HI = 0x1.62e4p-1f;
+static const float K_LN2_LO = 0x1.7f7d1cp-20f;
+static const float K_INV_FACT[8] = {1.0f, 1.0f, 0x1p-1f, 0x1.555556p-3f, 0x1.555556p-5f,
+                                    0x1.111112p-7f, 0x1.6c16c2p-10f, 0x1.a01a02p-13f};
+
+float orc_exp32(float a) {
+    if (a != a) return a;
+    if (a > 88.0f) return INFINITY;
+    if (a < -87.0f) return 0.0f;
+    float t = a * K_LOG2E;
+    float n = rintf(t);
+    float r = fmaf(-n, K_LN2_HI, a);
+    r = fmaf(-n, K_LN2_LO, r);
+    float p = K_INV_FACT[7];
+    for (int i = 6; i >= 0; --i) p = fmaf(p, r, K_INV_FACT[i]);
+    int ni = (int)n;                       /* -126 <= ni <= 127 here */
+    uint32_t bits = (uint32_t)(ni + 127) << 23;
+    float scale;
+    memcpy(&scale, &bits, 4);
+    return p * scale;
+}
+
+float orc_sigmoid32(float x) {
+    float e = orc_exp32(-x);
+    float den = 1.0f + e;
+    return 1.0f / den;
+}
+
+/* ------------------------------------------------------------------ */
+/* step 1: router logits                                                */
+/* ------------------------------------------------------------------ */
+/* logits[t,e] = sum_i x[t,i] * W_r[e,i] (+ b_r[e]), summed in fp64 and
+ * stored as fp32. */
+void orc_router_logits(const orc_cfg *c, const orc_tensors *w, float *logits) {
+    const int64_t T = c->T, d = c->d, E = c->E;
+    double *wr = (double *)malloc(sizeof(double) * (size_t)(E * d));
+    decode_row(w->w_router, c->dtype, 0, E * d, wr);
+#pragma omp parallel
+    {
+        double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            decode_row(w->x, c->dtype, t * d, d, xv);
+            for (int64_t e = 0; e < E; ++e) {
+                double acc = 0.0;
+                const double *we = wr + e * d;
+                for (int64_t i = 0; i < d; ++i) acc += xv[i] * we[i];
+                if (w->b_router) acc += (double)w->b_router[e];
+                logits[t * E + e] = (float)acc;
+            }
+        }
+        free(xv);
+    }
+    free(wr);
+}
+
+/* ------------------------------------------------------------------ */
+/* step 2: scores, top-k, gates, per-token logsumexp                   */
+/* ------------------------------------------------------------------ */
+/*
+ * Keys: softmax routing ranks experts by their fp32 logit (softmax is
+ * strictly increasing, so the top-k set of the probabilities is the top-k
+ * set of the logits); sigmoid routing ranks by sigmoid32(logit) + b_i.
+ * The k largest keys are taken largest first; equal keys go to the lower
+ * expert index.
+ *
+ * Gates (fp64): softmax p_j = exp(l_j - lse); sigmoid s_j = 1/(1+exp(-l_j))
+ * (b_i is not part of the gate).  With renormalize the selected values are
+ * divided by their sum.
+ *
+ * Outputs: idx[t*k+j], gate[t*k+j], lse[t] (fp64) and, if prob_sum is not
+ * NULL, prob_sum[e] = sum_t softmax(logits_t)_e summed in token order.
+ */
+void orc_route(const orc_cfg *c, const float *logits, const float *sel_bias,
+               int32_t *idx, double *gate, double *lse, double *prob_sum) {
+    const int64_t T = c->T, E = c->E, k = c->k;
+#pragma omp parallel
+    {
+        float *key = (float *)malloc(sizeof(float) * (size_t)E);
+        unsigned char *taken = (unsigned char *)malloc((size_t)E);
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            const float *l = logits + t * E;
+            for (int64_t e = 0; e < E; ++e) {
+                if (c->score_fn == 0) {
+                    key[e] = l[e];
+                } else {
+                    float s = orc_sigmoid32(l[e]);
+                    float b = sel_bias ? sel_bias[e] : 0.0f;
+                    key[e] = s + b;
+                }
+                taken[e] = 0;
+            }
+            /* selection: k passes, each takes the largest remaining key */
+            for (int64_t j = 0; j < k; ++j) {
+                int64_t best = -1;
+                for (int64_t e = 0; e < E; ++e) {
+                    if (taken[e]) continue;
+                    if (best < 0 || key[e] > key[best]) best = e;
+                }
+                taken[best] = 1;
+                idx[t * k + j] = (int32_t)best;
+            }
+            /* log-sum-exp of the logits in fp64 */
+            double m = -INFINITY;
+            for (int64_t e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+            double s = 0.0;
+            for (int64_t e = 0; e < E; ++e) s += exp((double)l[e] - m);
+            lse[t] = m + log(s);
+            /* gates */
+            double tot = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                double le = (double)l[idx[t * k + j]];
+                double v = (c->score_fn == 0) ? exp(le - lse[t]) : 1.0 / (1.0 + exp(-le));
+                gate[t * k + j] = v;
+                tot += v;
+            }
+            if (c->renormalize)
+                for (int64_t j = 0; j < k; ++j) gate[t * k + j] /= tot;
+        }
+        free(key);
+        free(taken);
+    }
+    if (prob_sum) {
+        for (int64_t e = 0; e < E; ++e) prob_sum[e] = 0.0;
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t e = 0; e < E; ++e)
+                prob_sum[e] += exp((double)logits[t * E + e] - lse[t]);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* step 3: capacity, drop, permutation                                  */
+/* ------------------------------------------------------------------ */
+/* capacity = max(min_capacity, ceil(T / E * capacity_factor)); without
+ * token dropping every slot is kept (returns T * k, an upper bound). */
+int64_t orc_capacity(const orc_cfg *c) {
+    if (!c->drop_tokens) return c->T * (int64_t)c->k;
+    double v = ceil((double)c->T / (double)c->E * c->capacity_factor);
+    int64_t cap = (int64_t)v;
+    return cap > c->min_capacity ? cap : c->min_capacity;
+}
+
+/*
+ * Slots s = t*k + j are visited in priority order: all j = 0 slots in token
+ * order, then all j = 1 slots, and so on (the Quick Start loop runs over
+ * the top-k rank outside and the tokens inside).  Each slot takes the next
+ * rank of its expert; a rank >= capacity is dropped.  Kept slots of expert
+ * e fill rows offsets[e] .. offsets[e+1]-1 in that priority order.
+ *
+ * counts[e]: slots routed to e before dropping; kept[e] = min(counts, cap);
+ * offsets[E+1]: exclusive prefix sum of kept; perm[row] = slot (rows past
+ * offsets[E] are -1); inv[slot] = row or -1 for a dropped slot.
+ */
+void orc_dispatch(const orc_cfg *c, const int32_t *idx, int32_t *counts, int32_t *kept,
+                  int32_t *offsets, int32_t *perm, int32_t *inv) {
+    const int64_t T = c->T, E = c->E, k = c->k, S = T * k;
+    const int64_t cap = orc_capacity(c);
+    int32_t *rank = (int32_t *)malloc(sizeof(int32_t) * (size_t)(S > 0 ? S : 1));
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t j = 0; j < k; ++j)
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t s = t * k + j;
+            rank[s] = counts[idx[s]]++;
+        }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        kept[e] = counts[e] < cap ? counts[e] : (int32_t)cap;
+        offsets[e + 1] = offsets[e] + kept[e];
+    }
+    for (int64_t r = 0; r < S; ++r) perm[r] = -1;
+    for (int64_t s = 0; s < S; ++s) {
+        if (rank[s] < cap) {
+            int32_t row = offsets[idx[s]] + rank[s];
+            inv[s] = row;
+            perm[row] = (int32_t)s;
+        } else {
+            inv[s] = -1;
+        }
+    }
+    free(rank);
+}
+
+/* ------------------------------------------------------------------ */
+/* step 4: experts                                                       */
+/* ------------------------------------------------------------------ */
+static double act_gelu(double a) { return 0.5 * a * (1.0 + erf(a / sqrt(2.0))); }
+static double act_relu(double a) { return a > 0.0 ? a : 0.0; }
+static double act_silu(double a) { return a / (1.0 + exp(-a)); }
+
+double orc_gelu(double a) { return act_gelu(a); }
+double orc_silu(double a) { return act_silu(a); }
+
+/*
+ * One expert on one token row (fp64):
+ *   GELU / ReLU:  y = W2 act(W1 x + b1) + b2
+ *   SwiGLU:       y = W2 (silu(W1 x) * (W3 x))        (no biases)
+ * W1, W3: [F, d] and W2: [d, F] slices of expert e; h holds F scratch values.
+ */
+static void expert_row(const orc_cfg *c, const void *W1, const void *B1, const void *W3,
+                       const void *W2, const void *B2, int64_t e, const double *xv,
+                       double *h, double *y) {
+    const int64_t d = c->d, F = c->F;
+    const int dt = c->dtype;
+    for (int64_t f = 0; f < F; ++f) {
+        double a = dot_row(W1, dt, e * F * d + f * d, xv, d);
+        double v;
+        if (c->activation == 2) {
+            double u = dot_row(W3, dt, e * F * d + f * d, xv, d);
+            v = act_silu(a) * u;
+        } else {
+            if (B1) a += elem(B1, dt, e * F + f);
+            v = (c->activation == 0) ? act_gelu(a) : act_relu(a);
+        }
+        h[f] = (dt == 1) ? orc_round_bf16(v) : v;
+    }
+    for (int64_t n = 0; n < d; ++n) {
+        double acc = dot_row(W2, dt, e * d * F + n * F, h, F);
+        if (c->activation != 2 && B2) acc += elem(B2, dt, e * d + n);
+        y[n] = acc;
+    }
+}
+
+/* Exposed for tests: one routed expert on one row (y has d entries). */
+void orc_expert_row(const orc_cfg *c, const orc_tensors *w, int64_t e, const double *xv, double *y) {
+    double *h = (double *)malloc(sizeof(double) * (size_t)c->F);
+    expert_row(c, w->w1, w->b1, w->w3, w->w2, w->b2, e, xv, h, y);
+    free(h);
+}
+
+/*
+ * Layer output for the listed tokens (fp64, out[n_tok, d]):
+ *   out_t = sum_j [slot kept] gate[t,j] * E_{idx[t,j]}(x_t)
+ *         + sum_s Shared_s(x_t) + (residual ? x_t : 0)
+ * summed in that order, j ascending.
+ */
+void orc_forward_tokens(const orc_cfg *c, const orc_tensors *w, const int32_t *idx,
+                        const double *gate, const int32_t *inv, const int64_t *tokens,
+                        int64_t n_tok, double *out) {
+    const int64_t d = c->d, k = c->k;
+#pragma omp parallel
+    {
+        double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+        double *y = (double *)malloc(sizeof(double) * (size_t)d);
+        double *h = (double *)malloc(sizeof(double) * (size_t)c->F);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_tok; ++i) {
+            const int64_t t = tokens[i];
+            double *o = out + i * d;
+            decode_row(w->x, c->dtype, t * d, d, xv);
+            for (int64_t n = 0; n < d; ++n) o[n] = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                const int64_t s = t * k + j;
+                if (inv && inv[s] < 0) continue;   /* dropped: contributes 0 */
+                expert_row(c, w->w1, w->b1, w->w3, w->w2, w->b2, idx[s], xv, h, y);
+                for (int64_t n = 0; n < d; ++n) o[n] += gate[s] * y[n];
+            }
+            for (int64_t sh = 0; sh < c->num_shared; ++sh) {
+                expert_row(c, w->sw1, NULL, w->sw3, w->sw2, NULL, sh, xv, h, y);
+                for (int64_t n = 0; n < d; ++n) o[n] += y[n];
+            }
+            if (c->residual)
+                for (int64_t n = 0; n < d; ++n) o[n] += xv[n];
+        }
+        free(xv);
+        free(y);
+        free(h);
+    }
+}
+
+/*
+ * Brute force (EfficientMoE): all[t, e, :] = E_e(x_t) for every token and
+ * every routed expert, then out_t = sum_j gate[t,j] * all[t, idx[t,j], :]
+ * (+ shared + residual as above).  Dropped slots (inv < 0) are skipped.
+ * Only for tiny layers: T * E expert evaluations.
+ */
+void orc_dense_all(const orc_cfg *c, const orc_tensors *w, const int32_t *idx,
+                   const double *gate, const int32_t *inv, double *all, double *out) {
+    const int64_t T = c->T, d = c->d, E = c->E, k = c->k;
+    double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+    double *h = (double *)malloc(sizeof(double) * (size_t)c->F);
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int64_t t = 0; t < T; ++t) {
+        decode_row(w->x, c->dtype, t * d, d, xv);
+        for (int64_t e = 0; e < E; ++e)
+            expert_row(c, w->w1, w->b1, w->w3, w->w2, w->b2, e, xv, h, all + (t * E + e) * d);
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        double *o = out + t * d;
+        decode_row(w->x, c->dtype, t * d, d, xv);
+        for (int64_t n = 0; n < d; ++n) o[n] = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            const int64_t s = t * k + j;
+            if (inv && inv[s] < 0) continue;
+            const double *sel = all + (t * E + idx[s]) * d;
+            for (int64_t n = 0; n < d; ++n) o[n] += gate[s] * sel[n];
+        }
+        for (int64_t sh = 0; sh < c->num_shared; ++sh) {
+            expert_row(c, w->sw1, NULL, w->sw3, w->sw2, NULL, sh, xv, h, y);
+            for (int64_t n = 0; n < d; ++n) o[n] += y[n];
+        }
+        if (c->residual)
+            for (int64_t n = 0; n < d; ++n) o[n] += xv[n];
+    }
+    free(xv);
+    free(h);
+    free(y);
+}
+
+/* ------------------------------------------------------------------ */
+/* step 5: balance statistics and monitoring                            */
+/* ------------------------------------------------------------------ */
+/*
+ * f_e = counts_e / (T k)            (fraction of routed slots, pre-drop)
+ * P_e = prob_sum_e / T              (mean softmax probability)
+ * aux = E * sum_e f_e P_e
+ * z   = mean_t lse_t^2
+ * scal[0..5] = aux, z, dropped, imbalance (max kept / min kept, +inf when
+ * an expert is empty), utilisation (#experts with kept > 0 / E),
+ * drop rate (dropped / (T k)).
+ */
+void orc_stats(const orc_cfg *c, const int32_t *counts, const int32_t *kept,
+               const double *prob_sum, const double *lse, double *f, double *P, double *scal) {
+    const int64_t T = c->T, E = c->E, S = c->T * (int64_t)c->k;
+    double aux = 0.0, z = 0.0;
+    int64_t dropped = 0, used = 0, kmax = 0, kmin = -1;
+    for (int64_t e = 0; e < E; ++e) {
+        f[e] = S > 0 ? (double)counts[e] / (double)S : 0.0;
+        P[e] = T > 0 ? prob_sum[e] / (double)T : 0.0;
+        aux += f[e] * P[e];
+        dropped += counts[e] - kept[e];
+        if (kept[e] > 0) ++used;
+        if (kept[e] > kmax) kmax = kept[e];
+        if (kmin < 0 || kept[e] < kmin) kmin = kept[e];
+    }
+    for (int64_t t = 0; t < T; ++t) z += lse[t] * lse[t];
+    scal[0] = (double)E * aux;
+    scal[1] = T > 0 ? z / (double)T : 0.0;
+    scal[2] = (double)dropped;
+    scal[3] = kmin > 0 ? (double)kmax / (double)kmin : INFINITY;
+    scal[4] = (double)used / (double)E;
+    scal[5] = S > 0 ? (double)dropped / (double)S : 0.0;
+}
+
+/* b_e <- b_e + gamma * sign(mean_load - counts_e), mean_load = T k / E,
+ * sign(0) = 0, stored as fp32. */
+void orc_bias_update(const orc_cfg *c, const int32_t *counts, float *bias, float gamma) {
+    const int64_t E = c->E, S = c->T * (int64_t)c->k;
+    for (int64_t e = 0; e < E; ++e) {
+        int64_t diff = S - E * (int64_t)counts[e];   /* sign of S/E - counts_e */
+        double sgn = diff > 0 ? 1.0 : (diff < 0 ? -1.0 : 0.0);
+        bias[e] = (float)((double)bias[e] + (double)gamma * sgn);
+    }
+}
+
+/* Parameter counts, biases ignored as on the pages:
+ * out[0] = one expert (2 d F, or 3 d F for a gated expert), out[1] = router
+ * d E, out[2] = total E * expert + router, out[3] = active k * expert +
+ * router. */
+void orc_param_counts(int64_t d, int64_t F, int64_t E, int64_t k, int gated, int64_t *out) {
+    int64_t expert = (gated ? 3 : 2) * d * F;
+    int64_t router = d * E;
+    out[0] = expert;
+    out[1] = router;
+    out[2] = E * expert + router;
+    out[3] = k * expert + router;
+}

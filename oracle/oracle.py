@@ -1,0 +1,253 @@
+"""ctypes wrapper of the plain CPU oracle (``moe_oracle.c``).
+
+TEST INFRASTRUCTURE: only the tests, the package smoke check and the
+benchmark's CPU-baseline leg use this module.  It never imports the product
+package; a layer description is any object with the attributes
+``T d E k F score_fn activation renormalize drop_tokens min_capacity
+capacity_factor num_shared residual dtype`` (the workload generator's
+``Workload`` has them).
+
+Parity unpinned: the floating-point layer output of the bf16 workloads has
+no printed worked example on the pages; it is pinned only through the
+brute-force path, the E=1 dense special case, and the closed forms checked
+in the oracle tests.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+from typing import Dict, Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+          "-shared", "-fPIC", "-Wall", "-Wno-unused-function"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp contraction off: every fp32 and fp64
+    operation is rounded on its own, as written)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Cfg(C.Structure):
+    _fields_ = [("T", C.c_int64), ("d", C.c_int32), ("E", C.c_int32), ("k", C.c_int32),
+                ("F", C.c_int32), ("score_fn", C.c_int32), ("activation", C.c_int32),
+                ("renormalize", C.c_int32), ("drop_tokens", C.c_int32),
+                ("min_capacity", C.c_int32), ("num_shared", C.c_int32), ("residual", C.c_int32),
+                ("dtype", C.c_int32), ("capacity_factor", C.c_double)]
+
+
+class _Tensors(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in
+                ("x", "w_router", "b_router", "sel_bias", "w1", "b1", "w3", "w2", "b2",
+                 "sw1", "sw3", "sw2")]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            P = C.c_void_p
+            L.orc_num_threads.restype = C.c_int
+            L.orc_exp32.restype = C.c_float
+            L.orc_exp32.argtypes = [C.c_float]
+            L.orc_sigmoid32.restype = C.c_float
+            L.orc_sigmoid32.argtypes = [C.c_float]
+            L.orc_round_bf16.restype = C.c_double
+            L.orc_round_bf16.argtypes = [C.c_double]
+            L.orc_gelu.restype = C.c_double
+            L.orc_gelu.argtypes = [C.c_double]
+            L.orc_silu.restype = C.c_double
+            L.orc_silu.argtypes = [C.c_double]
+            L.orc_capacity.restype = C.c_int64
+            L.orc_capacity.argtypes = [P]
+            L.orc_router_logits.argtypes = [P, P, P]
+            L.orc_route.argtypes = [P, P, P, P, P, P, P]
+            L.orc_dispatch.argtypes = [P] * 7
+            L.orc_expert_row.argtypes = [P, P, C.c_int64, P, P]
+            L.orc_forward_tokens.argtypes = [P, P, P, P, P, P, C.c_int64, P]
+            L.orc_dense_all.argtypes = [P] * 7
+            L.orc_stats.argtypes = [P] * 8
+            L.orc_bias_update.argtypes = [P, P, P, C.c_float]
+            L.orc_param_counts.argtypes = [C.c_int64] * 4 + [C.c_int, P]
+            _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    return lib().orc_num_threads()
+
+
+def _cfg(w) -> _Cfg:
+    return _Cfg(T=w.T, d=w.d, E=w.E, k=w.k, F=w.F, score_fn=w.score_fn, activation=w.activation,
+                renormalize=int(w.renormalize), drop_tokens=int(w.drop_tokens),
+                min_capacity=w.min_capacity, num_shared=w.num_shared, residual=int(w.residual),
+                dtype=w.dtype, capacity_factor=float(np.float32(w.capacity_factor)))
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _tensors(inp: Dict[str, np.ndarray]) -> _Tensors:
+    g = inp.get
+    return _Tensors(x=_p(g("x")), w_router=_p(g("w_router")), b_router=_p(g("b_router")),
+                    sel_bias=_p(g("sel_bias")), w1=_p(g("w1")), b1=_p(g("b1")), w3=_p(g("w3")),
+                    w2=_p(g("w2")), b2=_p(g("b2")), sw1=_p(g("shared_w1")),
+                    sw3=_p(g("shared_w3")), sw2=_p(g("shared_w2")))
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+# ---------------------------------------------------------------- steps
+def exp32(a: float) -> float:
+    return lib().orc_exp32(float(a))
+
+
+def sigmoid32(a: float) -> float:
+    return lib().orc_sigmoid32(float(a))
+
+
+def round_bf16(v: float) -> float:
+    return lib().orc_round_bf16(float(v))
+
+
+def gelu(v: float) -> float:
+    return lib().orc_gelu(float(v))
+
+
+def silu(v: float) -> float:
+    return lib().orc_silu(float(v))
+
+
+def capacity(w) -> int:
+    c = _cfg(w)
+    return int(lib().orc_capacity(C.byref(c)))
+
+
+def router_logits(w, inp) -> np.ndarray:
+    c, tn = _cfg(w), _tensors(inp)
+    out = np.empty((w.T, w.E), np.float32)
+    lib().orc_router_logits(C.byref(c), C.byref(tn), out.ctypes.data)
+    return out
+
+
+def route(w, logits: np.ndarray, sel_bias: Optional[np.ndarray] = None):
+    """-> dict(idx [T,k] int32, gate [T,k] f64, lse [T] f64, prob_sum [E] f64)"""
+    c = _cfg(w)
+    logits = _c(logits, np.float32)
+    sb = None if sel_bias is None else _c(sel_bias, np.float32)
+    idx = np.empty((w.T, w.k), np.int32)
+    gate = np.empty((w.T, w.k), np.float64)
+    lse = np.empty(w.T, np.float64)
+    ps = np.empty(w.E, np.float64)
+    lib().orc_route(C.byref(c), logits.ctypes.data, _p(sb), idx.ctypes.data, gate.ctypes.data,
+                    lse.ctypes.data, ps.ctypes.data)
+    return dict(idx=idx, gate=gate, lse=lse, prob_sum=ps)
+
+
+def dispatch(w, idx: np.ndarray):
+    """-> dict(counts, kept [E], offsets [E+1], perm [S], inv [S]) all int32"""
+    c = _cfg(w)
+    idx = _c(idx, np.int32)
+    S = w.T * w.k
+    counts = np.empty(w.E, np.int32)
+    kept = np.empty(w.E, np.int32)
+    offsets = np.empty(w.E + 1, np.int32)
+    perm = np.empty(max(S, 1), np.int32)[:S]
+    inv = np.empty(max(S, 1), np.int32)[:S]
+    lib().orc_dispatch(C.byref(c), idx.ctypes.data, counts.ctypes.data, kept.ctypes.data,
+                       offsets.ctypes.data, perm.ctypes.data, inv.ctypes.data)
+    return dict(counts=counts, kept=kept, offsets=offsets, perm=perm, inv=inv)
+
+
+def expert_row(w, inp, e: int, xrow: np.ndarray) -> np.ndarray:
+    c, tn = _cfg(w), _tensors(inp)
+    xv = _c(xrow, np.float64)
+    y = np.empty(w.d, np.float64)
+    lib().orc_expert_row(C.byref(c), C.byref(tn), int(e), xv.ctypes.data, y.ctypes.data)
+    return y
+
+
+def forward_tokens(w, inp, idx, gate, inv, tokens) -> np.ndarray:
+    c, tn = _cfg(w), _tensors(inp)
+    idx = _c(idx, np.int32)
+    gate = _c(gate, np.float64)
+    inv = None if inv is None else _c(inv, np.int32)
+    tokens = _c(tokens, np.int64)
+    out = np.empty((len(tokens), w.d), np.float64)
+    lib().orc_forward_tokens(C.byref(c), C.byref(tn), idx.ctypes.data, gate.ctypes.data, _p(inv),
+                             tokens.ctypes.data, len(tokens), out.ctypes.data)
+    return out
+
+
+def dense_all(w, inp, idx, gate, inv):
+    """Brute force: (all-experts tensor [T,E,d], layer output [T,d])."""
+    c, tn = _cfg(w), _tensors(inp)
+    idx = _c(idx, np.int32)
+    gate = _c(gate, np.float64)
+    inv = None if inv is None else _c(inv, np.int32)
+    allv = np.empty((w.T, w.E, w.d), np.float64)
+    out = np.empty((w.T, w.d), np.float64)
+    lib().orc_dense_all(C.byref(c), C.byref(tn), idx.ctypes.data, gate.ctypes.data, _p(inv),
+                        allv.ctypes.data, out.ctypes.data)
+    return allv, out
+
+
+def stats(w, counts, kept, prob_sum, lse):
+    """-> dict(f, P, aux, z, dropped, imbalance, utilization, drop_rate)"""
+    c = _cfg(w)
+    counts = _c(counts, np.int32)
+    kept = _c(kept, np.int32)
+    prob_sum = _c(prob_sum, np.float64)
+    lse = _c(lse, np.float64)
+    f = np.empty(w.E, np.float64)
+    P = np.empty(w.E, np.float64)
+    s = np.empty(6, np.float64)
+    lib().orc_stats(C.byref(c), counts.ctypes.data, kept.ctypes.data, prob_sum.ctypes.data,
+                    lse.ctypes.data, f.ctypes.data, P.ctypes.data, s.ctypes.data)
+    return dict(f=f, P=P, aux=s[0], z=s[1], dropped=int(s[2]), imbalance=s[3],
+                utilization=s[4], drop_rate=s[5])
+
+
+def bias_update(w, counts, bias, gamma: float) -> np.ndarray:
+    c = _cfg(w)
+    counts = _c(counts, np.int32)
+    b = np.array(bias, dtype=np.float32, copy=True)
+    lib().orc_bias_update(C.byref(c), counts.ctypes.data, b.ctypes.data, float(gamma))
+    return b
+
+
+def param_counts(d: int, F: int, E: int, k: int, gated: bool):
+    out = np.empty(4, np.int64)
+    lib().orc_param_counts(d, F, E, k, int(gated), out.ctypes.data)
+    return dict(expert=int(out[0]), router=int(out[1]), total=int(out[2]), active=int(out[3]))
+
+
+def layer(w, inp, tokens=None):
+    """Whole reference layer: routing for every token, outputs for `tokens`
+    (all tokens when None).  Returns a dict of every intermediate."""
+    logits = router_logits(w, inp)
+    r = route(w, logits, inp.get("sel_bias"))
+    dsp = dispatch(w, r["idx"])
+    st = stats(w, dsp["counts"], dsp["kept"], r["prob_sum"], r["lse"])
+    if tokens is None:
+        tokens = np.arange(w.T, dtype=np.int64)
+    out = forward_tokens(w, inp, r["idx"], r["gate"], dsp["inv"], tokens)
+    return dict(logits=logits, tokens=np.asarray(tokens), out=out, **r, **dsp, stats=st)
