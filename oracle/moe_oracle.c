@@ -188,6 +188,16 @@ float orc_sigmoid32(float x) {
     return 1.0f / den;
 }
 
+/* selection keys of sigmoid routing for a [T, E] block of logits */
+void orc_sigmoid_keys(const float *logits, const float *sel_bias, int64_t T, int64_t E, float *keys) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t e = 0; e < E; ++e) {
+            float s = orc_sigmoid32(logits[t * E + e]);
+            float b = sel_bias ? sel_bias[e] : 0.0f;
+            keys[t * E + e] = s + b;
+        }
+}
+
 /* ------------------------------------------------------------------ */
 /* step 1: router logits                                                */
 /* ------------------------------------------------------------------ */
@@ -388,6 +398,25 @@ void orc_expert_row(const orc_cfg *c, const orc_tensors *w, int64_t e, const dou
     double *h = (double *)malloc(sizeof(double) * (size_t)c->F);
     expert_row(c, w->w1, w->b1, w->w3, w->w2, w->b2, e, xv, h, y);
     free(h);
+}
+
+/* Several (expert, row) evaluations in parallel: y[i] = E_{experts[i]}(x[i]);
+ * experts[i] < 0 selects shared expert -experts[i]-1.  x is fp64 [n, d]. */
+void orc_expert_rows(const orc_cfg *c, const orc_tensors *w, int64_t n, const int32_t *experts,
+                     const double *x, double *y) {
+#pragma omp parallel
+    {
+        double *h = (double *)malloc(sizeof(double) * (size_t)c->F);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n; ++i) {
+            const int32_t e = experts[i];
+            if (e >= 0)
+                expert_row(c, w->w1, w->b1, w->w3, w->w2, w->b2, e, x + i * c->d, h, y + i * c->d);
+            else
+                expert_row(c, w->sw1, NULL, w->sw3, w->sw2, NULL, -e - 1, x + i * c->d, h, y + i * c->d);
+        }
+        free(h);
+    }
 }
 
 /*

@@ -84,6 +84,8 @@ def lib():
             L.orc_stats.argtypes = [P] * 8
             L.orc_bias_update.argtypes = [P, P, P, C.c_float]
             L.orc_param_counts.argtypes = [C.c_int64] * 4 + [C.c_int, P]
+            L.orc_sigmoid_keys.argtypes = [P, P, C.c_int64, C.c_int64, P]
+            L.orc_expert_rows.argtypes = [P, P, C.c_int64, P, P, P]
             _lib = L
     return _lib
 
@@ -122,6 +124,15 @@ def exp32(a: float) -> float:
 
 def sigmoid32(a: float) -> float:
     return lib().orc_sigmoid32(float(a))
+
+
+def sigmoid_keys(logits: np.ndarray, sel_bias: Optional[np.ndarray]) -> np.ndarray:
+    """fp32 selection keys sigmoid32(logit) + b_e of a [T, E] logit block."""
+    lg = _c(logits, np.float32)
+    sb = None if sel_bias is None else _c(sel_bias, np.float32)
+    out = np.empty_like(lg)
+    lib().orc_sigmoid_keys(lg.ctypes.data, _p(sb), lg.shape[0], lg.shape[1], out.ctypes.data)
+    return out
 
 
 def round_bf16(v: float) -> float:
@@ -182,6 +193,17 @@ def expert_row(w, inp, e: int, xrow: np.ndarray) -> np.ndarray:
     xv = _c(xrow, np.float64)
     y = np.empty(w.d, np.float64)
     lib().orc_expert_row(C.byref(c), C.byref(tn), int(e), xv.ctypes.data, y.ctypes.data)
+    return y
+
+
+def expert_rows(w, inp, experts, xrows) -> np.ndarray:
+    """y[i] = E_{experts[i]}(xrows[i]) in parallel; a negative expert id -s-1
+    selects shared expert s."""
+    c, tn = _cfg(w), _tensors(inp)
+    ex = _c(experts, np.int32)
+    xv = _c(xrows, np.float64)
+    y = np.empty((len(ex), w.d), np.float64)
+    lib().orc_expert_rows(C.byref(c), C.byref(tn), len(ex), ex.ctypes.data, xv.ctypes.data, y.ctypes.data)
     return y
 
 

@@ -1,1 +1,228 @@
-"""B300-native forward of a token-choice top-k Mixture-of-Experts FFN layer."""
+"""B300-native (sm_103a) forward of a token-choice top-k Mixture-of-Experts
+FFN layer.
+
+The functions below carry the names of the C ABI in ``include/moe_b300.h``
+and only marshal arguments: torch CUDA tensors become device pointers, the
+current torch stream becomes the launch stream, and a non-zero status
+becomes a ``MoEError``.  Every step of the layer runs in the CUDA library
+``libmoe_b300.so`` (build it with ``python -m
+sparse_mixture_experts_60_b300.build``); nothing here computes.
+
+``MoELayer`` is a convenience owner of weights, workspace and intermediate
+buffers (allocated with torch) around ``moe_forward``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Dict, Optional
+
+from ._lib import (MOE_WS_EXPERT_FFN, MOE_WS_FORWARD, MOE_WS_PERMUTE, MOE_WS_ROUTE,  # noqa: F401
+                   MOE_WS_SHARED_FFN, MoEConfig, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
+                   last_error, lib)
+
+SOFTMAX, SIGMOID = 0, 1
+GELU, RELU, SWIGLU = 0, 1, 2
+F32, BF16 = 0, 1
+
+
+def make_config(num_tokens: int, d_model: int, num_experts: int, top_k: int, d_ff: int, *,
+                score_fn: int = SOFTMAX, activation: int = GELU, dtype: int = BF16,
+                renormalize: bool = True, drop_tokens: bool = False, min_capacity: int = 4,
+                num_shared: int = 0, residual: bool = False, capacity_factor: float = 1.0) -> MoEConfig:
+    return MoEConfig(num_tokens=num_tokens, d_model=d_model, num_experts=num_experts, top_k=top_k,
+                     d_ff=d_ff, score_fn=score_fn, activation=activation, dtype=dtype,
+                     renormalize=int(renormalize), drop_tokens=int(drop_tokens),
+                     min_capacity=min_capacity, num_shared=num_shared, residual=int(residual),
+                     capacity_factor=capacity_factor)
+
+
+def config_for(w) -> MoEConfig:
+    """MoEConfig of a layer description with the attributes T d E k F score_fn
+    activation dtype renormalize drop_tokens min_capacity num_shared residual
+    capacity_factor (for example a ``workloads.Workload``)."""
+    return make_config(w.T, w.d, w.E, w.k, w.F, score_fn=w.score_fn, activation=w.activation,
+                       dtype=w.dtype, renormalize=w.renormalize, drop_tokens=w.drop_tokens,
+                       min_capacity=w.min_capacity, num_shared=w.num_shared, residual=w.residual,
+                       capacity_factor=w.capacity_factor)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ws(ws):
+    if ws is None:
+        return None, 0
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def moe_workspace_size(cfg: MoEConfig, which: int = MOE_WS_FORWARD) -> int:
+    n = C.c_size_t(0)
+    check(lib().moe_workspace_size(C.byref(cfg), which, C.byref(n)))
+    return n.value
+
+
+def moe_route(cfg, x, w_router, b_router, sel_bias, logits, topk_idx, topk_w, lse, prob_mean, counts,
+              ws, stream=None) -> None:
+    p, n = _ws(ws)
+    check(lib().moe_route(C.byref(cfg), _ptr(x), _ptr(w_router), _ptr(b_router), _ptr(sel_bias),
+                          _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(lse), _ptr(prob_mean),
+                          _ptr(counts), p, n, _stream(stream)))
+
+
+def moe_route_from_logits(cfg, logits, sel_bias, topk_idx, topk_w, lse, prob_mean, counts, ws,
+                          stream=None) -> None:
+    p, n = _ws(ws)
+    check(lib().moe_route_from_logits(C.byref(cfg), _ptr(logits), _ptr(sel_bias), _ptr(topk_idx),
+                                      _ptr(topk_w), _ptr(lse), _ptr(prob_mean), _ptr(counts), p, n,
+                                      _stream(stream)))
+
+
+def moe_permute(cfg, x, topk_idx, counts, kept, offsets, perm, inv, x_perm, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    check(lib().moe_permute(C.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(kept),
+                            _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm), p, n, _stream(stream)))
+
+
+def moe_expert_ffn(cfg, x_perm, offsets, w1, b1, w3, w2, b2, y_perm, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    check(lib().moe_expert_ffn(C.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(w1), _ptr(b1), _ptr(w3),
+                               _ptr(w2), _ptr(b2), _ptr(y_perm), p, n, _stream(stream)))
+
+
+def moe_shared_ffn(cfg, x, shared_w1, shared_w3, shared_w2, z, ws, stream=None) -> None:
+    p, n = _ws(ws)
+    check(lib().moe_shared_ffn(C.byref(cfg), _ptr(x), _ptr(shared_w1), _ptr(shared_w3),
+                               _ptr(shared_w2), _ptr(z), p, n, _stream(stream)))
+
+
+def moe_combine(cfg, y_perm, inv, topk_w, shared_out, x, out, stream=None) -> None:
+    check(lib().moe_combine(C.byref(cfg), _ptr(y_perm), _ptr(inv), _ptr(topk_w), _ptr(shared_out),
+                            _ptr(x), _ptr(out), _stream(stream)))
+
+
+def moe_stats(cfg, counts, kept, prob_mean, lse, f, stats, stream=None) -> None:
+    """``stats`` is a CUDA buffer of at least ``ctypes.sizeof(MoEStats)`` bytes."""
+    check(lib().moe_stats(C.byref(cfg), _ptr(counts), _ptr(kept), _ptr(prob_mean), _ptr(lse), _ptr(f),
+                          _ptr(stats), _stream(stream)))
+
+
+def moe_bias_update(cfg, counts, sel_bias, gamma: float, stream=None) -> None:
+    check(lib().moe_bias_update(C.byref(cfg), _ptr(counts), _ptr(sel_bias), float(gamma),
+                                _stream(stream)))
+
+
+def weights_struct(w: Dict) -> MoEWeights:
+    g = w.get
+    return MoEWeights(w_router=_ptr(g("w_router")), b_router=_ptr(g("b_router")), w1=_ptr(g("w1")),
+                      b1=_ptr(g("b1")), w3=_ptr(g("w3")), w2=_ptr(g("w2")), b2=_ptr(g("b2")),
+                      shared_w1=_ptr(g("shared_w1")), shared_w3=_ptr(g("shared_w3")),
+                      shared_w2=_ptr(g("shared_w2")))
+
+
+def io_struct(io: Optional[Dict]) -> Optional[MoEForwardIO]:
+    if io is None:
+        return None
+    return MoEForwardIO(**{k: _ptr(io.get(k)) for k, _ in MoEForwardIO._fields_})
+
+
+def moe_forward(cfg, weights: Dict, x, sel_bias, out, io: Optional[Dict], ws, stream=None) -> None:
+    """``weights``: dict of CUDA tensors keyed like ``MoEWeights`` fields;
+    ``io``: dict of optional intermediate output tensors keyed like
+    ``MoEForwardIO`` fields (missing keys stay in the workspace)."""
+    p, n = _ws(ws)
+    wst = weights_struct(weights)
+    ios = io_struct(io)
+    check(lib().moe_forward(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(sel_bias), _ptr(out),
+                            C.byref(ios) if ios is not None else None, p, n, _stream(stream)))
+
+
+def moe_check_device_error() -> int:
+    code = C.c_int32(0)
+    check(lib().moe_check_device_error(C.byref(code)))
+    return code.value
+
+
+def stats_from_buffer(buf) -> Dict:
+    """Decode a CUDA (or CPU) byte tensor holding one moe_stats_t."""
+    raw = bytes(buf.detach().cpu().numpy().tobytes())[:C.sizeof(MoEStats)]
+    s = MoEStats.from_buffer_copy(raw)
+    return {k: getattr(s, k) for k, _ in MoEStats._fields_}
+
+
+class MoELayer:
+    """Owner of one layer's device weights, workspace and intermediate
+    buffers.  ``weights``: dict of CUDA tensors (``w_router``, ``b_router``,
+    ``w1``, ``b1``, ``w3``, ``w2``, ``b2``, ``shared_w1``, ``shared_w3``,
+    ``shared_w2``), ``sel_bias``: CUDA fp32 [E] for sigmoid scoring."""
+
+    def __init__(self, cfg: MoEConfig, weights: Dict, sel_bias=None, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.weights = weights
+        self.sel_bias = sel_bias
+        self.device = torch.device(device)
+        T, E, k = cfg.num_tokens, cfg.num_experts, cfg.top_k
+        dev = self.device
+        self.ws = torch.empty(max(moe_workspace_size(cfg), 1), dtype=torch.uint8, device=dev)
+        i32, f32 = torch.int32, torch.float32
+        self.io = dict(logits=torch.empty(T, E, dtype=f32, device=dev),
+                       topk_idx=torch.empty(T, k, dtype=i32, device=dev),
+                       topk_w=torch.empty(T, k, dtype=f32, device=dev),
+                       lse=torch.empty(T, dtype=f32, device=dev),
+                       prob_mean=torch.empty(E, dtype=f32, device=dev),
+                       counts=torch.empty(E, dtype=i32, device=dev),
+                       kept=torch.empty(E, dtype=i32, device=dev),
+                       offsets=torch.empty(E + 1, dtype=i32, device=dev),
+                       perm=torch.empty(T * k, dtype=i32, device=dev),
+                       inv=torch.empty(T * k, dtype=i32, device=dev),
+                       f=torch.empty(E, dtype=f32, device=dev),
+                       stats=torch.empty(C.sizeof(MoEStats), dtype=torch.uint8, device=dev))
+
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.cfg.dtype == F32 else torch.bfloat16
+
+    def forward(self, x, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(self.cfg.num_tokens, self.cfg.d_model, dtype=self.out_dtype(),
+                              device=self.device)
+        moe_forward(self.cfg, self.weights, x, self.sel_bias, out, self.io, self.ws, stream)
+        return out
+
+    def forward_host(self, x_host, out_host, x_dev=None, out_dev=None, stream=None):
+        """End-to-end call from host buffers (pinned for overlap): copy x in,
+        run the layer, copy out back; asynchronous on the stream."""
+        import torch
+        st = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(st):
+            if x_dev is None:
+                x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=self.device)
+            x_dev.copy_(x_host, non_blocking=True)
+            out_dev = self.forward(x_dev, out_dev, st)
+            out_host.copy_(out_dev, non_blocking=True)
+        return out_host
+
+    def stats(self) -> Dict:
+        return stats_from_buffer(self.io["stats"])
+
+
+def bias_update(layer: MoELayer, gamma: float, stream=None) -> None:
+    """Aux-loss-free balancing step after ``layer.forward``."""
+    moe_bias_update(layer.cfg, layer.io["counts"], layer.sel_bias, gamma, stream)

@@ -1,0 +1,193 @@
+// Gate-weighted combine back to token order, balance statistics, and the
+// aux-loss-free bias update.
+//
+// Pages: "MoE Training: Mixture of Experts" (Quick Start MoELayer
+// output[mask] += score * expert_output; Load Balancing: auxiliary loss
+// N sum f_i P_i and router z-loss mean(logsumexp^2)); "Mixture of Experts
+// (MoE) From Scratch to DeepSeek V3" (output y = sum Gate_i E_i(x) + x;
+// shared experts; bias b_i lowered for an overloaded expert and raised for
+// an idle one); "MoE Training Guide" (Monitoring: imbalance, utilisation,
+// drop rate).
+#include <math.h>
+#include <stdint.h>
+
+#include "moe_b300.h"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// One warp per token; each lane owns V consecutive output columns per step.
+//   out = sum_j w_j * y[inv_j]  (j ascending, dropped slots skipped)
+//         + z (shared expert) + x (residual), in fp32, stored in dtype.
+template <bool BF16>
+__global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, const float *__restrict__ y,
+                                                      const int32_t *__restrict__ inv,
+                                                      const float *__restrict__ topk_w,
+                                                      const float *__restrict__ z, const void *__restrict__ x,
+                                                      void *__restrict__ out) {
+    constexpr int V = BF16 ? 8 : 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int my_r = lane < k ? inv[t * k + lane] : -1;
+    const float my_w = lane < k ? topk_w[t * k + lane] : 0.0f;
+    int rows[kMaxTopK];
+    float wts[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        rows[j] = __shfl_sync(kFull, my_r, j);
+        wts[j] = __shfl_sync(kFull, my_w, j);
+    }
+    const int nchunk = d / V;
+    for (int c = lane; c < nchunk; c += 32) {
+        float acc[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k && rows[j] >= 0) {
+                const float4 *src = reinterpret_cast<const float4 *>(y + (int64_t)rows[j] * d) + c * (V / 4);
+#pragma unroll
+                for (int h = 0; h < V / 4; ++h) {
+                    const float4 u = __ldg(src + h);
+                    acc[4 * h + 0] = fmaf(wts[j], u.x, acc[4 * h + 0]);
+                    acc[4 * h + 1] = fmaf(wts[j], u.y, acc[4 * h + 1]);
+                    acc[4 * h + 2] = fmaf(wts[j], u.z, acc[4 * h + 2]);
+                    acc[4 * h + 3] = fmaf(wts[j], u.w, acc[4 * h + 3]);
+                }
+            }
+        }
+        if (z) {
+            const float4 *src = reinterpret_cast<const float4 *>(z + t * d) + c * (V / 4);
+#pragma unroll
+            for (int h = 0; h < V / 4; ++h) {
+                const float4 u = __ldg(src + h);
+                acc[4 * h + 0] += u.x;
+                acc[4 * h + 1] += u.y;
+                acc[4 * h + 2] += u.z;
+                acc[4 * h + 3] += u.w;
+            }
+        }
+        if (BF16) {
+            if (x) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(x) + t * d) + c);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    acc[2 * h] += __uint_as_float(w[h] << 16);
+                    acc[2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+                o[h] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + t * d)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            if (x) {
+                const float4 u = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + t * d) + c);
+                acc[0] += u.x;
+                acc[1] += u.y;
+                acc[2] += u.z;
+                acc[3] += u.w;
+            }
+            reinterpret_cast<float4 *>(static_cast<float *>(out) + t * d)[c] =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
+    }
+}
+
+template <typename T, typename Op>
+__device__ T block_reduce(T v, T *sm, Op op) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(kFull, v, o));
+    __syncthreads();
+    if (lane == 0) sm[warp] = v;
+    __syncthreads();
+    T r = sm[0];
+    for (int w = 1; w < nw; ++w) r = op(r, sm[w]);
+    return r;
+}
+
+struct AddD { __device__ double operator()(double a, double b) const { return a + b; } };
+struct AddL { __device__ long long operator()(long long a, long long b) const { return a + b; } };
+struct MaxL { __device__ long long operator()(long long a, long long b) const { return a > b ? a : b; } };
+struct MinL { __device__ long long operator()(long long a, long long b) const { return a < b ? a : b; } };
+
+__global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
+    __shared__ double sd[32];
+    __shared__ long long sl[32];
+    const int64_t S = p.T * p.k;
+    double z = 0.0;
+    for (int64_t i = threadIdx.x; i < p.T; i += blockDim.x) z += (double)p.lse[i] * (double)p.lse[i];
+    z = block_reduce(z, sd, AddD());
+    double aux = 0.0;
+    long long dropped = 0, used = 0, kept_tot = 0, kmax = 0, kmin = 0x7fffffffffffffffLL;
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        const double f = S > 0 ? (double)p.counts[e] / (double)S : 0.0;
+        if (p.f) p.f[e] = (float)f;
+        aux += f * (double)p.prob_mean[e];
+        dropped += p.counts[e] - p.kept[e];
+        used += p.kept[e] > 0;
+        kept_tot += p.kept[e];
+        kmax = p.kept[e] > kmax ? p.kept[e] : kmax;
+        kmin = p.kept[e] < kmin ? p.kept[e] : kmin;
+    }
+    aux = block_reduce(aux, sd, AddD());
+    dropped = block_reduce(dropped, sl, AddL());
+    used = block_reduce(used, sl, AddL());
+    kept_tot = block_reduce(kept_tot, sl, AddL());
+    kmax = block_reduce(kmax, sl, MaxL());
+    kmin = block_reduce(kmin, sl, MinL());
+    if (threadIdx.x == 0) {
+        moe_stats_t st;
+        st.aux_loss = (float)((double)p.E * aux);
+        st.z_loss = p.T > 0 ? (float)(z / (double)p.T) : 0.0f;
+        st.imbalance = kmin > 0 ? (float)((double)kmax / (double)kmin) : INFINITY;
+        st.utilization = (float)((double)used / (double)p.E);
+        st.drop_rate = S > 0 ? (float)((double)dropped / (double)S) : 0.0f;
+        st.dropped = (int32_t)dropped;
+        st.capacity = p.drop ? (int32_t)p.cap : -1;
+        st.total_kept = (int32_t)kept_tot;
+        *static_cast<moe_stats_t *>(p.stats) = st;
+    }
+}
+
+__global__ void bias_update_kernel(int64_t S, int E, const int32_t *counts, float *b, float gamma) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const long long diff = (long long)S - (long long)E * counts[e];  // sign of S/E - counts_e
+    const float sg = diff > 0 ? 1.0f : (diff < 0 ? -1.0f : 0.0f);
+    b[e] = __fadd_rn(b[e], __fmul_rn(gamma, sg));
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_perm, const int32_t *inv,
+                           const float *topk_w, const float *shared_out, const void *x_res, void *out,
+                           cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)ceil_div(T, 8);
+    if (dtype == 1) combine_kernel<true><<<grid, 256, 0, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
+    else combine_kernel<false><<<grid, 256, 0, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const StatsParams &p, cudaStream_t s) {
+    stats_kernel<<<1, 1024, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bias_update(int64_t T, int E, int k, const int32_t *counts, float *bias, float gamma,
+                               cudaStream_t s) {
+    bias_update_kernel<<<(unsigned)ceil_div(E, 256), 256, 0, s>>>(T * k, E, counts, bias, gamma);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,602 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators, TMA loads) for the expert FFNs and the router of wide
+// layers.
+//
+//   out[r, n] = epilogue( sum_k A[r, k] * B[g * b_group_rows + n, k] )
+//
+// for every row r of group g (rows seg[g] .. seg[g+1]-1 of A).  A is the
+// permuted token matrix (experts' segments are contiguous) and B the stacked
+// expert weights in nn.Linear layout, so both operands are K-major.  The
+// epilogue adds the bias and applies GELU / ReLU, or for a gated (SwiGLU)
+// layer multiplies silu(A W1^T) by A W3^T; the two products share one MMA
+// (the B tile stacks BN/2 rows of W1 over BN/2 rows of W3, so accumulator
+// columns [0, BN/2) are the gate and [BN/2, BN) the up projection).
+//
+// Pages: "MoE Training: Mixture of Experts" (Quick Start expert Linear-GELU-
+// Linear); "moe_code.py" (Expert: ReLU FFN); the Mixtral parameter
+// arithmetic of the MoE technical survey (three-matrix SwiGLU expert).
+//
+// Structure: one persistent CTA per SM, 192 threads.
+//   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage,
+//               128-byte swizzle, completion on an mbarrier (expect_tx).
+//   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma
+//               (M=128, N=BN, K=16, bf16 -> fp32) per stage, tcgen05.commit
+//               frees the stage and, after the last K block, publishes the
+//               accumulator.
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time (warp w reads
+//               TMEM lanes 32*(w%4) ..), bias/activation in fp32, 16-byte
+//               stores; then releases the accumulator.
+// Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
+// the main loop of tile i+1.  Tiles are ordered group-major, then N-block,
+// then M-block, so the CTAs working at the same time share weight tiles.
+// Every wait is bounded: a wait that gives up raises the library's device
+// error flag and an abort flag in shared memory, every role leaves its
+// loop, copies and MMAs in flight are drained (again bounded) and TMEM is
+// released before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ device flag
+__device__ int32_t g_moe_device_error = 0;
+
+int32_t *device_error_flag() {
+    static int32_t *ptr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_moe_device_error) != cudaSuccess) return nullptr;
+        ptr[dev] = static_cast<int32_t *>(p);
+    }
+    return ptr[dev];
+}
+
+int num_sms() {
+    static int n[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!n[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev] = v > 0 ? v : 148;
+    }
+    return n[dev];
+}
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                 // one 128-byte swizzle atom of bf16
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static size_t smem_bytes(int G) {
+        return 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
+    }
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase parity.  Returns false when the CTA is aborting
+// (flag already set) or the limit ran out (then sets both flags).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                            int32_t *err) {
+    const uint64_t t0 = global_timer();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(err, 6);  // MOE_ERR_DEVICE_TIMEOUT
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, err);
+}
+// Wait bounded by time only (teardown: in-flight work must land first).
+__device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, uint64_t *bar, int32_t c0,
+                                            int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *holder, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
+// 8-row core-matrix groups 1024 bytes apart (SBO), version field 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;              // LBO (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;    // SBO
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+template <int M, int N>
+struct IDesc {
+    static constexpr uint32_t value =
+        (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+};
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 columns of fp32 from TMEM (one row per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ kernel
+struct Args {
+    const int32_t *seg;
+    int64_t a_rows;
+    int G, M, N, K, b_group_rows;
+    void *out;
+    int64_t ldo;
+    const bf16 *bias;
+    int64_t bias_stride;
+    int act;
+    int32_t *err;
+};
+
+struct Tile {
+    int g, row0, seg_end, n0;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const int *pre_s, int G, int bn_out) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre_s[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    const int rows = seg_s[lo + 1] - seg_s[lo];
+    const int mt = (rows + BM - 1) / BM;
+    const int local = tile - pre_s[lo];
+    const int nb = local / mt, mb = local - nb * mt;
+    Tile t;
+    t.g = lo;
+    t.row0 = seg_s[lo] + mb * BM;
+    t.seg_end = seg_s[lo + 1];
+    t.n0 = nb * bn_out;
+    return t;
+}
+
+__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
+
+template <int BN, bool GATED, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmB2, const Args args) {
+    using C = Cfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int BN_OUT = GATED ? BN / 2 : BN;
+    constexpr uint32_t IDESC = IDesc<BM, BN>::value;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * C::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t *full = bars;                 // [STAGES]
+    uint64_t *empty = bars + STAGES;       // [STAGES]
+    uint64_t *tfull = bars + 2 * STAGES;   // [2]
+    uint64_t *tempty = tfull + 2;          // [2]
+    uint64_t *drain = tempty + 2;          // [1]
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *consumed = abort_flag + 1;
+    int *seg_s = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+    int *pre_s = seg_s + (args.G + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = args.G;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (GATED) tma_prefetch_desc(&tmB2);
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+    for (int i = threadIdx.x; i <= G; i += kThreads)
+        seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
+    __syncthreads();
+    // tile prefix over groups: n_tiles * ceil(rows_g / BM)
+    const int n_tiles = (args.N + BN_OUT - 1) / BN_OUT;
+    volatile int *seg_bad = consumed + 1;
+    if (warp == 0) {
+        int carry = 0;
+        bool bad = seg_s[0] < 0 || (int64_t)seg_s[G] > args.a_rows;
+        for (int b = 0; b < G; b += 32) {
+            const int g = b + lane;
+            int v = 0;
+            if (g < G) {
+                const int rows = seg_s[g + 1] - seg_s[g];
+                bad |= rows < 0;
+                v = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (g < G) pre_s[g + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            pre_s[0] = 0;
+            *seg_bad = bad ? 1 : 0;
+            if (bad) atomicExch(args.err, 1);  // MOE_ERR_INVALID_ARG
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    // segments must be monotone and inside A; otherwise the kernel does nothing
+    const int total = *seg_bad ? 0 : pre_s[G];
+    const int num_kb = (args.K + BK - 1) / BK;
+    int issued = 0;  // producer: TMA stages issued
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const Tile tl = decode_tile(tile, seg_s, pre_s, G, BN_OUT);
+            const int brow = tl.g * args.b_group_rows + tl.n0;
+            bool ok = true;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, args.err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+                tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * BK, tl.row0);
+                if (GATED) {
+                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * BK, brow);
+                    tma_load_2d(sB + stage * C::B_BYTES + (BN / 2) * BK * 2, &tmB2, &full[stage], kb * BK, brow);
+                } else {
+                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * BK, brow);
+                }
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&full[stage], ph, abort_flag, args.err)) {
+                    ok = false;
+                    break;
+                }
+                *consumed = *consumed + 1;
+                tc_fence_after();
+                const uint64_t adesc = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
+                const uint64_t bdesc = sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                    // +32 bytes per K step inside the swizzle atom (encoded >> 4)
+                    umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
+                              (kb > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(&tfull[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const Tile tl = decode_tile(tile, seg_s, pre_s, G, BN_OUT);
+            // tcgen05.ld below is warp-collective: leave only as a whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag, args.err))) break;
+            tc_fence_after();
+            const int grow = tl.row0 + row_in_tile;
+            const bool row_ok = grow < tl.seg_end;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN_OUT; c += 32) {
+                const int col = tl.n0 + c;
+                float v[32];
+                if (GATED) {
+                    float u[32];
+                    tmem_ld32(tbase + c, v);
+                    tmem_ld32(tbase + BN / 2 + c, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
+                } else {
+                    tmem_ld32(tbase + c, v);
+                    if (args.bias && col < args.N) {
+                        const uint4 *bp = reinterpret_cast<const uint4 *>(args.bias + (int64_t)tl.g * args.bias_stride + col);
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const uint4 b = __ldg(bp + qq);
+                            const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                v[qq * 8 + 2 * h] += __uint_as_float(w[h] << 16);
+                                v[qq * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                            }
+                        }
+                    }
+                    if (args.act == 1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                    } else if (args.act == 2) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+                    }
+                }
+                if (row_ok && col < args.N) {
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.out) + (int64_t)grow * args.ldo + col);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<bf16 *>(args.out) + (int64_t)grow * args.ldo + col);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * h], v[8 * i + 2 * h + 1]);
+                                w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                            }
+                            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    }
+    // ---------------------------------------------------- teardown
+    __syncthreads();  // every role has left its loop
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // copies issued but never consumed must land before the CTA exits
+        for (int i = *consumed; i < issued; ++i)
+            if (!mbar_wait_drain(&full[i % STAGES], (uint32_t)((i / STAGES) & 1))) break;
+    }
+    if (warp == 1 && lane == 0) {
+        // every MMA issued by this CTA has completed once the drain barrier flips
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] (row-major), box [box_rows, 64], 128-byte swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool GATED, bool OUT_F32>
+cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
+    using C = Cfg<BN>;
+    constexpr int BN_B = GATED ? BN / 2 : BN;   // rows per TMA box of B
+    CUtensorMap ta, tb, tb2;
+    if (!make_tmap(&ta, p.A, (uint64_t)p.K, (uint64_t)p.a_rows, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, p.B, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) return cudaErrorInvalidValue;
+    if (GATED) {
+        if (!make_tmap(&tb2, p.B2, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) return cudaErrorInvalidValue;
+    } else {
+        tb2 = tb;
+    }
+    Args a;
+    a.seg = p.seg;
+    a.a_rows = p.a_rows;
+    a.G = p.seg ? p.G : 1;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.b_group_rows = p.b_group_rows;
+    a.out = p.out;
+    a.ldo = p.ldo;
+    a.bias = p.bias;
+    a.bias_stride = p.bias_stride;
+    a.act = p.act;
+    a.err = device_error_flag();
+    if (!a.err) return cudaErrorUnknown;
+    const size_t smem = C::smem_bytes(a.G);
+    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<num_sms(), kThreads, smem, s>>>(ta, tb, tb2, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool grouped_gemm_supported(int N, int K, int gated) {
+    (void)gated;
+    return N > 0 && K > 0 && N % 32 == 0 && K % 8 == 0;
+}
+
+cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
+    if (!grouped_gemm_supported(p.N, p.K, p.gated)) return cudaErrorInvalidValue;
+    if (p.gated) {
+        return p.out_f32 ? launch_t<256, true, true>(p, s) : launch_t<256, true, false>(p, s);
+    }
+    if (p.out_f32) {
+        if (p.N <= 64) return launch_t<64, false, true>(p, s);
+        if (p.N <= 128) return launch_t<128, false, true>(p, s);
+        return launch_t<256, false, true>(p, s);
+    }
+    return launch_t<256, false, false>(p, s);
+}
+
+}  // namespace moe

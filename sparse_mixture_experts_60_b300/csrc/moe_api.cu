@@ -1,0 +1,569 @@
+// C ABI of the MoE-layer forward: argument validation, workspace layout and
+// the launch sequence.  Every step of the layer runs in this library's own
+// kernels; the host code only checks arguments, carves the caller's
+// workspace, encodes TMA descriptors and launches on the caller's stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_b300.h"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+moe_status_t fail(moe_status_t st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+moe_status_t cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MOE_OK;
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int elem_bytes(const moe_config_t *c) { return c->dtype == MOE_DTYPE_F32 ? 4 : 2; }
+
+moe_status_t check_cfg(const moe_config_t *c) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+    if (c->num_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "num_tokens < 0");
+    if (c->num_experts < 1 || c->num_experts > kMaxExperts)
+        return fail(MOE_ERR_INVALID_ARG, "num_experts must be in [1, %d]", kMaxExperts);
+    if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > kMaxTopK)
+        return fail(MOE_ERR_INVALID_ARG, "top_k must be in [1, min(num_experts, %d)]", kMaxTopK);
+    if (c->d_model < 1 || c->d_ff < 1) return fail(MOE_ERR_INVALID_ARG, "d_model and d_ff must be >= 1");
+    if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID)
+        return fail(MOE_ERR_INVALID_ARG, "bad score_fn %d", c->score_fn);
+    if (c->activation < MOE_ACT_GELU || c->activation > MOE_ACT_SWIGLU)
+        return fail(MOE_ERR_INVALID_ARG, "bad activation %d", c->activation);
+    if (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16)
+        return fail(MOE_ERR_INVALID_ARG, "bad dtype %d", c->dtype);
+    if (c->num_shared != 0 && c->num_shared != 1) return fail(MOE_ERR_UNSUPPORTED, "num_shared must be 0 or 1");
+    if (c->drop_tokens && !(c->capacity_factor > 0.0f && isfinite(c->capacity_factor)))
+        return fail(MOE_ERR_INVALID_ARG, "capacity_factor must be finite and > 0 with drop_tokens");
+    if (c->min_capacity < 0) return fail(MOE_ERR_INVALID_ARG, "min_capacity < 0");
+    if (c->num_tokens * (int64_t)c->top_k > INT32_MAX)
+        return fail(MOE_ERR_UNSUPPORTED, "num_tokens * top_k must fit in int32");
+    if (c->dtype == MOE_DTYPE_BF16 && (c->d_model % 64 || c->d_ff % 64))
+        return fail(MOE_ERR_UNSUPPORTED, "bf16 layers need d_model and d_ff multiples of 64");
+    if (c->dtype == MOE_DTYPE_F32 && (c->d_model % 4 || c->d_ff % 4))
+        return fail(MOE_ERR_UNSUPPORTED, "fp32 layers need d_model and d_ff multiples of 4");
+    return MOE_OK;
+}
+
+int64_t capacity_of(const moe_config_t *c) {
+    const int64_t S = c->num_tokens * c->top_k;
+    if (!c->drop_tokens) return S;
+    const double v = ceil((double)c->num_tokens / (double)c->num_experts * (double)c->capacity_factor);
+    const int64_t cap = (int64_t)v;
+    return cap > c->min_capacity ? cap : (int64_t)c->min_capacity;
+}
+
+int64_t route_blocks(const moe_config_t *c) { return ceil_div(c->num_tokens, kRouteTokPerCta); }
+int64_t perm_chunks(const moe_config_t *c) { return ceil_div(c->num_tokens * c->top_k, kPermChunk); }
+
+size_t route_ws(const moe_config_t *c) {
+    return 2 * align256((size_t)route_blocks(c) * c->num_experts * 4);
+}
+size_t permute_ws(const moe_config_t *c) { return 2 * align256((size_t)perm_chunks(c) * c->num_experts * 4); }
+size_t ffn_ws(const moe_config_t *c) {
+    return align256((size_t)c->num_tokens * c->top_k * c->d_ff * elem_bytes(c));
+}
+size_t shared_ws(const moe_config_t *c) {
+    return c->num_shared ? align256((size_t)c->num_tokens * c->d_ff * elem_bytes(c)) : 0;
+}
+
+// Bump allocator over the caller's workspace.
+struct Carve {
+    uint8_t *base;
+    size_t used = 0;
+    template <typename T>
+    T *take(size_t bytes) {
+        T *p = reinterpret_cast<T *>(base + used);
+        used += align256(bytes);
+        return p;
+    }
+};
+
+size_t forward_ws(const moe_config_t *c) {
+    const size_t T = (size_t)c->num_tokens, E = (size_t)c->num_experts, S = T * c->top_k;
+    const size_t d = (size_t)c->d_model;
+    size_t n = route_ws(c) + permute_ws(c) + ffn_ws(c) + shared_ws(c);
+    n += align256(S * d * elem_bytes(c));                         // x_perm
+    n += align256(S * d * 4);                                     // y_perm
+    if (c->num_shared) n += align256(T * d * 4);                  // z
+    n += align256(T * E * 4) + 4 * align256(S * 4) + align256(T * 4);  // logits, idx, w, perm, inv, lse
+    n += 4 * align256(E * 4) + align256((E + 1) * 4) + align256(sizeof(moe_stats_t));
+    return n;
+}
+
+// ------------------------------------------------------------------ step bodies (no validation)
+moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_router, const float *b_router,
+                        const float *sel_bias, float *logits, const float *logits_in, int32_t *topk_idx,
+                        float *topk_w, float *lse, float *prob_mean, int32_t *counts, void *ws,
+                        cudaStream_t s) {
+    Carve cv{static_cast<uint8_t *>(ws)};
+    const int64_t nblk = route_blocks(c);
+    float *part_prob = cv.take<float>((size_t)nblk * c->num_experts * 4);
+    int32_t *part_cnt = cv.take<int32_t>((size_t)nblk * c->num_experts * 4);
+    RouteParams p{};
+    p.T = c->num_tokens;
+    p.E = c->num_experts;
+    p.k = c->top_k;
+    p.d = c->d_model;
+    p.score_fn = c->score_fn;
+    p.renormalize = c->renormalize;
+    p.x = x;
+    p.w_router = w_router;
+    p.b_router = b_router;
+    p.sel_bias = sel_bias;
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.lse = lse;
+    p.part_prob = part_prob;
+    p.part_cnt = part_cnt;
+    cudaError_t e = cudaSuccess;
+    if (logits_in) {
+        p.logits = const_cast<float *>(logits_in);
+        p.logits_add_bias = 0;
+        e = launch_route_logits(p, s);
+    } else if (c->num_experts <= 32) {
+        p.logits = logits;
+        e = launch_router_fused(p, c->dtype, s);
+    } else {
+        p.logits = logits;
+        p.logits_add_bias = 1;
+        if (c->num_tokens > 0) {
+            if (c->dtype == MOE_DTYPE_BF16 && c->num_experts % 32 == 0) {
+                GemmProblem g{};
+                g.A = static_cast<const bf16 *>(x);
+                g.a_rows = c->num_tokens;
+                g.B = static_cast<const bf16 *>(w_router);
+                g.b_rows_total = c->num_experts;
+                g.b_group_rows = c->num_experts;
+                g.seg = nullptr;
+                g.G = 1;
+                g.M = (int)c->num_tokens;
+                g.N = c->num_experts;
+                g.K = c->d_model;
+                g.out = logits;
+                g.ldo = c->num_experts;
+                g.out_f32 = 1;
+                e = launch_grouped_gemm(g, s);
+            } else {
+                e = launch_router_logits_simt(p, c->dtype, s);
+            }
+        }
+        if (e == cudaSuccess) e = launch_route_logits(p, s);
+    }
+    if (e == cudaSuccess)
+        e = launch_route_reduce(part_prob, part_cnt, nblk, c->num_experts, c->num_tokens, prob_mean, counts, s);
+    return cuda_status(e, "moe_route launch");
+}
+
+moe_status_t permute_impl(const moe_config_t *c, const void *x, const int32_t *topk_idx, int32_t *counts,
+                          int32_t *kept, int32_t *offsets, int32_t *perm, int32_t *inv, void *x_perm,
+                          void *ws, cudaStream_t s) {
+    Carve cv{static_cast<uint8_t *>(ws)};
+    const int64_t nch = perm_chunks(c);
+    PermuteParams p{};
+    p.T = c->num_tokens;
+    p.E = c->num_experts;
+    p.k = c->top_k;
+    p.d = c->d_model;
+    p.dtype = c->dtype;
+    p.cap = capacity_of(c);
+    p.x = x;
+    p.topk_idx = topk_idx;
+    p.counts = counts;
+    p.kept = kept;
+    p.offsets = offsets;
+    p.perm = perm;
+    p.inv = inv;
+    p.x_perm = x_perm;
+    p.hist = cv.take<int32_t>((size_t)nch * c->num_experts * 4);
+    p.base = cv.take<int32_t>((size_t)nch * c->num_experts * 4);
+    return cuda_status(launch_permute(p, s), "moe_permute launch");
+}
+
+// Two-layer FFN over row groups (routed: seg = offsets, G = E; shared: seg = null).
+moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, const int32_t *seg, int G, int M,
+                      const void *w1, const void *b1, const void *w3, const void *w2, const void *b2, void *H,
+                      float *y, cudaStream_t s) {
+    const int d = c->d_model, F = c->d_ff;
+    const int gated = c->activation == MOE_ACT_SWIGLU;
+    const int act = c->activation == MOE_ACT_GELU ? 1 : (c->activation == MOE_ACT_RELU ? 2 : 0);
+    if (a_rows == 0) return MOE_OK;
+    cudaError_t e;
+    if (c->dtype == MOE_DTYPE_BF16) {
+        GemmProblem g1{};
+        g1.A = static_cast<const bf16 *>(A);
+        g1.a_rows = a_rows;
+        g1.B = static_cast<const bf16 *>(w1);
+        g1.B2 = static_cast<const bf16 *>(w3);
+        g1.b_rows_total = (int64_t)G * F;
+        g1.b_group_rows = F;
+        g1.seg = seg;
+        g1.G = G;
+        g1.M = M;
+        g1.N = F;
+        g1.K = d;
+        g1.out = H;
+        g1.ldo = F;
+        g1.out_f32 = 0;
+        g1.bias = gated ? nullptr : static_cast<const bf16 *>(b1);
+        g1.bias_stride = F;
+        g1.act = act;
+        g1.gated = gated;
+        e = launch_grouped_gemm(g1, s);
+        if (e != cudaSuccess) return cuda_status(e, "expert FFN1 launch");
+        GemmProblem g2{};
+        g2.A = static_cast<const bf16 *>(H);
+        g2.a_rows = a_rows;
+        g2.B = static_cast<const bf16 *>(w2);
+        g2.b_rows_total = (int64_t)G * d;
+        g2.b_group_rows = d;
+        g2.seg = seg;
+        g2.G = G;
+        g2.M = M;
+        g2.N = d;
+        g2.K = F;
+        g2.out = y;
+        g2.ldo = d;
+        g2.out_f32 = 1;
+        g2.bias = gated ? nullptr : static_cast<const bf16 *>(b2);
+        g2.bias_stride = d;
+        g2.act = 0;
+        g2.gated = 0;
+        e = launch_grouped_gemm(g2, s);
+        return cuda_status(e, "expert FFN2 launch");
+    }
+    SimtProblem p1{};
+    p1.A = static_cast<const float *>(A);
+    p1.B = static_cast<const float *>(w1);
+    p1.B2 = static_cast<const float *>(w3);
+    p1.seg = seg;
+    p1.G = G;
+    p1.M = M;
+    p1.max_rows = a_rows;
+    p1.N = F;
+    p1.K = d;
+    p1.out = static_cast<float *>(H);
+    p1.ldo = F;
+    p1.bias = gated ? nullptr : static_cast<const float *>(b1);
+    p1.bias_stride = F;
+    p1.act = act;
+    p1.gated = gated;
+    e = launch_ffn_simt(p1, s);
+    if (e != cudaSuccess) return cuda_status(e, "expert FFN1 launch");
+    SimtProblem p2{};
+    p2.A = static_cast<const float *>(H);
+    p2.B = static_cast<const float *>(w2);
+    p2.seg = seg;
+    p2.G = G;
+    p2.M = M;
+    p2.max_rows = a_rows;
+    p2.N = d;
+    p2.K = F;
+    p2.out = y;
+    p2.ldo = d;
+    p2.bias = gated ? nullptr : static_cast<const float *>(b2);
+    p2.bias_stride = d;
+    p2.act = 0;
+    p2.gated = 0;
+    return cuda_status(launch_ffn_simt(p2, s), "expert FFN2 launch");
+}
+
+moe_status_t need(const void *p, const char *name) {
+    return p ? MOE_OK : fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+}
+moe_status_t need16(const void *p, const char *name) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+    return aligned16(p) ? MOE_OK : fail(MOE_ERR_BAD_ALIGNMENT, "%s is not 16-byte aligned", name);
+}
+moe_status_t need_ws(const void *ws, size_t have, size_t want) {
+    if (want == 0) return MOE_OK;
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL (%zu bytes needed)", want);
+    if (have < want) return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, %zu needed", have, want);
+    if (!aligned16(ws)) return fail(MOE_ERR_BAD_ALIGNMENT, "workspace is not 16-byte aligned");
+    return MOE_OK;
+}
+
+#define TRY(x)                             \
+    do {                                   \
+        moe_status_t st_ = (x);            \
+        if (st_ != MOE_OK) return st_;     \
+    } while (0)
+
+moe_status_t check_weights_ffn(const moe_config_t *c, const void *w1, const void *w3, const void *w2) {
+    TRY(need16(w1, "w1"));
+    TRY(need16(w2, "w2"));
+    if (c->activation == MOE_ACT_SWIGLU) TRY(need16(w3, "w3 (SwiGLU)"));
+    return MOE_OK;
+}
+moe_status_t check_bias(const void *b) {
+    return (b && !aligned16(b)) ? fail(MOE_ERR_BAD_ALIGNMENT, "expert bias is not 16-byte aligned") : MOE_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+int32_t moe_version(void) { return MOE_B300_VERSION; }
+
+void moe_last_error(char *buf, size_t len) {
+    if (!buf || len == 0) return;
+    snprintf(buf, len, "%s", g_msg);
+}
+
+moe_status_t moe_workspace_size(const moe_config_t *cfg, int32_t which, size_t *bytes) {
+    TRY(check_cfg(cfg));
+    TRY(need(bytes, "bytes"));
+    switch (which) {
+        case MOE_WS_FORWARD: *bytes = forward_ws(cfg); return MOE_OK;
+        case MOE_WS_ROUTE: *bytes = route_ws(cfg); return MOE_OK;
+        case MOE_WS_PERMUTE: *bytes = permute_ws(cfg); return MOE_OK;
+        case MOE_WS_EXPERT_FFN: *bytes = ffn_ws(cfg); return MOE_OK;
+        case MOE_WS_SHARED_FFN: *bytes = shared_ws(cfg); return MOE_OK;
+        default: return fail(MOE_ERR_INVALID_ARG, "unknown workspace kind %d", which);
+    }
+}
+
+moe_status_t moe_route(const moe_config_t *cfg, const void *x, const void *w_router, const float *b_router,
+                       const float *sel_bias, float *logits, int32_t *topk_idx, float *topk_w, float *lse,
+                       float *prob_mean, int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need16(x, "x"));
+    TRY(need16(w_router, "w_router"));
+    TRY(need(logits, "logits"));
+    TRY(need(topk_idx, "topk_idx"));
+    TRY(need(topk_w, "topk_w"));
+    TRY(need(lse, "lse"));
+    TRY(need(prob_mean, "prob_mean"));
+    TRY(need(counts, "counts"));
+    if (cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
+    TRY(need_ws(ws, ws_bytes, route_ws(cfg)));
+    return route_impl(cfg, x, w_router, b_router, cfg->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr,
+                      logits, nullptr, topk_idx, topk_w, lse, prob_mean, counts, ws,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits, const float *sel_bias,
+                                   int32_t *topk_idx, float *topk_w, float *lse, float *prob_mean,
+                                   int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need(logits, "logits"));
+    TRY(need(topk_idx, "topk_idx"));
+    TRY(need(topk_w, "topk_w"));
+    TRY(need(lse, "lse"));
+    TRY(need(prob_mean, "prob_mean"));
+    TRY(need(counts, "counts"));
+    if (cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
+    TRY(need_ws(ws, ws_bytes, route_ws(cfg)));
+    return route_impl(cfg, nullptr, nullptr, nullptr, cfg->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr,
+                      nullptr, logits, topk_idx, topk_w, lse, prob_mean, counts, ws,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *topk_idx, int32_t *counts,
+                         int32_t *kept, int32_t *offsets, int32_t *perm, int32_t *inv, void *x_perm, void *ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need16(x, "x"));
+    TRY(need(topk_idx, "topk_idx"));
+    TRY(need(counts, "counts"));
+    TRY(need(kept, "kept"));
+    TRY(need(offsets, "offsets"));
+    TRY(need(perm, "perm"));
+    TRY(need(inv, "inv"));
+    TRY(need16(x_perm, "x_perm"));
+    TRY(need_ws(ws, ws_bytes, permute_ws(cfg)));
+    return permute_impl(cfg, x, topk_idx, counts, kept, offsets, perm, inv, x_perm, ws,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
+                            const void *b1, const void *w3, const void *w2, const void *b2, float *y_perm,
+                            void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need16(x_perm, "x_perm"));
+    TRY(need(offsets, "offsets"));
+    TRY(check_weights_ffn(cfg, w1, w3, w2));
+    TRY(check_bias(b1));
+    TRY(check_bias(b2));
+    TRY(need16(y_perm, "y_perm"));
+    TRY(need_ws(ws, ws_bytes, ffn_ws(cfg)));
+    return ffn_impl(cfg, x_perm, cfg->num_tokens * cfg->top_k, offsets, cfg->num_experts, 0, w1, b1, w3, w2, b2,
+                    ws, y_perm, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *shared_w1, const void *shared_w3,
+                            const void *shared_w2, float *z, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    if (cfg->num_shared != 1) return fail(MOE_ERR_INVALID_ARG, "moe_shared_ffn needs num_shared = 1");
+    TRY(need16(x, "x"));
+    TRY(check_weights_ffn(cfg, shared_w1, shared_w3, shared_w2));
+    TRY(need16(z, "z"));
+    TRY(need_ws(ws, ws_bytes, shared_ws(cfg)));
+    return ffn_impl(cfg, x, cfg->num_tokens, nullptr, 1, (int)cfg->num_tokens, shared_w1, nullptr, shared_w3,
+                    shared_w2, nullptr, ws, z, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_config_t *cfg, const float *y_perm, const int32_t *inv, const float *topk_w,
+                         const float *shared_out, const void *x, void *out, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need16(y_perm, "y_perm"));
+    TRY(need(inv, "inv"));
+    TRY(need(topk_w, "topk_w"));
+    if (shared_out) TRY(need16(shared_out, "shared_out"));
+    if (cfg->residual) TRY(need16(x, "x (residual)"));
+    TRY(need16(out, "out"));
+    return cuda_status(launch_combine(cfg->num_tokens, cfg->d_model, cfg->top_k, cfg->dtype, y_perm, inv, topk_w,
+                                      shared_out, cfg->residual ? x : nullptr, out,
+                                      static_cast<cudaStream_t>(stream)),
+                       "moe_combine launch");
+}
+
+moe_status_t moe_stats(const moe_config_t *cfg, const int32_t *counts, const int32_t *kept, const float *prob_mean,
+                       const float *lse, float *f, moe_stats_t *stats, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need(counts, "counts"));
+    TRY(need(kept, "kept"));
+    TRY(need(prob_mean, "prob_mean"));
+    if (cfg->num_tokens > 0) TRY(need(lse, "lse"));
+    TRY(need(stats, "stats"));
+    StatsParams p{};
+    p.T = cfg->num_tokens;
+    p.E = cfg->num_experts;
+    p.k = cfg->top_k;
+    p.cap = capacity_of(cfg);
+    p.drop = cfg->drop_tokens;
+    p.counts = counts;
+    p.kept = kept;
+    p.prob_mean = prob_mean;
+    p.lse = lse;
+    p.f = f;
+    p.stats = stats;
+    return cuda_status(launch_stats(p, static_cast<cudaStream_t>(stream)), "moe_stats launch");
+}
+
+moe_status_t moe_bias_update(const moe_config_t *cfg, const int32_t *counts, float *sel_bias, float gamma,
+                             moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need(counts, "counts"));
+    TRY(need(sel_bias, "sel_bias"));
+    if (!isfinite(gamma)) return fail(MOE_ERR_INVALID_ARG, "gamma must be finite");
+    return cuda_status(launch_bias_update(cfg->num_tokens, cfg->num_experts, cfg->top_k, counts, sel_bias, gamma,
+                                          static_cast<cudaStream_t>(stream)),
+                       "moe_bias_update launch");
+}
+
+moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const void *x, const float *sel_bias,
+                         void *out, const moe_forward_io_t *io, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(need(w, "weights"));
+    TRY(need16(x, "x"));
+    TRY(need16(out, "out"));
+    TRY(need16(w->w_router, "w_router"));
+    TRY(check_weights_ffn(cfg, w->w1, w->w3, w->w2));
+    TRY(check_bias(w->b1));
+    TRY(check_bias(w->b2));
+    if (cfg->num_shared) TRY(check_weights_ffn(cfg, w->shared_w1, w->shared_w3, w->shared_w2));
+    if (cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
+    TRY(need_ws(ws, ws_bytes, forward_ws(cfg)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const moe_config_t *c = cfg;
+    const size_t T = (size_t)c->num_tokens, E = (size_t)c->num_experts, S = T * c->top_k, d = (size_t)c->d_model;
+    Carve cv{static_cast<uint8_t *>(ws)};
+    void *ws_route = cv.take<uint8_t>(route_ws(c));
+    void *ws_perm = cv.take<uint8_t>(permute_ws(c));
+    void *ws_ffn = cv.take<uint8_t>(ffn_ws(c));
+    void *ws_shared = cv.take<uint8_t>(shared_ws(c));
+    void *x_perm = cv.take<uint8_t>(S * d * elem_bytes(c));
+    float *y_perm = cv.take<float>(S * d * 4);
+    float *z = c->num_shared ? cv.take<float>(T * d * 4) : nullptr;
+    moe_forward_io_t o{};
+    if (io) o = *io;
+    float *logits_ws = cv.take<float>(T * E * 4);
+    int32_t *idx_ws = cv.take<int32_t>(S * 4);
+    float *w_ws = cv.take<float>(S * 4);
+    int32_t *perm_ws = cv.take<int32_t>(S * 4);
+    int32_t *inv_ws = cv.take<int32_t>(S * 4);
+    float *lse_ws = cv.take<float>(T * 4);
+    float *P_ws = cv.take<float>(E * 4);
+    int32_t *cnt_ws = cv.take<int32_t>(E * 4);
+    int32_t *kept_ws = cv.take<int32_t>(E * 4);
+    float *f_ws = cv.take<float>(E * 4);
+    int32_t *off_ws = cv.take<int32_t>((E + 1) * 4);
+    moe_stats_t *st_ws = cv.take<moe_stats_t>(sizeof(moe_stats_t));
+    if (!o.logits) o.logits = logits_ws;
+    if (!o.topk_idx) o.topk_idx = idx_ws;
+    if (!o.topk_w) o.topk_w = w_ws;
+    if (!o.perm) o.perm = perm_ws;
+    if (!o.inv) o.inv = inv_ws;
+    if (!o.lse) o.lse = lse_ws;
+    if (!o.prob_mean) o.prob_mean = P_ws;
+    if (!o.counts) o.counts = cnt_ws;
+    if (!o.kept) o.kept = kept_ws;
+    if (!o.f) o.f = f_ws;
+    if (!o.offsets) o.offsets = off_ws;
+    if (!o.stats) o.stats = st_ws;
+
+    TRY(route_impl(c, x, w->w_router, w->b_router, c->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr, o.logits,
+                   nullptr, o.topk_idx, o.topk_w, o.lse, o.prob_mean, o.counts, ws_route, s));
+    TRY(permute_impl(c, x, o.topk_idx, o.counts, o.kept, o.offsets, o.perm, o.inv, x_perm, ws_perm, s));
+    TRY(ffn_impl(c, x_perm, (int64_t)S, o.offsets, c->num_experts, 0, w->w1, w->b1, w->w3, w->w2, w->b2, ws_ffn,
+                 y_perm, s));
+    if (c->num_shared)
+        TRY(ffn_impl(c, x, (int64_t)T, nullptr, 1, (int)T, w->shared_w1, nullptr, w->shared_w3, w->shared_w2,
+                     nullptr, ws_shared, z, s));
+    TRY(cuda_status(launch_combine(c->num_tokens, c->d_model, c->top_k, c->dtype, y_perm, o.inv, o.topk_w, z,
+                                   c->residual ? x : nullptr, out, s),
+                    "combine launch"));
+    StatsParams sp{};
+    sp.T = c->num_tokens;
+    sp.E = c->num_experts;
+    sp.k = c->top_k;
+    sp.cap = capacity_of(c);
+    sp.drop = c->drop_tokens;
+    sp.counts = o.counts;
+    sp.kept = o.kept;
+    sp.prob_mean = o.prob_mean;
+    sp.lse = o.lse;
+    sp.f = o.f;
+    sp.stats = o.stats;
+    return cuda_status(launch_stats(sp, s), "stats launch");
+}
+
+moe_status_t moe_check_device_error(int32_t *code) {
+    TRY(need(code, "code"));
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_status(e, "cudaDeviceSynchronize");
+    int32_t *flag = device_error_flag();
+    if (!flag) return fail(MOE_ERR_CUDA, "device error flag unavailable");
+    int32_t v = 0;
+    e = cudaMemcpy(&v, flag, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e, "read device error flag");
+    if (v != 0) {
+        const int32_t zero = 0;
+        e = cudaMemcpy(flag, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_status(e, "clear device error flag");
+    }
+    *code = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// Internal launch interface between the C ABI (moe_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kRouteTokPerCta = 32;   // tokens per router CTA (fixed: partials are deterministic)
+constexpr int kPermChunk = 2048;      // priority-ordered slots per permute chunk
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Device error flag shared by every kernel of the library (defined in
+// gemm_sm103.cu).  Returns its device address on the current device.
+int32_t *device_error_flag();
+
+int num_sms();
+
+// ----------------------------------------------------------------- router
+struct RouteParams {
+    int64_t T;
+    int E, k, d;
+    int score_fn;          // 0 softmax, 1 sigmoid
+    int renormalize;
+    const void *x;         // [T,d] (fused path)
+    const void *w_router;  // [E,d]
+    const float *b_router; // [E] or null
+    const float *sel_bias; // [E] or null
+    float *logits;         // [T,E]: output (fused path), input (logits path)
+    int logits_add_bias;   // logits path: add b_router and write back
+    int32_t *topk_idx;
+    float *topk_w;
+    float *lse;
+    float *part_prob;      // [nblk, E]
+    int32_t *part_cnt;     // [nblk, E]
+};
+// E <= 32: one kernel computes logits from x and routes (dtype 0 f32, 1 bf16)
+cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s);
+// logits given in p.logits (optionally + bias, written back): route only
+cudaError_t launch_route_logits(const RouteParams &p, cudaStream_t s);
+// logits = x w_r^T on CUDA cores (fp32, or shapes the tensor-core path does not take)
+cudaError_t launch_router_logits_simt(const RouteParams &p, int dtype, cudaStream_t s);
+// deterministic reduction of the per-CTA partials: prob_mean[E], counts[E]
+cudaError_t launch_route_reduce(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
+                                int E, int64_t T, float *prob_mean, int32_t *counts,
+                                cudaStream_t s);
+
+// ----------------------------------------------------------------- permute
+struct PermuteParams {
+    int64_t T;
+    int E, k, d, dtype;
+    int64_t cap;           // capacity (T*k when no dropping)
+    const void *x;
+    const int32_t *topk_idx;
+    int32_t *counts, *kept, *offsets, *perm, *inv;
+    void *x_perm;
+    int32_t *hist;         // [nchunk, E] scratch
+    int32_t *base;         // [nchunk, E] scratch
+};
+cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
+
+// ----------------------------------------------------------------- experts
+// Grouped GEMM with fused epilogue on the tensor cores (bf16 in, fp32 acc).
+//   out[r, n] = epi( sum_k A[r, k] * B[g*b_rows + n, k] )   for rows r of group g
+// gated: B2 is the second weight; epi = silu(acc1) * acc2.
+// act: 0 none, 1 GELU, 2 ReLU.  out is bf16 (out_f32 = 0) or fp32.
+struct GemmProblem {
+    const bf16 *A; int64_t a_rows;           // A [a_rows, K]
+    const bf16 *B; const bf16 *B2; int64_t b_rows_total; int b_group_rows;
+    const int32_t *seg;                      // [G+1] row offsets (device) or null
+    int G; int M;                            // M: rows when seg is null
+    int N, K;
+    void *out; int64_t ldo; int out_f32;
+    const bf16 *bias; int64_t bias_stride;   // per group, or null
+    int act; int gated;
+};
+cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
+bool grouped_gemm_supported(int N, int K, int gated);
+
+// CUDA-core grouped FFN layer for fp32 storage (same contract as above, fp32).
+struct SimtProblem {
+    const float *A; const float *B; const float *B2;
+    const int32_t *seg; int G; int M; int64_t max_rows;
+    int N, K; float *out; int64_t ldo;
+    const float *bias; int64_t bias_stride; int act; int gated;
+};
+cudaError_t launch_ffn_simt(const SimtProblem &p, cudaStream_t s);
+
+// ----------------------------------------------------------------- combine / stats
+cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_perm,
+                           const int32_t *inv, const float *topk_w, const float *shared_out,
+                           const void *x_res, void *out, cudaStream_t s);
+struct StatsParams {
+    int64_t T; int E, k; int64_t cap; int drop;
+    const int32_t *counts, *kept; const float *prob_mean, *lse;
+    float *f; void *stats;
+};
+cudaError_t launch_stats(const StatsParams &p, cudaStream_t s);
+cudaError_t launch_bias_update(int64_t T, int E, int k, const int32_t *counts, float *bias,
+                               float gamma, cudaStream_t s);
+
+}  // namespace moe

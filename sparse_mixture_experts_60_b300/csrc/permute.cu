@@ -1,0 +1,240 @@
+// Dispatch: per-expert histogram and scan with the capacity clamp, a stable
+// rank of every slot within its expert in priority order, the permutation
+// and its inverse, and the row copy of x into per-expert segments.
+//
+// Pages: "MoE Training Guide" (Core MoE Parameters: capacity =
+// tokens / num_experts x capacity_factor, min capacity, drop_tokens);
+// "Mixture of Experts (MoE) From Scratch to DeepSeek V3" (Token Dropping:
+// slots past an expert's buffer are left unprocessed); "MoE Training:
+// Mixture of Experts" (Quick Start MoELayer dispatch x_flat[mask], with the
+// top-k rank outside and the experts inside, which fixes the priority:
+// all rank-0 slots in token order, then rank-1, ...).
+//
+// Priority index of slot (t, j) is p = j*T + t.  Chunks of kPermChunk
+// consecutive priorities are the unit of parallel work:
+//   perm_hist  : per-chunk expert histogram                    [nchunk, E]
+//   perm_scan  : exclusive scan over chunks per expert (chunk bases),
+//                counts, kept = min(counts, C), offsets = scan(kept)
+//   perm_rank  : within a chunk, 8 warps x 256 priorities; warp bases from
+//                a scan of the warp histograms, then __match_any_sync ranks
+//                32 slots at a time in order -> perm, inv
+//   perm_copy  : token-major row copy (x read once, written to its k rows)
+// Integer work only: the result is unique and deterministic.
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kPermThreads = 256;
+constexpr int kWarpSpan = kPermChunk / (kPermThreads / 32);  // 256 priorities per warp
+
+__device__ __forceinline__ int slot_expert(const int32_t *idx, int64_t p, int64_t T, int k, int E,
+                                           int64_t S, int64_t *slot_out, int32_t *err) {
+    if (p >= S) return -1;
+    const int64_t j = p / T, t = p - j * T;
+    const int64_t s = t * k + j;
+    *slot_out = s;
+    const int e = idx[s];
+    if (e < 0 || e >= E) {
+        atomicExch(err, 1);  // MOE_ERR_INVALID_ARG
+        return -2;
+    }
+    return e;
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *idx, int64_t T, int k,
+                                                                 int E, int32_t *hist, int32_t *err) {
+    extern __shared__ int h[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+    __syncthreads();
+    const int64_t S = T * k;
+    const int64_t p0 = (int64_t)blockIdx.x * kPermChunk;
+    for (int i = threadIdx.x; i < kPermChunk; i += blockDim.x) {
+        int64_t s;
+        const int e = slot_expert(idx, p0 + i, T, k, E, S, &s, err);
+        if (e >= 0) atomicAdd(&h[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = h[e];
+}
+
+// One CTA of 1024 threads (E <= 1024).
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *hist, int32_t *base,
+                                                         int64_t nchunk, int E, int64_t cap,
+                                                         int32_t *counts, int32_t *kept,
+                                                         int32_t *offsets) {
+    __shared__ int warp_tot[32];
+    const int e = threadIdx.x;
+    int kp = 0;
+    if (e < E) {
+        int run = 0;
+        for (int64_t c = 0; c < nchunk; ++c) {
+            base[c * E + e] = run;
+            run += hist[c * E + e];
+        }
+        counts[e] = run;
+        kp = (int64_t)run < cap ? run : (int)cap;
+        kept[e] = kp;
+    }
+    // exclusive block scan of kept
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int v = kp;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += u;
+        }
+        warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + v - kp;
+    if (e < E) offsets[e] = before;
+    if (e == E - 1) offsets[E] = before + kp;
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *idx, int64_t T, int k,
+                                                                 int E, int64_t cap,
+                                                                 const int32_t *base,
+                                                                 const int32_t *offsets,
+                                                                 int32_t *perm, int32_t *inv,
+                                                                 int32_t *err) {
+    extern __shared__ int wh[];  // [8][E] warp histograms, then warp running bases
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = kPermThreads / 32;
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wh[i] = 0;
+    __syncthreads();
+    const int64_t S = T * k;
+    const int64_t p0 = (int64_t)blockIdx.x * kPermChunk + (int64_t)warp * kWarpSpan;
+    int *my = wh + warp * E;
+    // A: warp histogram of its 256 priorities
+    for (int g = 0; g < kWarpSpan; g += 32) {
+        int64_t s;
+        const int e = slot_expert(idx, p0 + g + lane, T, k, E, S, &s, err);
+        if (e >= 0) atomicAdd(&my[e], 1);
+    }
+    __syncthreads();
+    // B: exclusive scan over warps, seeded with this chunk's base
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = base[(int64_t)blockIdx.x * E + e];
+        for (int w = 0; w < nw; ++w) {
+            const int c = wh[w * E + e];
+            wh[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // C: ranks, 32 slots at a time in priority order
+    const unsigned lt = (1u << lane) - 1u;
+    for (int g = 0; g < kWarpSpan; g += 32) {
+        int64_t s = -1;
+        const int e = slot_expert(idx, p0 + g + lane, T, k, E, S, &s, err);
+        const unsigned peers = __match_any_sync(kFull, e);
+        const int rank_in = __popc(peers & lt);
+        int rank = 0;
+        if (e >= 0) rank = my[e] + rank_in;
+        __syncwarp();
+        if (e >= 0 && (peers & lt) == 0) my[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            if ((int64_t)rank < cap) {
+                const int row = offsets[e] + rank;
+                perm[row] = (int32_t)s;
+                inv[s] = row;
+            } else {
+                inv[s] = -1;
+            }
+        } else if (e == -2) {
+            inv[s] = -1;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) perm_copy_kernel(const uint4 *x, int64_t T, int k, int64_t nvec,
+                                                        const int32_t *inv, const int32_t *offsets,
+                                                        int E, int32_t *perm, int64_t S, uint4 *x_perm) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    // unused tail of perm -> -1
+    {
+        const int64_t used = offsets[E];
+        const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        const int64_t gsz = (int64_t)gridDim.x * blockDim.x;
+        for (int64_t i = used + gtid; i < S; i += gsz) perm[i] = -1;
+    }
+    if (t >= T) return;
+    int rows[kMaxTopK];
+    const int my_row = lane < k ? inv[t * k + lane] : -1;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(kFull, my_row, j);
+    const uint4 *src = x + t * nvec;
+    int64_t v = lane;
+    for (; v + 96 < nvec; v += 128) {
+        uint4 a0 = __ldg(src + v), a1 = __ldg(src + v + 32), a2 = __ldg(src + v + 64),
+              a3 = __ldg(src + v + 96);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k && rows[j] >= 0) {
+                uint4 *dst = x_perm + (int64_t)rows[j] * nvec;
+                dst[v] = a0;
+                dst[v + 32] = a1;
+                dst[v + 64] = a2;
+                dst[v + 96] = a3;
+            }
+        }
+    }
+    for (; v < nvec; v += 32) {
+        const uint4 a = __ldg(src + v);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k && rows[j] >= 0) x_perm[(int64_t)rows[j] * nvec + v] = a;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
+    const int64_t S = p.T * p.k;
+    const int64_t nchunk = ceil_div(S, kPermChunk);
+    int32_t *err = device_error_flag();
+    if (!err) return cudaErrorUnknown;
+    if (nchunk > 0) {
+        perm_hist_kernel<<<(unsigned)nchunk, kPermThreads, p.E * sizeof(int), s>>>(p.topk_idx, p.T, p.k,
+                                                                                 p.E, p.hist, err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    perm_scan_kernel<<<1, 1024, 0, s>>>(p.hist, p.base, nchunk, p.E, p.cap, p.counts, p.kept,
+                                        p.offsets);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nchunk == 0) return e;
+    const size_t rank_smem = (size_t)(kPermThreads / 32) * p.E * sizeof(int);
+    if (rank_smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)rank_smem);
+        if (e != cudaSuccess) return e;
+    }
+    perm_rank_kernel<<<(unsigned)nchunk, kPermThreads, rank_smem, s>>>(
+        p.topk_idx, p.T, p.k, p.E, p.cap, p.base, p.offsets, p.perm, p.inv, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int eb = p.dtype == 0 ? 4 : 2;
+    const int64_t nvec = (int64_t)p.d * eb / 16;
+    const unsigned grid = (unsigned)ceil_div(p.T, 8);
+    perm_copy_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(p.x), p.T, p.k, nvec, p.inv,
+                                             p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

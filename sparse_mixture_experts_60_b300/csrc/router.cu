@@ -1,0 +1,434 @@
+// Router: logits, fp32 softmax / sigmoid scores, warp-level top-k in
+// registers, gates, logsumexp, and deterministic balance partials.
+//
+// Pages: "MoE Training: Mixture of Experts" (Quick Start MoELayer: gate
+// Linear, softmax, topk, renormalise); "Mixture of Experts (MoE) From
+// Scratch to DeepSeek V3" (routing formula h(x) = x W_g, fp32 router,
+// sigmoid routing, selection bias b_i); "moe_code.py" (Router,
+// MixtureOfExperts steps 1-3).
+//
+// Layout of the work: a CTA owns 32 consecutive tokens (8 warps x 4).  A
+// token's experts are spread over a "group" of G lanes (G = 8, 16 or 32),
+// lane r of the group holding experts r, r+G, r+2G, ... (VPL values).  With
+// G < 32 one warp routes 32/G tokens at once.  All reductions are xor
+// butterflies, so every lane of a group ends with bit-identical values and
+// the result does not depend on scheduling.
+#include <math.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------- fp32 key
+// The sigmoid selection key must be reproducible bit for bit, so it is a
+// fixed sequence of correctly rounded fp32 operations (explicit _rn
+// intrinsics: no contraction, no reassociation):
+//   exp: Cody-Waite reduction n = rint(a log2e), r = a - n ln2 with ln 2
+//        split into a 16-bit head (exact products) and an fp32 tail, then
+//        the degree-7 Taylor polynomial of e^r in Horner form, then one
+//        multiply by the exact power of two 2^n;  a > 88 -> +inf,
+//        a < -87 -> 0.
+//   sigmoid(x) = 1 / (1 + exp(-x));  key = sigmoid(logit) + b_i.
+__device__ __forceinline__ float exp_key(float a) {
+    if (a != a) return a;
+    if (a > 88.0f) return __int_as_float(0x7f800000);
+    if (a < -87.0f) return 0.0f;
+    const float n = rintf(__fmul_rn(a, 0x1.715476p+0f));
+    float r = __fmaf_rn(-n, 0x1.62e4p-1f, a);
+    r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+    float q = 0x1.a01a02p-13f;           // 1/7!
+    q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);  // 1/6!
+    q = __fmaf_rn(q, r, 0x1.111112p-7f);   // 1/5!
+    q = __fmaf_rn(q, r, 0x1.555556p-5f);   // 1/4!
+    q = __fmaf_rn(q, r, 0x1.555556p-3f);   // 1/3!
+    q = __fmaf_rn(q, r, 0x1p-1f);          // 1/2!
+    q = __fmaf_rn(q, r, 1.0f);
+    q = __fmaf_rn(q, r, 1.0f);
+    const int ni = (int)n;                 // -126 .. 127
+    return __fmul_rn(q, __int_as_float((ni + 127) << 23));
+}
+
+__device__ __forceinline__ float sigmoid_key(float x) {
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_key(-x)));
+}
+
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// (key descending, expert ascending)
+__device__ __forceinline__ bool ranks_before(float ka, int ea, float kb, int eb) {
+    return ka > kb || (ka == kb && ea < eb);
+}
+
+// Route one token held by a group of G lanes (VPL logits per lane).
+template <int G, int VPL>
+__device__ __forceinline__ void route_group(const RouteParams &p, const float (&l)[VPL], int r,
+                                            bool tok_ok, int64_t t, float (&psum)[VPL],
+                                            int *s_cnt) {
+    const int E = p.E, k = p.k;
+    float key[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = r + G * i;
+        float kv = -INFINITY;
+        if (e < E) {
+            kv = (p.score_fn == 0) ? l[i]
+                                   : __fadd_rn(sigmoid_key(l[i]), p.sel_bias ? p.sel_bias[e] : 0.0f);
+            if (kv != kv) kv = -INFINITY;
+        }
+        key[i] = kv;
+    }
+    // logsumexp of the logits (fp32)
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        if (r + G * i < E) m = fmaxf(m, l[i]);
+    m = group_max<G>(m);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        if (r + G * i < E) s += expf(l[i] - m);
+    s = group_sum<G>(s);
+    const float lse = m + logf(s);
+    if (tok_ok) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+            if (r + G * i < E) psum[i] += expf(l[i] - lse);
+    }
+    // top-k: k rounds of a group arg-max over the keys not yet taken
+    unsigned taken = 0u;
+    int my_e = 0;
+    float my_l = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        float bk = -INFINITY, bl = 0.0f;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = r + G * i;
+            if (e < E && !((taken >> i) & 1u) && ranks_before(key[i], e, bk, be)) {
+                bk = key[i];
+                be = e;
+                bl = l[i];
+            }
+        }
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) {
+            const float ok = __shfl_xor_sync(kFull, bk, o);
+            const int oe = __shfl_xor_sync(kFull, be, o);
+            const float ol = __shfl_xor_sync(kFull, bl, o);
+            if (ranks_before(ok, oe, bk, be)) {
+                bk = ok;
+                be = oe;
+                bl = ol;
+            }
+        }
+        if (be < E && (be & (G - 1)) == r) taken |= 1u << (be / G);
+        if (r == j) {
+            my_e = be;
+            my_l = bl;
+        }
+    }
+    // gates
+    float g = 0.0f;
+    if (r < k) g = (p.score_fn == 0) ? expf(my_l - m) : 1.0f / (1.0f + expf(-my_l));
+    const float tot = group_sum<G>(g);
+    float w;
+    if (p.renormalize) w = g / tot;
+    else w = (p.score_fn == 0) ? expf(my_l - lse) : g;
+    if (tok_ok) {
+        if (r < k) {
+            p.topk_idx[t * k + r] = my_e;
+            p.topk_w[t * k + r] = w;
+            atomicAdd(&s_cnt[my_e], 1);
+        }
+        if (r == 0) p.lse[t] = lse;
+    }
+}
+
+// Per-CTA partials: psum is summed over the groups of a warp (xor
+// butterfly), then over the 8 warps in warp order.
+template <int G, int VPL>
+__device__ __forceinline__ void write_partials(const RouteParams &p, float (&psum)[VPL], int r,
+                                               int grp, float *s_prob, const int *s_cnt) {
+    const int warp = threadIdx.x >> 5;
+    const int EP = G * VPL;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+#pragma unroll
+        for (int o = G; o < 32; o <<= 1) psum[i] += __shfl_xor_sync(kFull, psum[i], o);
+        if (grp == 0) s_prob[warp * EP + r + G * i] = psum[i];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        float acc = 0.0f;
+        for (int w = 0; w < 8; ++w) acc += s_prob[w * EP + e];
+        p.part_prob[(int64_t)blockIdx.x * p.E + e] = acc;
+        p.part_cnt[(int64_t)blockIdx.x * p.E + e] = s_cnt[e];
+    }
+}
+
+template <typename Tin>
+struct Vec;
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void unpack(const uint4 &u, float *f) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+};
+template <>
+struct Vec<bf16> {
+    static constexpr int N = 8;
+    __device__ static void unpack(const uint4 &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// After the loop, lane l holds the warp-wide sum of v[l] (a reduce-scatter
+// by recursive halving: 31 shuffles for 32 values).
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, s);
+        }
+    }
+    return v[0];
+}
+
+// E <= EP <= 32: logits from x on the CUDA cores (the router is read from
+// L1, x streamed once with 16-byte loads), then routing in registers.
+template <typename Tin, int EP>
+__global__ void __launch_bounds__(256) router_fused_kernel(RouteParams p) {
+    constexpr int TPW = 32 / EP;            // tokens per warp per round
+    constexpr int VN = Vec<Tin>::N;
+    __shared__ float s_prob[8 * EP];
+    __shared__ int s_cnt[EP];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = lane % EP, grp = lane / EP;
+    const int E = p.E, d = p.d;
+    const Tin *x = static_cast<const Tin *>(p.x);
+    const Tin *W = static_cast<const Tin *>(p.w_router);
+    if (threadIdx.x < EP) s_cnt[threadIdx.x] = 0;
+    __syncthreads();
+    float psum[1] = {0.0f};
+    const int nvec = d / VN;
+    const int64_t cta_t0 = (int64_t)blockIdx.x * kRouteTokPerCta;
+#pragma unroll 1
+    for (int round = 0; round < 4 / TPW; ++round) {
+        const int64_t t0 = cta_t0 + warp * 4 + round * TPW;
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        for (int v = lane; v < nvec; v += 32) {
+            float xf[TPW][VN];
+#pragma unroll
+            for (int ti = 0; ti < TPW; ++ti) {
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (t0 + ti < p.T)
+                    u = __ldg(reinterpret_cast<const uint4 *>(x + (t0 + ti) * d) + v);
+                Vec<Tin>::unpack(u, xf[ti]);
+            }
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                if (e < E) {
+                    float wf[VN];
+                    Vec<Tin>::unpack(__ldg(reinterpret_cast<const uint4 *>(W + (int64_t)e * d) + v), wf);
+#pragma unroll
+                    for (int ti = 0; ti < TPW; ++ti)
+#pragma unroll
+                        for (int q = 0; q < VN; ++q) acc[ti * EP + e] = fmaf(xf[ti][q], wf[q], acc[ti * EP + e]);
+                }
+            }
+        }
+        float logit = transpose_reduce32(acc, lane);   // token grp, expert r
+        const int64_t t = t0 + grp;
+        const bool tok_ok = t < p.T;
+        if (r < E) {
+            if (p.b_router) logit += p.b_router[r];
+            if (tok_ok) p.logits[t * E + r] = logit;
+        }
+        const float l1[1] = {logit};
+        route_group<EP, 1>(p, l1, r, tok_ok, t, psum, s_cnt);
+    }
+    __syncthreads();
+    write_partials<EP, 1>(p, psum, r, grp, s_prob, s_cnt);
+}
+
+// Routing from logits in memory (optionally adding the router bias and
+// writing the biased logits back).
+template <int G, int VPL>
+__global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
+    constexpr int TPR = 32 / G;             // tokens per warp per round
+    extern __shared__ float dyn[];
+    float *s_prob = dyn;                                  // [8][G*VPL]
+    int *s_cnt = reinterpret_cast<int *>(dyn + 8 * G * VPL);  // [G*VPL]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r = lane % G, grp = lane / G;
+    const int E = p.E;
+    for (int e = threadIdx.x; e < G * VPL; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    float psum[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) psum[i] = 0.0f;
+    const int64_t cta_t0 = (int64_t)blockIdx.x * kRouteTokPerCta;
+#pragma unroll 1
+    for (int round = 0; round < 4 / TPR; ++round) {
+        const int64_t t = cta_t0 + warp * 4 + round * TPR + grp;
+        const bool tok_ok = t < p.T;
+        float l[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = r + G * i;
+            float v = 0.0f;
+            if (tok_ok && e < E) {
+                v = p.logits[t * E + e];
+                if (p.logits_add_bias && p.b_router) {
+                    v += p.b_router[e];
+                    p.logits[t * E + e] = v;
+                }
+            }
+            l[i] = v;
+        }
+        route_group<G, VPL>(p, l, r, tok_ok, t, psum, s_cnt);
+    }
+    __syncthreads();
+    write_partials<G, VPL>(p, psum, r, grp, s_prob, s_cnt);
+}
+
+// logits = x W^T on CUDA cores, 32x32 output tiles (no bias).
+template <typename Tin>
+__global__ void __launch_bounds__(256) router_logits_simt_kernel(const Tin *x, const Tin *W,
+                                                                 float *logits, int64_t T, int E,
+                                                                 int d) {
+    __shared__ float xs[32][33], ws[32][33];
+    const int64_t t0 = (int64_t)blockIdx.x * 32;
+    const int e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < d; k0 += 32) {
+        for (int i = ty; i < 32; i += 8) {
+            const int kk = k0 + tx;
+            xs[i][tx] = (t0 + i < T && kk < d) ? (float)x[(t0 + i) * d + kk] : 0.0f;
+            ws[i][tx] = (e0 + i < E && kk < d) ? (float)W[(int64_t)(e0 + i) * d + kk] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+            const float wv = ws[tx][kk];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = fmaf(xs[ty + 8 * q][kk], wv, acc[q]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t t = t0 + ty + 8 * q;
+        if (t < T && e0 + tx < E) logits[t * E + e0 + tx] = acc[q];
+    }
+}
+
+__global__ void route_reduce_kernel(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
+                                    int E, int64_t T, float *prob_mean, int32_t *counts) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    double s = 0.0;
+    int64_t c = 0;
+    for (int64_t b = 0; b < nblk; ++b) {
+        s += (double)part_prob[b * E + e];
+        c += part_cnt[b * E + e];
+    }
+    prob_mean[e] = T > 0 ? (float)(s / (double)T) : 0.0f;
+    counts[e] = (int32_t)c;
+}
+
+template <int G, int VPL>
+cudaError_t launch_route_logits_t(const RouteParams &p, cudaStream_t s) {
+    const int64_t nblk = ceil_div(p.T, kRouteTokPerCta);
+    const size_t smem = (size_t)(8 * G * VPL) * sizeof(float) + (size_t)(G * VPL) * sizeof(int);
+    auto kern = route_logits_kernel<G, VPL>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<(unsigned)nblk, 256, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s) {
+    if (p.T == 0) return cudaSuccess;
+    const unsigned nblk = (unsigned)ceil_div(p.T, kRouteTokPerCta);
+    if (dtype == 0) {
+        if (p.E <= 8) router_fused_kernel<float, 8><<<nblk, 256, 0, s>>>(p);
+        else if (p.E <= 16) router_fused_kernel<float, 16><<<nblk, 256, 0, s>>>(p);
+        else router_fused_kernel<float, 32><<<nblk, 256, 0, s>>>(p);
+    } else {
+        if (p.E <= 8) router_fused_kernel<bf16, 8><<<nblk, 256, 0, s>>>(p);
+        else if (p.E <= 16) router_fused_kernel<bf16, 16><<<nblk, 256, 0, s>>>(p);
+        else router_fused_kernel<bf16, 32><<<nblk, 256, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_logits(const RouteParams &p, cudaStream_t s) {
+    if (p.T == 0) return cudaSuccess;
+    const int E = p.E;
+    if (E <= 8) return launch_route_logits_t<8, 1>(p, s);
+    if (E <= 16) return launch_route_logits_t<16, 1>(p, s);
+    if (E <= 32) return launch_route_logits_t<32, 1>(p, s);
+    if (E <= 64) return launch_route_logits_t<32, 2>(p, s);
+    if (E <= 128) return launch_route_logits_t<32, 4>(p, s);
+    if (E <= 256) return launch_route_logits_t<32, 8>(p, s);
+    if (E <= 512) return launch_route_logits_t<32, 16>(p, s);
+    return launch_route_logits_t<32, 32>(p, s);
+}
+
+cudaError_t launch_router_logits_simt(const RouteParams &p, int dtype, cudaStream_t s) {
+    if (p.T == 0) return cudaSuccess;
+    dim3 grid((unsigned)ceil_div(p.T, 32), (unsigned)ceil_div(p.E, 32));
+    if (dtype == 0)
+        router_logits_simt_kernel<float><<<grid, 256, 0, s>>>(
+            static_cast<const float *>(p.x), static_cast<const float *>(p.w_router), p.logits, p.T, p.E, p.d);
+    else
+        router_logits_simt_kernel<bf16><<<grid, 256, 0, s>>>(
+            static_cast<const bf16 *>(p.x), static_cast<const bf16 *>(p.w_router), p.logits, p.T, p.E, p.d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_reduce(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
+                                int E, int64_t T, float *prob_mean, int32_t *counts,
+                                cudaStream_t s) {
+    route_reduce_kernel<<<(unsigned)ceil_div(E, 256), 256, 0, s>>>(part_prob, part_cnt, nblk, E, T,
+                                                                   prob_mean, counts);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,142 @@
+"""Whole-layer parity on the GPU through moe_forward (the call the benchmark
+times): output, intermediates, statistics, the bias update, determinism and
+the empty batch."""
+import numpy as np
+import pytest
+import torch
+
+import sparse_mixture_experts_60_b300 as moe
+from oracle import oracle as orc
+from sparse_mixture_experts_60_b300 import workloads as wl
+from tests.gpu_util import as_f32, dev, float_check, host, weights
+from tests.test_gpu_1_route import check_route_from_x
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(w, inp):
+    cfg = moe.config_for(w)
+    layer = moe.MoELayer(cfg, weights(inp), dev(inp["sel_bias"]) if "sel_bias" in inp else None)
+    out = layer.forward(dev(inp["x"]))
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == 0
+    got = {k: host(v) for k, v in layer.io.items() if k != "stats"}
+    got["out"] = host(out)
+    got["stats"] = layer.stats()
+    return layer, got
+
+
+def check_layer(w, inp, got, tokens, report=None):
+    """Routing from x (exact where unambiguous), dispatch, output, stats."""
+    ref_r, n_near = check_route_from_x(w, inp, dict(logits=got["logits"], idx=got["topk_idx"],
+                                                    w=got["topk_w"], lse=got["lse"], P=got["prob_mean"],
+                                                    counts=got["counts"]))
+    ref_d = orc.dispatch(w, ref_r["idx"])
+    S = w.T * w.k
+    if n_near == 0:
+        for key in ("counts", "kept", "offsets"):
+            np.testing.assert_array_equal(got[key], ref_d[key], err_msg=key)
+        np.testing.assert_array_equal(got["perm"][:S], ref_d["perm"])
+        np.testing.assert_array_equal(got["inv"].reshape(-1)[:S], ref_d["inv"])
+        ok_tokens = tokens
+    else:
+        # a near-tie flipped a choice: compare tokens whose route and slots agree
+        same = np.all(got["topk_idx"] == ref_r["idx"], axis=1)
+        inv_g = got["inv"].reshape(w.T, w.k)
+        inv_same = np.all((inv_g >= 0) == (ref_d["inv"].reshape(w.T, w.k) >= 0), axis=1)
+        ok_tokens = np.array([t for t in tokens if same[t] and inv_same[t]])
+    out_ref = orc.forward_tokens(w, inp, ref_r["idx"], ref_r["gate"], ref_d["inv"], ok_tokens)
+    float_check(got["out"][ok_tokens], out_ref, w, f"{w.name} out", report)
+    st = orc.stats(w, ref_d["counts"], ref_d["kept"], ref_r["prob_sum"], ref_r["lse"])
+    gs = got["stats"]
+    if n_near == 0:
+        assert gs["dropped"] == st["dropped"]
+        assert gs["total_kept"] == int(ref_d["kept"].sum())
+        np.testing.assert_allclose(got["f"], st["f"], rtol=1e-6)
+        assert abs(gs["utilization"] - st["utilization"]) < 1e-6
+        assert (gs["imbalance"] == st["imbalance"]) or abs(gs["imbalance"] - st["imbalance"]) < 1e-5 * st["imbalance"]
+        assert abs(gs["drop_rate"] - st["drop_rate"]) < 1e-7
+    np.testing.assert_allclose(gs["aux_loss"], st["aux"], rtol=1e-4)
+    np.testing.assert_allclose(gs["z_loss"], st["z"], rtol=1e-4)
+    assert gs["capacity"] == (orc.capacity(w) if w.drop_tokens else -1)
+    return ref_r, ref_d, n_near
+
+
+LAYER_CASES = [("tiny_fp32", 64, None), ("quickstart_bf16", 1000, 96), ("capacity_e128", 2000, 128),
+               ("mixtral", 256, 12), ("deepseek_v3", 200, 24)]
+
+
+@pytest.mark.parametrize("name,T,ntok", LAYER_CASES)
+def test_layer_forward(name, T, ntok):
+    w = wl.WORKLOADS[name].scaled(T)
+    inp = wl.make_inputs(w)
+    _, got = run_layer(w, inp)
+    tokens = np.arange(T) if ntok is None else wl.sample_tokens(w, ntok)
+    check_layer(w, inp, got, tokens)
+
+
+def test_tiny_layer_against_bruteforce():
+    """The fp32 Quick Start layer against the EfficientMoE brute-force form."""
+    w = wl.WORKLOADS["tiny_fp32"]
+    inp = wl.make_inputs(w)
+    _, got = run_layer(w, inp)
+    ref = orc.layer(w, inp)
+    _, dense = orc.dense_all(w, inp, ref["idx"], ref["gate"], ref["inv"])
+    float_check(got["out"], dense, w, "tiny vs brute force")
+
+
+def test_layer_deterministic():
+    w = wl.WORKLOADS["deepseek_v3"].scaled(300)
+    inp = wl.make_inputs(w)
+    _, a = run_layer(w, inp)
+    _, b = run_layer(w, inp)
+    for key in ("out", "logits", "topk_idx", "topk_w", "lse", "prob_mean", "perm", "inv", "f"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    assert a["stats"] == b["stats"]
+
+
+def test_bias_update_bit_exact():
+    w = wl.WORKLOADS["deepseek_v3"].scaled(512)
+    inp = wl.make_inputs(w)
+    layer, got = run_layer(w, inp)
+    b0 = host(layer.sel_bias).copy()
+    moe.bias_update(layer, w.bias_gamma)
+    torch.cuda.synchronize()
+    ref = orc.bias_update(w, got["counts"], b0, w.bias_gamma)
+    np.testing.assert_array_equal(host(layer.sel_bias), ref)
+    # the update moves overloaded experts down and idle ones up by exactly gamma
+    mean = w.T * w.k / w.E
+    d = host(layer.sel_bias) - b0
+    assert np.all(d[got["counts"] > mean] < 0) and np.all(d[got["counts"] < mean] > 0)
+
+
+def test_layer_empty_batch():
+    w = wl.WORKLOADS["quickstart_bf16"].scaled(0)
+    inp = wl.make_inputs(w)
+    _, got = run_layer(w, inp)
+    assert got["out"].shape == (0, w.d)
+    assert got["counts"].tolist() == [0] * w.E
+    assert got["stats"]["total_kept"] == 0
+
+
+def test_layer_single_token_and_k_equals_E():
+    w = wl.Workload("k_eq_E", 60, T=1, d=128, E=4, k=4, F=128, activation=wl.GELU, score_fn=wl.SOFTMAX,
+                    dtype=wl.BF16, router_bias=True, expert_bias=True, residual=True)
+    inp = wl.make_inputs(w)
+    _, got = run_layer(w, inp)
+    check_layer(w, inp, got, np.arange(1))
+
+
+def test_layer_capacity_all_drop_but_capacity():
+    """Every token prefers one expert: exactly C tokens (the first C) are
+    processed by it, the rest output zero (no residual, no shared)."""
+    w = wl.Workload("collapse", 61, T=600, d=128, E=8, k=1, F=128, activation=wl.RELU, score_fn=wl.SOFTMAX,
+                    dtype=wl.BF16, router_bias=True, expert_bias=True, drop_tokens=True,
+                    capacity_factor=1.0, min_capacity=4)
+    inp = wl.make_inputs(w)
+    inp["b_router"] = np.array([0, 0, 0, 40.0, 0, 0, 0, 0], np.float32)
+    _, got = run_layer(w, inp)
+    cap = orc.capacity(w)
+    assert got["kept"].tolist() == [0, 0, 0, cap, 0, 0, 0, 0]
+    assert np.all(got["out"][cap:] == 0.0)
+    check_layer(w, inp, got, np.arange(0, w.T, 7))

@@ -393,3 +393,30 @@ def test_dropped_slot_contributes_nothing():
     dropped = np.nonzero(ref["inv"] < 0)[0]
     assert len(dropped) > 0
     np.testing.assert_array_equal(ref["out"][dropped], 0.0)    # no residual, no shared
+
+
+def test_sigmoid_keys_block_matches_scalar_spec():
+    g = np.random.default_rng(9)
+    lg = g.standard_normal((7, 33)).astype(np.float32) * 4
+    b = g.uniform(-0.1, 0.1, 33).astype(np.float32)
+    keys = orc.sigmoid_keys(lg, b)
+    for t in range(7):
+        for e in range(33):
+            assert keys[t, e] == np.float32(np.float32(orc.sigmoid32(float(lg[t, e]))) + b[e])
+
+
+def test_expert_rows_parallel_equals_single_row():
+    w = _cfg(T=12, d=16, E=3, k=1, F=24, activation=wl.SWIGLU, expert_bias=False, num_shared=1,
+             dtype=wl.BF16)
+    inp = wl.make_inputs(w)
+    X = wl.bf16_to_f32(inp["x"]).astype(np.float64)
+    ex = np.array([0, 2, 1, -1, 0, 2, -1, 1, 1, 0, 2, -1], np.int32)
+    y = orc.expert_rows(w, inp, ex, X)
+    for i, e in enumerate(ex):
+        if e >= 0:
+            np.testing.assert_array_equal(y[i], orc.expert_row(w, inp, e, X[i]))
+    # the shared expert rows equal the layer's shared contribution (routed part removed)
+    lay = orc.layer(w, inp)
+    routed = np.stack([lay["gate"][t, 0] * orc.expert_row(w, inp, lay["idx"][t, 0], X[t]) for t in range(w.T)])
+    shared_rows = np.nonzero(ex == -1)[0]
+    np.testing.assert_allclose(lay["out"][shared_rows] - routed[shared_rows], y[shared_rows], atol=1e-12)
