@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE-layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral]
+                    [--impl ours|reference]
+
+One step is one moe_forward (router -> dispatch -> expert grouped GEMMs ->
+combine -> statistics) over the whole synthetic batch of the workload.  The
+default workload is the Mixtral-8x7B-shaped layer (16384 tokens, d_model
+4096, 8 experts, top-2, SwiGLU d_ff 14336, bf16, residual).  Inputs are
+resident in HBM before the timed region; the 2.82 GB of expert weights and
+the 134 MB activation exceed the 126 MB L2, so every step reads from HBM
+without an explicit flush.
+
+Prints one JSON line (rank 0).  With --gpus N > 1 (under torchrun) every rank
+runs an independent replica of the workload (weak scaling, no collective on
+the data path); the time is the maximum over ranks.
+
+--impl reference times the plain CPU oracle on this machine's host cores on
+a bounded sample of the same workload (full routing of every token plus the
+experts of a sample of tokens, extrapolated to the whole batch).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mixture_experts_60_b300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s on 1 B300; expert GEMM TFLOP/s and % of bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+GEMM_SRC = os.path.join(ROOT, "sparse_mixture_experts_60_b300", "csrc", "gemm_sm103.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+ACT_NAME = {wl.GELU: "gelu", wl.RELU: "relu", wl.SWIGLU: "swiglu"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_of(w):
+    return {"workload": w.name, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d_model": w.d,
+            "experts": w.E, "top_k": w.k, "d_ff": w.F, "activation": ACT_NAME[w.activation],
+            "score": "sigmoid" if w.score_fn == wl.SIGMOID else "softmax",
+            "shared_experts": w.num_shared, "residual": bool(w.residual),
+            "capacity": "dropping" if w.drop_tokens else "none",
+            "l2": "no flush: expert weights (%.2f GB) and x (%.0f MB) exceed L2 and are read every step"
+                  % (weight_bytes(w) / 1e9, w.T * w.d * w.elem_bytes / 1e6)}
+
+
+def weight_bytes(w):
+    mats = (3 if w.gated else 2) * w.E * w.F * w.d + w.E * w.d
+    if w.num_shared:
+        mats += (3 if w.gated else 2) * w.F * w.d
+    return mats * w.elem_bytes
+
+
+def gemm_flops(w, kept_rows):
+    """Algorithmic FLOPs (2 per multiply-add) of the two expert GEMMs."""
+    n1 = (2 if w.gated else 1) * w.F
+    f1 = 2.0 * kept_rows * w.d * n1
+    f2 = 2.0 * kept_rows * w.F * w.d
+    if w.num_shared:
+        f1 += 2.0 * w.T * w.d * n1
+        f2 += 2.0 * w.T * w.F * w.d
+    return f1, f2
+
+
+def hbm_bytes(w, kept_rows):
+    """Algorithmic bytes of the HBM-bound stages (route, dispatch, combine)."""
+    eb = w.elem_bytes
+    T, d, E, S = w.T, w.d, w.E, w.T * w.k
+    route = T * d * eb + E * d * eb + T * E * 4 + S * 8 + T * 4
+    permute = T * d * eb + kept_rows * d * eb + S * 4 * 3 + T * w.k * 4
+    combine = kept_rows * d * 4 + T * d * eb + (T * d * eb if w.residual else 0) + (T * d * 4 if w.num_shared else 0) + S * 8
+    return route, permute, combine
+
+
+def launches_per_step(w):
+    n = 2 if w.E <= 32 else 3            # router (+ logits GEMM) + routing + partial reduce
+    n += 4 if w.T * w.k > 0 else 1       # histogram, scan, rank, row copy
+    n += 2 + (2 if w.num_shared else 0)  # expert GEMMs (+ shared expert)
+    n += 2                               # combine, statistics
+    return n
+
+
+def traffic_for_gemm():
+    """dram bytes per launch of the first expert GEMM from the committed ncu
+    summary, valid only while the kernel source is unchanged."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        t = json.load(f)
+    sha = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
+    if t.get("source_sha256") != sha:
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", self.uuid], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons, pw = [], 0.0, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s, p in zip(sm, pw) if p > 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+def upload(inp, torch):
+    out = {}
+    for k, a in inp.items():
+        if a.dtype == np.uint16:
+            out[k] = torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return out
+
+
+# ---------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, inp, budget_s, n_first=None):
+    """Oracle time for the whole layer from a bounded sample: every token is
+    routed and dispatched, the experts run for a sample of tokens, and the
+    expert time is scaled to all tokens.  Returns (seconds for the layer,
+    sample description, threads)."""
+    from oracle import oracle as orc
+    cores = orc.num_threads()
+    t0 = time.perf_counter()
+    lg = orc.router_logits(w, inp)
+    r = orc.route(w, lg, inp.get("sel_bias"))
+    dsp = orc.dispatch(w, r["idx"])
+    orc.stats(w, dsp["counts"], dsp["kept"], r["prob_sum"], r["lse"])
+    t_route = time.perf_counter() - t0
+    n = n_first or max(1, cores)
+    spent, done = 0.0, 0
+    g = np.random.default_rng(7)
+    while True:
+        toks = np.sort(g.choice(w.T, size=min(n, w.T), replace=False))
+        t1 = time.perf_counter()
+        orc.forward_tokens(w, inp, r["idx"], r["gate"], dsp["inv"], toks)
+        spent += time.perf_counter() - t1
+        done += len(toks)
+        if spent >= budget_s or done >= w.T:
+            break
+        per = spent / done
+        n = int(max(1, min(w.T - done, (budget_s - spent) / per)))
+    total = t_route + spent * w.T / done
+    desc = (f"routing+dispatch of all {w.T} tokens ({t_route:.2f} s) + experts of {done} sampled tokens "
+            f"({spent:.2f} s) scaled to {w.T}")
+    return total, desc, cores
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    inp = wl.make_inputs(w)
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, per_step * 0.5)
+    times, desc, cores = [], "", 1
+    for _ in range(args.steps):
+        t, desc, cores = oracle_sample(w, inp, per_step * 0.5)
+        times.append(t)
+    ms = 1e3 * statistics.mean(times)
+    value = w.T * world / (ms / 1e3) if world > 1 else w.T / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- GPU path
+def run_ours(args, w, rank, world, local):
+    import torch
+    import sparse_mixture_experts_60_b300 as moe
+    from sparse_mixture_experts_60_b300 import build as mbuild
+
+    mbuild.build()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    inp = wl.make_inputs(w)
+    dev = upload(inp, torch)
+    cfg = moe.config_for(w)
+    wts = {k: dev[k] for k in ("w_router", "b_router", "w1", "b1", "w3", "w2", "b2", "shared_w1",
+                               "shared_w3", "shared_w2") if k in dev}
+    layer = moe.MoELayer(cfg, wts, dev.get("sel_bias"))
+    x = dev["x"]
+    out = torch.empty(w.T, w.d, dtype=layer.out_dtype(), device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    def new_events(n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_STAGE_EVENTS)] for _ in range(n)]
+        for row in evs:
+            for e in row:
+                e.record(stream)      # creates the underlying cudaEvent_t
+        torch.cuda.synchronize()
+        return evs, [[e.cuda_event for e in row] for row in evs]
+
+    for _ in range(max(3, args.warmup)):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    code = moe.moe_check_device_error()
+    if code:
+        raise RuntimeError(f"device error flag {code} after warm-up")
+
+    uuid = str(torch.cuda.get_device_properties(local).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+
+    def timed():
+        evs, handles = new_events(args.steps)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        with ClockSampler(uuid) as cs:
+            t0.record(stream)
+            for i in range(args.steps):
+                layer.forward(x, out, stage_events=handles[i])
+            t1.record(stream)
+            barrier()
+        return t0.elapsed_time(t1), evs, cs.summary()
+
+    total_ms, evs, clocks = timed()
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(clocks["reasons"]):
+        total_ms, evs, clocks = timed()          # re-measure once
+        clocks["remeasured"] = True
+    stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)] for i in range(args.steps)])
+    stage_ms = stage.mean(axis=0)               # route, permute, ffn1, ffn2, shared, combine, stats
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    stats = layer.stats()
+    kept = int(stats["total_kept"])
+    code = moe.moe_check_device_error()
+    if code:
+        raise RuntimeError(f"device error flag {code} after the timed region")
+
+    # ----------------------------------------------------------- end to end from host buffers
+    if args.no_e2e:
+        return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, None)
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    n_e2e = max(3, min(args.steps, 50))
+    for _ in range(2):
+        layer.forward_host(x_host, out_host, x_dev, out)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        layer.forward_host(x_host, out_host, x_dev, out)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms)
+
+
+def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms):
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    pk, pk_kind = peaks()
+    f1, f2 = gemm_flops(w, kept)
+    ffn1_ms, ffn2_ms = float(stage_ms[2]), float(stage_ms[3])
+    achieved = f1 / (ffn1_ms * 1e-3) / 1e12
+    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    rb, pb, cb = hbm_bytes(w, kept)
+    hbm_ms = float(stage_ms[0] + stage_ms[1] + stage_ms[5])
+    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gemm_ms = ffn1_ms + ffn2_ms + float(stage_ms[4])
+    line = {
+        "metric": METRIC, "value": w.T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
+        "data": "synthetic", "config": config_of(w),
+        "roofline": {"kernel": "grouped_gemm_kernel (expert W1/W3 + SwiGLU)" if w.gated
+                     else "grouped_gemm_kernel (expert W1 + activation)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_kind": f"bf16_tflops_sustained of {pk_kind}",
+                     "traffic": traffic_for_gemm(), "flops_per_launch": f1, "ms_per_launch": ffn1_ms},
+        "expert_gemm": {"tflops": (f1 + f2) / (gemm_ms * 1e-3) / 1e12,
+                        "frac_of_bf16_sustained": (f1 + f2) / (gemm_ms * 1e-3) / 1e12 / peak,
+                        "ms": gemm_ms, "kept_rows": kept},
+        "hbm_stages": {"gbs": (rb + pb + cb) / (hbm_ms * 1e-3) / 1e9, "peak_gbs": hbm_peak,
+                       "frac": (rb + pb + cb) / (hbm_ms * 1e-3) / 1e9 / hbm_peak, "ms": hbm_ms,
+                       "route_gbs": rb / (stage_ms[0] * 1e-3) / 1e9,
+                       "permute_gbs": pb / (stage_ms[1] * 1e-3) / 1e9,
+                       "combine_gbs": cb / (stage_ms[5] * 1e-3) / 1e9},
+        "stage_ms": {"route": stage_ms[0], "permute": stage_ms[1], "ffn1": ffn1_ms, "ffn2": ffn2_ms,
+                     "shared": stage_ms[4], "combine": stage_ms[5], "stats": stage_ms[6]},
+        "clocks": clocks,
+        "e2e": None if e2e_ms is None else {
+            "value": w.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(x.numel() * x.element_size()),
+            "d2h_bytes_per_step": int(out.numel() * out.element_size()), "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step(w) * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        t, desc, cores = oracle_sample(w, inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": w.T / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line, default=float), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=150)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the token count (profiling of a smaller case; not a headline)")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    w = wl.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = w.scaled(args.tokens)
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+    return run_ours(args, w, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

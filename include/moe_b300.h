@@ -128,7 +128,13 @@ typedef struct {
 /* Intermediate results of moe_forward.  Each pointer may be NULL, in which
  * case the value is kept in the workspace instead.  Shapes: logits [T,E],
  * topk_idx/topk_w/inv [T*k], lse [T], prob_mean/counts/kept/f [E],
- * offsets [E+1], perm [T*k], stats one moe_stats_t. */
+ * offsets [E+1], perm [T*k], stats one moe_stats_t.
+ * stage_events: optional host array of MOE_STAGE_EVENTS cudaEvent_t handles
+ * (created by the caller) that moe_forward records on its stream at the
+ * stage boundaries: [0] start, [1] routed, [2] dispatched, [3] expert
+ * first GEMM (W1/W3 + activation) done, [4] expert second GEMM done,
+ * [5] shared expert done, [6] combined, [7] statistics done.  NULL: none. */
+#define MOE_STAGE_EVENTS 8
 typedef struct {
     float *logits;
     int32_t *topk_idx;
@@ -142,6 +148,7 @@ typedef struct {
     int32_t *inv;
     float *f;
     moe_stats_t *stats;
+    void *const *stage_events;
 } moe_forward_io_t;
 
 /* Which call a workspace is sized for. */

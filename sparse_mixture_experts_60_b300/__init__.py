@@ -16,8 +16,8 @@ from __future__ import annotations
 import ctypes as C
 from typing import Dict, Optional
 
-from ._lib import (MOE_WS_EXPERT_FFN, MOE_WS_FORWARD, MOE_WS_PERMUTE, MOE_WS_ROUTE,  # noqa: F401
-                   MOE_WS_SHARED_FFN, MoEConfig, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
+from ._lib import (MOE_STAGE_EVENTS, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD, MOE_WS_PERMUTE,  # noqa: F401
+                   MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
                    last_error, lib)
 
 SOFTMAX, SIGMOID = 0, 1
@@ -135,19 +135,29 @@ def weights_struct(w: Dict) -> MoEWeights:
                       shared_w2=_ptr(g("shared_w2")))
 
 
-def io_struct(io: Optional[Dict]) -> Optional[MoEForwardIO]:
-    if io is None:
+def io_struct(io: Optional[Dict], stage_events=None) -> Optional[MoEForwardIO]:
+    """``stage_events``: None or a sequence of MOE_STAGE_EVENTS raw
+    cudaEvent_t handles (ints), recorded by moe_forward at stage boundaries."""
+    if io is None and stage_events is None:
         return None
-    return MoEForwardIO(**{k: _ptr(io.get(k)) for k, _ in MoEForwardIO._fields_})
+    io = io or {}
+    s = MoEForwardIO(**{k: _ptr(io.get(k)) for k, _ in MoEForwardIO._fields_ if k != "stage_events"})
+    if stage_events is not None:
+        arr = (C.c_void_p * MOE_STAGE_EVENTS)(*[int(e) for e in stage_events])
+        s._events_keepalive = arr
+        s.stage_events = C.cast(arr, C.c_void_p)
+    return s
 
 
-def moe_forward(cfg, weights: Dict, x, sel_bias, out, io: Optional[Dict], ws, stream=None) -> None:
+def moe_forward(cfg, weights: Dict, x, sel_bias, out, io: Optional[Dict], ws, stream=None,
+                stage_events=None) -> None:
     """``weights``: dict of CUDA tensors keyed like ``MoEWeights`` fields;
     ``io``: dict of optional intermediate output tensors keyed like
-    ``MoEForwardIO`` fields (missing keys stay in the workspace)."""
+    ``MoEForwardIO`` fields (missing keys stay in the workspace);
+    ``stage_events``: optional MOE_STAGE_EVENTS raw cudaEvent_t handles."""
     p, n = _ws(ws)
     wst = weights_struct(weights)
-    ios = io_struct(io)
+    ios = io_struct(io, stage_events)
     check(lib().moe_forward(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(sel_bias), _ptr(out),
                             C.byref(ios) if ios is not None else None, p, n, _stream(stream)))
 
@@ -198,12 +208,12 @@ class MoELayer:
         import torch
         return torch.float32 if self.cfg.dtype == F32 else torch.bfloat16
 
-    def forward(self, x, out=None, stream=None):
+    def forward(self, x, out=None, stream=None, stage_events=None):
         import torch
         if out is None:
             out = torch.empty(self.cfg.num_tokens, self.cfg.d_model, dtype=self.out_dtype(),
                               device=self.device)
-        moe_forward(self.cfg, self.weights, x, self.sel_bias, out, self.io, self.ws, stream)
+        moe_forward(self.cfg, self.weights, x, self.sel_bias, out, self.io, self.ws, stream, stage_events)
         return out
 
     def forward_host(self, x_host, out_host, x_dev=None, out_dev=None, stream=None):

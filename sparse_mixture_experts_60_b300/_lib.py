@@ -38,9 +38,13 @@ class MoEWeights(C.Structure):
                                           "shared_w1", "shared_w3", "shared_w2")]
 
 
+MOE_STAGE_EVENTS = 8
+
+
 class MoEForwardIO(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("logits", "topk_idx", "topk_w", "lse", "prob_mean",
-                                          "counts", "kept", "offsets", "perm", "inv", "f", "stats")]
+                                          "counts", "kept", "offsets", "perm", "inv", "f", "stats",
+                                          "stage_events")]
 
 
 class MoEError(RuntimeError):

@@ -201,7 +201,7 @@ moe_status_t permute_impl(const moe_config_t *c, const void *x, const int32_t *t
 // Two-layer FFN over row groups (routed: seg = offsets, G = E; shared: seg = null).
 moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, const int32_t *seg, int G, int M,
                       const void *w1, const void *b1, const void *w3, const void *w2, const void *b2, void *H,
-                      float *y, cudaStream_t s) {
+                      float *y, cudaStream_t s, void *mid_event = nullptr) {
     const int d = c->d_model, F = c->d_ff;
     const int gated = c->activation == MOE_ACT_SWIGLU;
     const int act = c->activation == MOE_ACT_GELU ? 1 : (c->activation == MOE_ACT_RELU ? 2 : 0);
@@ -229,6 +229,7 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
         g1.gated = gated;
         e = launch_grouped_gemm(g1, s);
         if (e != cudaSuccess) return cuda_status(e, "expert FFN1 launch");
+        if (mid_event) cudaEventRecord(static_cast<cudaEvent_t>(mid_event), s);
         GemmProblem g2{};
         g2.A = static_cast<const bf16 *>(H);
         g2.a_rows = a_rows;
@@ -268,6 +269,7 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
     p1.gated = gated;
     e = launch_ffn_simt(p1, s);
     if (e != cudaSuccess) return cuda_status(e, "expert FFN1 launch");
+    if (mid_event) cudaEventRecord(static_cast<cudaEvent_t>(mid_event), s);
     SimtProblem p2{};
     p2.A = static_cast<const float *>(H);
     p2.B = static_cast<const float *>(w2);
@@ -286,10 +288,14 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
     return cuda_status(launch_ffn_simt(p2, s), "expert FFN2 launch");
 }
 
-moe_status_t need(const void *p, const char *name) {
+// A buffer of n > 0 elements must be non-NULL (16-byte aligned for need16);
+// an empty buffer (n == 0) may be NULL.
+moe_status_t need(const void *p, const char *name, int64_t n = 1) {
+    if (n == 0) return MOE_OK;
     return p ? MOE_OK : fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
 }
-moe_status_t need16(const void *p, const char *name) {
+moe_status_t need16(const void *p, const char *name, int64_t n = 1) {
+    if (n == 0 && !p) return MOE_OK;
     if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
     return aligned16(p) ? MOE_OK : fail(MOE_ERR_BAD_ALIGNMENT, "%s is not 16-byte aligned", name);
 }
@@ -346,12 +352,13 @@ moe_status_t moe_route(const moe_config_t *cfg, const void *x, const void *w_rou
                        const float *sel_bias, float *logits, int32_t *topk_idx, float *topk_w, float *lse,
                        float *prob_mean, int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
-    TRY(need16(x, "x"));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    TRY(need16(x, "x", T));
     TRY(need16(w_router, "w_router"));
-    TRY(need(logits, "logits"));
-    TRY(need(topk_idx, "topk_idx"));
-    TRY(need(topk_w, "topk_w"));
-    TRY(need(lse, "lse"));
+    TRY(need(logits, "logits", T));
+    TRY(need(topk_idx, "topk_idx", S));
+    TRY(need(topk_w, "topk_w", S));
+    TRY(need(lse, "lse", T));
     TRY(need(prob_mean, "prob_mean"));
     TRY(need(counts, "counts"));
     if (cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
@@ -365,10 +372,11 @@ moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits,
                                    int32_t *topk_idx, float *topk_w, float *lse, float *prob_mean,
                                    int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
-    TRY(need(logits, "logits"));
-    TRY(need(topk_idx, "topk_idx"));
-    TRY(need(topk_w, "topk_w"));
-    TRY(need(lse, "lse"));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    TRY(need(logits, "logits", T));
+    TRY(need(topk_idx, "topk_idx", S));
+    TRY(need(topk_w, "topk_w", S));
+    TRY(need(lse, "lse", T));
     TRY(need(prob_mean, "prob_mean"));
     TRY(need(counts, "counts"));
     if (cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
@@ -382,14 +390,15 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *
                          int32_t *kept, int32_t *offsets, int32_t *perm, int32_t *inv, void *x_perm, void *ws,
                          size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
-    TRY(need16(x, "x"));
-    TRY(need(topk_idx, "topk_idx"));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    TRY(need16(x, "x", T));
+    TRY(need(topk_idx, "topk_idx", S));
     TRY(need(counts, "counts"));
     TRY(need(kept, "kept"));
     TRY(need(offsets, "offsets"));
-    TRY(need(perm, "perm"));
-    TRY(need(inv, "inv"));
-    TRY(need16(x_perm, "x_perm"));
+    TRY(need(perm, "perm", S));
+    TRY(need(inv, "inv", S));
+    TRY(need16(x_perm, "x_perm", S));
     TRY(need_ws(ws, ws_bytes, permute_ws(cfg)));
     return permute_impl(cfg, x, topk_idx, counts, kept, offsets, perm, inv, x_perm, ws,
                         static_cast<cudaStream_t>(stream));
@@ -399,12 +408,13 @@ moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const i
                             const void *b1, const void *w3, const void *w2, const void *b2, float *y_perm,
                             void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
-    TRY(need16(x_perm, "x_perm"));
+    const int64_t S = cfg->num_tokens * cfg->top_k;
+    TRY(need16(x_perm, "x_perm", S));
     TRY(need(offsets, "offsets"));
     TRY(check_weights_ffn(cfg, w1, w3, w2));
     TRY(check_bias(b1));
     TRY(check_bias(b2));
-    TRY(need16(y_perm, "y_perm"));
+    TRY(need16(y_perm, "y_perm", S));
     TRY(need_ws(ws, ws_bytes, ffn_ws(cfg)));
     return ffn_impl(cfg, x_perm, cfg->num_tokens * cfg->top_k, offsets, cfg->num_experts, 0, w1, b1, w3, w2, b2,
                     ws, y_perm, static_cast<cudaStream_t>(stream));
@@ -414,9 +424,9 @@ moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *
                             const void *shared_w2, float *z, void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     if (cfg->num_shared != 1) return fail(MOE_ERR_INVALID_ARG, "moe_shared_ffn needs num_shared = 1");
-    TRY(need16(x, "x"));
+    TRY(need16(x, "x", cfg->num_tokens));
     TRY(check_weights_ffn(cfg, shared_w1, shared_w3, shared_w2));
-    TRY(need16(z, "z"));
+    TRY(need16(z, "z", cfg->num_tokens));
     TRY(need_ws(ws, ws_bytes, shared_ws(cfg)));
     return ffn_impl(cfg, x, cfg->num_tokens, nullptr, 1, (int)cfg->num_tokens, shared_w1, nullptr, shared_w3,
                     shared_w2, nullptr, ws, z, static_cast<cudaStream_t>(stream));
@@ -425,12 +435,13 @@ moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *
 moe_status_t moe_combine(const moe_config_t *cfg, const float *y_perm, const int32_t *inv, const float *topk_w,
                          const float *shared_out, const void *x, void *out, moe_stream_t stream) {
     TRY(check_cfg(cfg));
-    TRY(need16(y_perm, "y_perm"));
-    TRY(need(inv, "inv"));
-    TRY(need(topk_w, "topk_w"));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    TRY(need16(y_perm, "y_perm", S));
+    TRY(need(inv, "inv", S));
+    TRY(need(topk_w, "topk_w", S));
     if (shared_out) TRY(need16(shared_out, "shared_out"));
-    if (cfg->residual) TRY(need16(x, "x (residual)"));
-    TRY(need16(out, "out"));
+    if (cfg->residual) TRY(need16(x, "x (residual)", T));
+    TRY(need16(out, "out", T));
     return cuda_status(launch_combine(cfg->num_tokens, cfg->d_model, cfg->top_k, cfg->dtype, y_perm, inv, topk_w,
                                       shared_out, cfg->residual ? x : nullptr, out,
                                       static_cast<cudaStream_t>(stream)),
@@ -475,8 +486,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const 
                          void *out, const moe_forward_io_t *io, void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     TRY(need(w, "weights"));
-    TRY(need16(x, "x"));
-    TRY(need16(out, "out"));
+    TRY(need16(x, "x", cfg->num_tokens));
+    TRY(need16(out, "out", cfg->num_tokens));
     TRY(need16(w->w_router, "w_router"));
     TRY(check_weights_ffn(cfg, w->w1, w->w3, w->w2));
     TRY(check_bias(w->b1));
@@ -522,17 +533,27 @@ moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const 
     if (!o.offsets) o.offsets = off_ws;
     if (!o.stats) o.stats = st_ws;
 
+    void *const *ev = o.stage_events;
+    auto mark = [&](int i) {
+        if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+    };
+    mark(0);
     TRY(route_impl(c, x, w->w_router, w->b_router, c->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr, o.logits,
                    nullptr, o.topk_idx, o.topk_w, o.lse, o.prob_mean, o.counts, ws_route, s));
+    mark(1);
     TRY(permute_impl(c, x, o.topk_idx, o.counts, o.kept, o.offsets, o.perm, o.inv, x_perm, ws_perm, s));
+    mark(2);
     TRY(ffn_impl(c, x_perm, (int64_t)S, o.offsets, c->num_experts, 0, w->w1, w->b1, w->w3, w->w2, w->b2, ws_ffn,
-                 y_perm, s));
+                 y_perm, s, ev ? ev[3] : nullptr));
+    mark(4);
     if (c->num_shared)
         TRY(ffn_impl(c, x, (int64_t)T, nullptr, 1, (int)T, w->shared_w1, nullptr, w->shared_w3, w->shared_w2,
                      nullptr, ws_shared, z, s));
+    mark(5);
     TRY(cuda_status(launch_combine(c->num_tokens, c->d_model, c->top_k, c->dtype, y_perm, o.inv, o.topk_w, z,
                                    c->residual ? x : nullptr, out, s),
                     "combine launch"));
+    mark(6);
     StatsParams sp{};
     sp.T = c->num_tokens;
     sp.E = c->num_experts;
@@ -545,7 +566,9 @@ moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const 
     sp.lse = o.lse;
     sp.f = o.f;
     sp.stats = o.stats;
-    return cuda_status(launch_stats(sp, s), "stats launch");
+    TRY(cuda_status(launch_stats(sp, s), "stats launch"));
+    mark(7);
+    return MOE_OK;
 }
 
 moe_status_t moe_check_device_error(int32_t *code) {

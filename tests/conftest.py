@@ -24,3 +24,17 @@ def golden():
             return json.load(f)
 
     return load
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the float-parity margins of the GPU tests (if any ran)."""
+    mod = sys.modules.get("tests.gpu_util")
+    rep = getattr(mod, "REPORT", None) if mod else None
+    if not rep:
+        return
+    out = os.path.join(ROOT, "gpurun_out")
+    os.makedirs(out, exist_ok=True)
+    name = os.environ.get("PARITY_REPORT", "parity_report.txt")
+    with open(os.path.join(out, name), "a") as f:
+        for what, err, rms, ratio in rep:
+            f.write(f"{what}\tmax_err={err:.4e}\trms={rms:.4e}\tratio={ratio:.4e}\n")

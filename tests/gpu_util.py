@@ -17,6 +17,7 @@ from sparse_mixture_experts_60_b300 import workloads as wl
 
 FP32_REL = 1e-4
 BF16_OF_RMS = 2e-2
+REPORT = []   # (what, max_err, rms, ratio) of every float check, written at session end
 WEIGHT_KEYS = ("w_router", "b_router", "w1", "b1", "w3", "w2", "b2", "shared_w1", "shared_w3", "shared_w2")
 
 
@@ -58,8 +59,10 @@ def float_check(gpu, ref, w, what="", report=None):
     else:
         ratio = float(err.max() / rms) if r.size else 0.0
         ok = ratio <= BF16_OF_RMS
+    rec = (what, float(err.max()) if r.size else 0.0, rms, ratio)
+    REPORT.append(rec)
     if report is not None:
-        report.append((what, float(err.max()) if r.size else 0.0, rms, ratio))
+        report.append(rec)
     assert ok, f"{what}: max err {err.max():.3e} rms {rms:.3e} ratio {ratio:.3e}"
     return float(err.max()) if r.size else 0.0, rms, ratio
 

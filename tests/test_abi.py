@@ -49,7 +49,7 @@ def test_struct_layouts_match_header():
     assert C.sizeof(_lib.MoEConfig) == 64
     assert C.sizeof(_lib.MoEStats) == 32
     assert C.sizeof(_lib.MoEWeights) == 80
-    assert C.sizeof(_lib.MoEForwardIO) == 96
+    assert C.sizeof(_lib.MoEForwardIO) == 104
 
 
 def _ws_expect(w):

@@ -111,12 +111,22 @@ def check_route_from_x(w, inp, got, report=None):
     ref = orc.route(w, ref_lg, sb)
     keys = keys_of(w, ref_lg, sb)
     srt = -np.sort(-keys, axis=1)
-    gap = srt[:, w.k - 1] - (srt[:, w.k] if w.k < w.E else -np.inf)
-    clear = gap > margin
+    k = w.k
+    # set boundary: k-th vs (k+1)-th key; order: every adjacent gap in the top k (+1)
+    set_gap = srt[:, k - 1] - (srt[:, k] if k < w.E else -np.inf)
+    ext = np.concatenate([srt[:, :k], (srt[:, k:k + 1] if k < w.E else np.full((w.T, 1), -np.inf))], axis=1)
+    order_gap = np.min(ext[:, :-1] - ext[:, 1:], axis=1)
+    clear = order_gap > margin
+    set_clear = set_gap > margin
     np.testing.assert_array_equal(got["idx"][clear], ref["idx"][clear])
     for t in np.nonzero(~clear)[0]:
-        assert len(set(got["idx"][t])) == w.k
-        assert topk_valid(got["idx"][t], keys[t], margin), t
+        sel = got["idx"][t]
+        assert len(set(sel)) == k
+        if set_clear[t]:
+            assert sorted(sel) == sorted(ref["idx"][t]), t
+        assert topk_valid(sel, keys[t], margin), t
+        ks = keys[t][sel]
+        assert np.all(ks[:-1] >= ks[1:] - margin), t          # descending within the margin
     np.testing.assert_array_equal(got["counts"], np.bincount(got["idx"].reshape(-1), minlength=w.E))
     # gates / lse / P from the GPU's own logits within fp32 rounding of the oracle's
     np.testing.assert_allclose(got["lse"][clear], ref["lse"][clear], rtol=1e-5, atol=1e-5)
