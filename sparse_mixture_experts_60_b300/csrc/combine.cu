@@ -115,31 +115,38 @@ __device__ T block_reduce(T v, T *sm, Op op) {
     return r;
 }
 
-struct AddD { __device__ double operator()(double a, double b) const { return a + b; } };
+struct AddF { __device__ float operator()(float a, float b) const { return a + b; } };
 struct AddL { __device__ long long operator()(long long a, long long b) const { return a + b; } };
 struct MaxL { __device__ long long operator()(long long a, long long b) const { return a > b ? a : b; } };
 struct MinL { __device__ long long operator()(long long a, long long b) const { return a < b ? a : b; } };
 
+// Single CTA, fp32 throughout (Kahan-compensated per-thread sums, then
+// fixed-order tree reductions): deterministic and free of fp64.
 __global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
-    __shared__ double sd[32];
+    __shared__ float sf[32];
     __shared__ long long sl[32];
     const int64_t S = p.T * p.k;
-    double z = 0.0;
-    for (int64_t i = threadIdx.x; i < p.T; i += blockDim.x) z += (double)p.lse[i] * (double)p.lse[i];
-    z = block_reduce(z, sd, AddD());
-    double aux = 0.0;
+    float z = 0.0f, zc = 0.0f;
+    for (int64_t i = threadIdx.x; i < p.T; i += blockDim.x) {
+        const float v = p.lse[i] * p.lse[i] - zc;
+        const float t = z + v;
+        zc = (t - z) - v;
+        z = t;
+    }
+    z = block_reduce(z, sf, AddF());
+    float aux = 0.0f;
     long long dropped = 0, used = 0, kept_tot = 0, kmax = 0, kmin = 0x7fffffffffffffffLL;
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-        const double f = S > 0 ? (double)p.counts[e] / (double)S : 0.0;
-        if (p.f) p.f[e] = (float)f;
-        aux += f * (double)p.prob_mean[e];
+        const float f = S > 0 ? (float)p.counts[e] / (float)S : 0.0f;
+        if (p.f) p.f[e] = f;
+        aux += f * p.prob_mean[e];
         dropped += p.counts[e] - p.kept[e];
         used += p.kept[e] > 0;
         kept_tot += p.kept[e];
         kmax = p.kept[e] > kmax ? p.kept[e] : kmax;
         kmin = p.kept[e] < kmin ? p.kept[e] : kmin;
     }
-    aux = block_reduce(aux, sd, AddD());
+    aux = block_reduce(aux, sf, AddF());
     dropped = block_reduce(dropped, sl, AddL());
     used = block_reduce(used, sl, AddL());
     kept_tot = block_reduce(kept_tot, sl, AddL());
@@ -147,11 +154,11 @@ __global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
     kmin = block_reduce(kmin, sl, MinL());
     if (threadIdx.x == 0) {
         moe_stats_t st;
-        st.aux_loss = (float)((double)p.E * aux);
-        st.z_loss = p.T > 0 ? (float)(z / (double)p.T) : 0.0f;
-        st.imbalance = kmin > 0 ? (float)((double)kmax / (double)kmin) : INFINITY;
-        st.utilization = (float)((double)used / (double)p.E);
-        st.drop_rate = S > 0 ? (float)((double)dropped / (double)S) : 0.0f;
+        st.aux_loss = (float)p.E * aux;
+        st.z_loss = p.T > 0 ? z / (float)p.T : 0.0f;
+        st.imbalance = kmin > 0 ? (float)kmax / (float)kmin : INFINITY;
+        st.utilization = (float)used / (float)p.E;
+        st.drop_rate = S > 0 ? (float)dropped / (float)S : 0.0f;
         st.dropped = (int32_t)dropped;
         st.capacity = p.drop ? (int32_t)p.cap : -1;
         st.total_kept = (int32_t)kept_tot;

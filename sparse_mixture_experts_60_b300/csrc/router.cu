@@ -176,9 +176,18 @@ __device__ __forceinline__ void write_partials(const RouteParams &p, float (&psu
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         float acc = 0.0f;
         for (int w = 0; w < 8; ++w) acc += s_prob[w * EP + e];
-        p.part_prob[(int64_t)blockIdx.x * p.E + e] = acc;
-        p.part_cnt[(int64_t)blockIdx.x * p.E + e] = s_cnt[e];
+        p.part_prob[(int64_t)e * gridDim.x + blockIdx.x] = acc;   // [E][blocks]
+        p.part_cnt[(int64_t)e * gridDim.x + blockIdx.x] = s_cnt[e];
     }
+}
+
+// 16-byte global load that is not allocated in L1 (read-once stream).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
 }
 
 template <typename Tin>
@@ -225,7 +234,7 @@ __device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 // E <= EP <= 32: logits from x on the CUDA cores (the router is read from
 // L1, x streamed once with 16-byte loads), then routing in registers.
 template <typename Tin, int EP>
-__global__ void __launch_bounds__(256) router_fused_kernel(RouteParams p) {
+__global__ void __launch_bounds__(256, EP <= 16 ? 2 : 1) router_fused_kernel(RouteParams p) {
     constexpr int TPW = 32 / EP;            // tokens per warp per round
     constexpr int VN = Vec<Tin>::N;
     __shared__ float s_prob[8 * EP];
@@ -246,24 +255,39 @@ __global__ void __launch_bounds__(256) router_fused_kernel(RouteParams p) {
         float acc[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-        for (int v = lane; v < nvec; v += 32) {
-            float xf[TPW][VN];
+        // U iterations of x loads are issued before any arithmetic, so each
+        // lane keeps U*TPW 16-byte loads in flight (x is streamed past L1,
+        // which keeps the router weights resident there)
+        constexpr int U = 4;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+            uint4 xr[U][TPW];
 #pragma unroll
-            for (int ti = 0; ti < TPW; ++ti) {
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (t0 + ti < p.T)
-                    u = __ldg(reinterpret_cast<const uint4 *>(x + (t0 + ti) * d) + v);
-                Vec<Tin>::unpack(u, xf[ti]);
-            }
+            for (int u = 0; u < U; ++u)
 #pragma unroll
-            for (int e = 0; e < EP; ++e) {
-                if (e < E) {
-                    float wf[VN];
-                    Vec<Tin>::unpack(__ldg(reinterpret_cast<const uint4 *>(W + (int64_t)e * d) + v), wf);
+                for (int ti = 0; ti < TPW; ++ti) {
+                    const int v = v0 + 32 * u;
+                    xr[u][ti] = (v < nvec && t0 + ti < p.T)
+                                    ? ld_stream(reinterpret_cast<const uint4 *>(x + (t0 + ti) * d) + v)
+                                    : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
-                    for (int ti = 0; ti < TPW; ++ti)
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= nvec) break;
+                float xf[TPW][VN];
 #pragma unroll
-                        for (int q = 0; q < VN; ++q) acc[ti * EP + e] = fmaf(xf[ti][q], wf[q], acc[ti * EP + e]);
+                for (int ti = 0; ti < TPW; ++ti) Vec<Tin>::unpack(xr[u][ti], xf[ti]);
+#pragma unroll
+                for (int e = 0; e < EP; ++e) {
+                    if (e < E) {
+                        float wf[VN];
+                        Vec<Tin>::unpack(__ldg(reinterpret_cast<const uint4 *>(W + (int64_t)e * d) + v), wf);
+#pragma unroll
+                        for (int ti = 0; ti < TPW; ++ti)
+#pragma unroll
+                            for (int q = 0; q < VN; ++q)
+                                acc[ti * EP + e] = fmaf(xf[ti][q], wf[q], acc[ti * EP + e]);
+                    }
                 }
             }
         }
@@ -354,18 +378,34 @@ __global__ void __launch_bounds__(256) router_logits_simt_kernel(const Tin *x, c
     }
 }
 
-__global__ void route_reduce_kernel(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
-                                    int E, int64_t T, float *prob_mean, int32_t *counts) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    double s = 0.0;
-    int64_t c = 0;
-    for (int64_t b = 0; b < nblk; ++b) {
-        s += (double)part_prob[b * E + e];
-        c += part_cnt[b * E + e];
+// One CTA per expert: fixed strided fp32 sums per thread, then a fixed
+// shared-memory tree (deterministic).
+__global__ void __launch_bounds__(256) route_reduce_kernel(const float *part_prob, const int32_t *part_cnt,
+                                                           int64_t nblk, int E, int64_t T, float *prob_mean,
+                                                           int32_t *counts) {
+    __shared__ float sp[256];
+    __shared__ int sc[256];
+    const int e = blockIdx.x;
+    float s = 0.0f;
+    int c = 0;
+    for (int64_t b = threadIdx.x; b < nblk; b += blockDim.x) {
+        s += part_prob[(int64_t)e * nblk + b];
+        c += part_cnt[(int64_t)e * nblk + b];
     }
-    prob_mean[e] = T > 0 ? (float)(s / (double)T) : 0.0f;
-    counts[e] = (int32_t)c;
+    sp[threadIdx.x] = s;
+    sc[threadIdx.x] = c;
+    __syncthreads();
+    for (int st = 128; st > 0; st >>= 1) {
+        if (threadIdx.x < st) {
+            sp[threadIdx.x] += sp[threadIdx.x + st];
+            sc[threadIdx.x] += sc[threadIdx.x + st];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        prob_mean[e] = T > 0 ? sp[0] / (float)T : 0.0f;
+        counts[e] = sc[0];
+    }
 }
 
 template <int G, int VPL>
@@ -426,8 +466,7 @@ cudaError_t launch_router_logits_simt(const RouteParams &p, int dtype, cudaStrea
 cudaError_t launch_route_reduce(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
                                 int E, int64_t T, float *prob_mean, int32_t *counts,
                                 cudaStream_t s) {
-    route_reduce_kernel<<<(unsigned)ceil_div(E, 256), 256, 0, s>>>(part_prob, part_cnt, nblk, E, T,
-                                                                   prob_mean, counts);
+    route_reduce_kernel<<<(unsigned)E, 256, 0, s>>>(part_prob, part_cnt, nblk, E, T, prob_mean, counts);
     return cudaGetLastError();
 }
 
