@@ -216,6 +216,32 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *
                          moe_stream_t stream);
 
 /*
+ * moe_permute without a workspace, for callers that cannot allocate device
+ * memory: code embedded in a host runtime that hands it only its input and
+ * output buffers and no allocator (a plugin or custom operator of an
+ * inference engine), or that must not allocate after start-up because it
+ * runs under a fixed memory budget or latency limit (cudaMalloc and cudaFree
+ * can synchronise the device or fail).  The pages have no counterpart; this
+ * is a deployment variant of moe_permute.
+ *   Same arguments, outputs and results as moe_permute, minus the
+ *   workspace.  The two scratch tables live in a 512 KB array of the
+ *   library's own device memory (a file-scope __device__ array, present on
+ *   every device that loads the library until the process exits).
+ *   Limit: ceil(num_tokens * top_k / 2048) * num_experts <= 65536 (for
+ *   example T*k <= 16.7M slots at E = 8, <= 524288 at E = 256); larger
+ *   layers return MOE_ERR_UNSUPPORTED and must use moe_permute.
+ *   The first call on a device looks the array's address up
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  No call allocates or frees device memory.
+ *   All calls share the array: every call writes the parts it reads, so
+ *   nothing has to be cleared between calls, but calls that overlap on the
+ *   GPU (concurrent streams, or several host threads) race on it.
+ */
+moe_status_t moe_permute_noalloc(const moe_config_t *cfg, const void *x, const int32_t *topk_idx,
+                                 int32_t *counts, int32_t *kept, int32_t *offsets, int32_t *perm,
+                                 int32_t *inv, void *x_perm, moe_stream_t stream);
+
+/*
  * Routed experts as a grouped GEMM over the segments of x_perm:
  * for rows offsets[e] .. offsets[e+1]-1,
  *   GELU/ReLU: y = W2_e act(W1_e x + b1_e) + b2_e

@@ -99,6 +99,14 @@ def moe_permute(cfg, x, topk_idx, counts, kept, offsets, perm, inv, x_perm, ws, 
                             _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm), p, n, _stream(stream)))
 
 
+def moe_permute_noalloc(cfg, x, topk_idx, counts, kept, offsets, perm, inv, x_perm, stream=None) -> None:
+    """moe_permute without a workspace: for callers that cannot allocate
+    device memory (the scratch is a fixed 512 KB array inside the library;
+    see include/moe_b300.h for the size limit and the first-call set-up)."""
+    check(lib().moe_permute_noalloc(C.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(kept),
+                                    _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm), _stream(stream)))
+
+
 def moe_expert_ffn(cfg, x_perm, offsets, w1, b1, w3, w2, b2, y_perm, ws, stream=None) -> None:
     p, n = _ws(ws)
     check(lib().moe_expert_ffn(C.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(w1), _ptr(b1), _ptr(w3),

@@ -64,6 +64,7 @@ _SIGS = {
     "moe_route": ([P] * 11 + [P, C.c_size_t, P], C.c_int),
     "moe_route_from_logits": ([P] * 8 + [P, C.c_size_t, P], C.c_int),
     "moe_permute": ([P] * 9 + [P, C.c_size_t, P], C.c_int),
+    "moe_permute_noalloc": ([P] * 9 + [P], C.c_int),
     "moe_expert_ffn": ([P] * 9 + [P, C.c_size_t, P], C.c_int),
     "moe_shared_ffn": ([P] * 6 + [P, C.c_size_t, P], C.c_int),
     "moe_combine": ([P] * 7 + [P], C.c_int),

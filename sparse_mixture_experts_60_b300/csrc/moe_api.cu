@@ -404,6 +404,47 @@ moe_status_t moe_permute(const moe_config_t *cfg, const void *x, const int32_t *
                         static_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_permute_noalloc(const moe_config_t *cfg, const void *x, const int32_t *topk_idx, int32_t *counts,
+                                 int32_t *kept, int32_t *offsets, int32_t *perm, int32_t *inv, void *x_perm,
+                                 moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    TRY(need16(x, "x", T));
+    TRY(need(topk_idx, "topk_idx", S));
+    TRY(need(counts, "counts"));
+    TRY(need(kept, "kept"));
+    TRY(need(offsets, "offsets"));
+    TRY(need(perm, "perm", S));
+    TRY(need(inv, "inv", S));
+    TRY(need16(x_perm, "x_perm", S));
+    const int64_t table = perm_chunks(cfg) * cfg->num_experts;
+    if (2 * table > kPermStaticScratchInts)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "moe_permute_noalloc: ceil(num_tokens*top_k/%d) * num_experts = %lld exceeds the static "
+                    "scratch limit of %lld; use moe_permute with a workspace",
+                    kPermChunk, (long long)table, (long long)(kPermStaticScratchInts / 2));
+    int32_t *scratch = permute_static_scratch();
+    if (!scratch) return fail(MOE_ERR_CUDA, "moe_permute_noalloc: cudaGetSymbolAddress of the scratch failed");
+    PermuteParams p{};
+    p.T = T;
+    p.E = cfg->num_experts;
+    p.k = cfg->top_k;
+    p.d = cfg->d_model;
+    p.dtype = cfg->dtype;
+    p.cap = capacity_of(cfg);
+    p.x = x;
+    p.topk_idx = topk_idx;
+    p.counts = counts;
+    p.kept = kept;
+    p.offsets = offsets;
+    p.perm = perm;
+    p.inv = inv;
+    p.x_perm = x_perm;
+    p.hist = scratch;
+    p.base = scratch + table;
+    return cuda_status(launch_permute(p, static_cast<cudaStream_t>(stream)), "moe_permute_noalloc launch");
+}
+
 moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
                             const void *b1, const void *w3, const void *w2, const void *b2, float *y_perm,
                             void *ws, size_t ws_bytes, moe_stream_t stream) {

@@ -38,8 +38,8 @@ struct RouteParams {
     int32_t *topk_idx;
     float *topk_w;
     float *lse;
-    float *part_prob;      // [nblk, E]
-    int32_t *part_cnt;     // [nblk, E]
+    float *part_prob;      // [E, nblk] per-CTA sums of softmax probabilities
+    int32_t *part_cnt;     // [E, nblk] per-CTA expert counts
 };
 // E <= 32: one kernel computes logits from x and routes (dtype 0 f32, 1 bf16)
 cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s);
@@ -65,6 +65,10 @@ struct PermuteParams {
     int32_t *base;         // [nchunk, E] scratch
 };
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
+// Device address of the file-scope scratch of the allocation-free dispatch
+// (looked up once per device, on first use, with that device current).
+constexpr int64_t kPermStaticScratchInts = 131072;
+int32_t *permute_static_scratch();
 
 // ----------------------------------------------------------------- experts
 // Grouped GEMM with fused epilogue on the tensor cores (bf16 in, fp32 acc).

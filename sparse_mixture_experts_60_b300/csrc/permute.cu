@@ -22,6 +22,8 @@
 // Integer work only: the result is unique and deterministic.
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -203,6 +205,28 @@ __global__ void __launch_bounds__(256) perm_copy_kernel(const uint4 *x, int64_t 
 }
 
 }  // namespace
+
+// Scratch of the allocation-free dispatch entry point: the chunk histogram
+// table followed by the chunk base table, kPermStaticScratchInts int32 in
+// total (512 KB), resident on every device that loads the library.  Host
+// code must not use this name as an address; permute_static_scratch()
+// returns the device address.
+static __device__ __align__(256) int32_t g_perm_static_scratch[kPermStaticScratchInts];
+
+int32_t *permute_static_scratch() {
+    // one cudaGetSymbolAddress per device, made with that device current
+    static std::mutex mu;
+    static int32_t *ptr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_perm_static_scratch) != cudaSuccess) return nullptr;
+        ptr[dev] = static_cast<int32_t *>(p);
+    }
+    return ptr[dev];
+}
 
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
     const int64_t S = p.T * p.k;
