@@ -237,6 +237,49 @@ class MoELayer:
             out_host.copy_(out_dev, non_blocking=True)
         return out_host
 
+    def run_host_batches(self, x_hosts, out_hosts, n_steps: int, stream=None):
+        """Run ``n_steps`` batches from host memory with the copies overlapped:
+        batch i is uploaded on a copy stream while batch i-1 computes, and its
+        output is downloaded on another copy stream while batch i+1 computes.
+        ``x_hosts`` / ``out_hosts``: sequences of pinned host tensors, used
+        round-robin (step i reads ``x_hosts[i % len]`` and writes
+        ``out_hosts[i % len]``).  Every step copies its whole input in and its
+        whole output out.  Returns after enqueueing; synchronise to wait."""
+        import torch
+        comp = stream or torch.cuda.current_stream()
+        if not hasattr(self, "_pipe"):
+            dev = self.device
+            T, d = self.cfg.num_tokens, self.cfg.d_model
+            xdt = x_hosts[0].dtype
+            self._pipe = dict(
+                h2d=torch.cuda.Stream(device=dev), d2h=torch.cuda.Stream(device=dev),
+                xd=[torch.empty(T, d, dtype=xdt, device=dev) for _ in range(2)],
+                od=[torch.empty(T, d, dtype=self.out_dtype(), device=dev) for _ in range(2)])
+        P = self._pipe
+        P["h2d"].wait_stream(comp)       # the first upload follows earlier work on `comp`
+        x_ready = [torch.cuda.Event() for _ in range(2)]
+        x_free = [torch.cuda.Event() for _ in range(2)]
+        o_ready = [torch.cuda.Event() for _ in range(2)]
+        o_free = [torch.cuda.Event() for _ in range(2)]
+        for i in range(n_steps):
+            b = i % 2
+            if i >= 2:
+                P["h2d"].wait_event(x_free[b])            # batch i-2 no longer reads xd[b]
+            with torch.cuda.stream(P["h2d"]):
+                P["xd"][b].copy_(x_hosts[i % len(x_hosts)], non_blocking=True)
+                x_ready[b].record(P["h2d"])
+            comp.wait_event(x_ready[b])
+            if i >= 2:
+                comp.wait_event(o_free[b])                # batch i-2's output left od[b]
+            self.forward(P["xd"][b], P["od"][b], comp)
+            x_free[b].record(comp)
+            o_ready[b].record(comp)
+            P["d2h"].wait_event(o_ready[b])
+            with torch.cuda.stream(P["d2h"]):
+                out_hosts[i % len(out_hosts)].copy_(P["od"][b], non_blocking=True)
+                o_free[b].record(P["d2h"])
+        comp.wait_stream(P["d2h"])
+
     def stats(self) -> Dict:
         return stats_from_buffer(self.io["stats"])
 

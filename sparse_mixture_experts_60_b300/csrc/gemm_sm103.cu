@@ -24,8 +24,9 @@
 //               frees the stage and, after the last K block, publishes the
 //               accumulator.
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time (warp w reads
-//               TMEM lanes 32*(w%4) ..), bias/activation in fp32, 16-byte
-//               stores; then releases the accumulator.
+//               TMEM lanes 32*(w%4) ..), bias/activation in fp32, staged
+//               through shared memory into row-contiguous 16-byte stores
+//               (whole sectors); then releases the accumulator.
 // Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
 // the main loop of tile i+1.  Tiles are ordered group-major, then N-block,
 // then M-block, so the CTAs working at the same time share weight tiles.
@@ -82,11 +83,12 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (BN >= 64 ? 8 : 10));
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr int EPI_BYTES = 4 * 32 * 32 * 4;   // per epilogue warp: 32 rows x 32 fp32
     static constexpr int BAR_BYTES = 256;
     static size_t smem_bytes(int G) {
-        return 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
+        return 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
     }
 };
 
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * C::A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+    uint8_t *sEpi = smem + STAGES * C::STAGE_BYTES;      // [4 warps][32 rows][32 cols] staging
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::EPI_BYTES);
     uint64_t *full = bars;                 // [STAGES]
     uint64_t *empty = bars + STAGES;       // [STAGES]
     uint64_t *tfull = bars + 2 * STAGES;   // [2]
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *consumed = abort_flag + 1;
-    int *seg_s = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+    int *seg_s = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES + C::BAR_BYTES);
     int *pre_s = seg_s + (args.G + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -425,8 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
+        // Thread = accumulator row.  Each 32-column chunk goes through a
+        // per-warp shared-memory buffer (16-byte units XOR-swizzled by row,
+        // conflict-free both ways) and leaves as row-contiguous 16-byte
+        // stores: 8 rows x 64 B (bf16) or 4 rows x 128 B (fp32) per warp
+        // instruction, i.e. whole 32-byte sectors.
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const int row_in_tile = q * 32 + lane;
+        uint8_t *stg = sEpi + (warp - 2) * (32 * 32 * 4);
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -434,8 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tcgen05.ld below is warp-collective: leave only as a whole warp
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag, args.err))) break;
             tc_fence_after();
-            const int grow = tl.row0 + row_in_tile;
-            const bool row_ok = grow < tl.seg_end;
+            const int row_base = tl.row0 + q * 32;          // first row of this warp's 32
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
             for (int c = 0; c < BN_OUT; c += 32) {
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
                 } else {
                     tmem_ld32(tbase + c, v);
-                    if (args.bias && col < args.N) {
+                    if (args.bias && col + 32 <= args.N) {
                         const uint4 *bp = reinterpret_cast<const uint4 *>(args.bias + (int64_t)tl.g * args.bias_stride + col);
 #pragma unroll
                         for (int qq = 0; qq < 4; ++qq) {
@@ -470,25 +477,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
                     }
                 }
-                if (row_ok && col < args.N) {
-                    if (OUT_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.out) + (int64_t)grow * args.ldo + col);
+                if (OUT_F32) {
+                    // row = lane: 8 units of 16 B, unit j stored at j ^ (row & 7)
+                    float4 *srow = reinterpret_cast<float4 *>(stg + lane * 128);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<bf16 *>(args.out) + (int64_t)grow * args.ldo + col);
+                    for (int j = 0; j < 8; ++j)
+                        srow[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    __syncwarp();
+                    if (col < args.N) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t w[4];
+                        for (int it = 0; it < 8; ++it) {
+                            const int cidx = it * 32 + lane, r = cidx >> 3, cc = cidx & 7;
+                            const float4 val = reinterpret_cast<const float4 *>(stg + r * 128)[cc ^ (r & 7)];
+                            if (row_base + r < tl.seg_end && col + 4 * cc < args.N)
+                                reinterpret_cast<float4 *>(static_cast<float *>(args.out) + (int64_t)(row_base + r) * args.ldo + col)[cc] = val;
+                        }
+                    }
+                } else {
+                    // row = lane: 4 units of 16 B (8 bf16), unit j stored at j ^ ((row >> 1) & 3)
+                    uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
 #pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * h], v[8 * i + 2 * h + 1]);
-                                w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-                            }
-                            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
+                            w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                        srow[j ^ ((lane >> 1) & 3)] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    __syncwarp();
+                    if (col < args.N) {
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int cidx = it * 32 + lane, r = cidx >> 2, cc = cidx & 3;
+                            const uint4 val = reinterpret_cast<const uint4 *>(stg + r * 64)[cc ^ ((r >> 1) & 3)];
+                            if (row_base + r < tl.seg_end && col + 8 * cc < args.N)
+                                reinterpret_cast<uint4 *>(static_cast<bf16 *>(args.out) + (int64_t)(row_base + r) * args.ldo + col)[cc] = val;
                         }
                     }
                 }
+                __syncwarp();
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -581,17 +610,23 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
 
 }  // namespace
 
-bool grouped_gemm_supported(int N, int K, int gated) {
-    (void)gated;
-    return N > 0 && K > 0 && N % 32 == 0 && K % 8 == 0;
+// Columns are written in 16-byte units: N % 4 == 0 for fp32 output, N % 8
+// for bf16; a bias needs whole 32-column chunks.  K % 8 == 0 keeps the TMA
+// row stride a multiple of 16 bytes.
+bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias) {
+    if (N <= 0 || K <= 0 || K % 8 != 0) return false;
+    if (N % (out_f32 ? 4 : 8) != 0) return false;
+    if ((gated || has_bias) && N % 32 != 0) return false;
+    return true;
 }
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
-    if (!grouped_gemm_supported(p.N, p.K, p.gated)) return cudaErrorInvalidValue;
+    if (!grouped_gemm_supported(p.N, p.K, p.gated, p.out_f32, p.bias != nullptr)) return cudaErrorInvalidValue;
     if (p.gated) {
         return p.out_f32 ? launch_t<256, true, true>(p, s) : launch_t<256, true, false>(p, s);
     }
     if (p.out_f32) {
+        if (p.N <= 32) return launch_t<32, false, true>(p, s);
         if (p.N <= 64) return launch_t<64, false, true>(p, s);
         if (p.N <= 128) return launch_t<128, false, true>(p, s);
         return launch_t<256, false, true>(p, s);

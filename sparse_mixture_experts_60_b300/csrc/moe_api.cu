@@ -139,14 +139,16 @@ moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_rout
         p.logits = const_cast<float *>(logits_in);
         p.logits_add_bias = 0;
         e = launch_route_logits(p, s);
-    } else if (c->num_experts <= 32) {
+    } else if (c->dtype == MOE_DTYPE_F32 && c->num_experts <= 32) {
         p.logits = logits;
         e = launch_router_fused(p, c->dtype, s);
     } else {
+        // bf16: logits on the tensor cores (x streamed once by TMA), then the
+        // routing kernel adds the router bias and selects
         p.logits = logits;
         p.logits_add_bias = 1;
         if (c->num_tokens > 0) {
-            if (c->dtype == MOE_DTYPE_BF16 && c->num_experts % 32 == 0) {
+            if (c->dtype == MOE_DTYPE_BF16 && grouped_gemm_supported(c->num_experts, c->d_model, 0, 1, 0)) {
                 GemmProblem g{};
                 g.A = static_cast<const bf16 *>(x);
                 g.a_rows = c->num_tokens;

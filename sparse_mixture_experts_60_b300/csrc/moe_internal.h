@@ -86,7 +86,7 @@ struct GemmProblem {
     int act; int gated;
 };
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
-bool grouped_gemm_supported(int N, int K, int gated);
+bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias);
 
 // CUDA-core grouped FFN layer for fp32 storage (same contract as above, fp32).
 struct SimtProblem {

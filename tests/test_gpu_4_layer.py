@@ -142,3 +142,25 @@ def test_layer_capacity_all_drop_but_capacity():
     # the float bar applies to the rows the layer computes (the zero rows
     # would otherwise deflate the RMS it is measured against)
     check_layer(w, inp, got, np.arange(0, cap))
+
+
+def test_host_batches_pipeline_matches_forward():
+    """MoELayer.run_host_batches (uploads, compute and downloads overlapped on
+    three streams) returns exactly what forward returns for every batch."""
+    w = wl.WORKLOADS["quickstart_bf16"].scaled(1000)
+    inp = wl.make_inputs(w)
+    layer, got = run_layer(w, inp)
+    x0 = dev(inp["x"])
+    x1 = x0.flip(0).contiguous()                      # a second, different batch
+    xs = [torch.empty_like(x0, device="cpu").pin_memory() for _ in range(2)]
+    xs[0].copy_(x0)
+    xs[1].copy_(x1)
+    outs = [torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    layer.run_host_batches(xs, outs, 5)
+    torch.cuda.synchronize()
+    ref0 = layer.forward(x0).cpu()
+    ref1 = layer.forward(x1).cpu()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], ref0)                 # step 4 used batch 0
+    assert torch.equal(outs[1], ref1)                 # step 3 used batch 1
+    np.testing.assert_array_equal(host(ref0), got["out"])
