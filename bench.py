@@ -94,6 +94,21 @@ def hbm_bytes(w, kept_rows):
     return route, permute, combine
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: every rank contributes its elapsed ms."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Tokens per second over all ranks (weak scaling: every rank runs a replica)."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 def launches_per_step(w):
     n = 2 if (w.E <= 32 and w.dtype == wl.F32) else 3   # (logits GEMM +) routing + partial reduce
     n += 4 if w.T * w.k > 0 else 1       # histogram, scan, rank, row copy
@@ -221,7 +236,7 @@ def run_reference(args, w, rank, world):
         t, desc, cores = oracle_sample(w, inp, per_step * 0.5)
         times.append(t)
     ms = 1e3 * statistics.mean(times)
-    value = w.T * world / (ms / 1e3) if world > 1 else w.T / (ms / 1e3)
+    value = w.T / (ms / 1e3)          # one host process: the oracle is not replicated
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -298,10 +313,7 @@ def run_ours(args, w, rank, world, local):
         clocks["remeasured"] = True
     stage = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)] for i in range(args.steps)])
     stage_ms = stage.mean(axis=0)               # route, permute, ffn1, ffn2, shared, combine, stats
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms = total_ms / args.steps
     stats = layer.stats()
     kept = int(stats["total_kept"])
@@ -328,11 +340,7 @@ def run_ours(args, w, rank, world, local):
     layer.run_host_batches(x_hosts, out_hosts, n_e2e)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, "cuda")
     return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms)
 
 
@@ -351,7 +359,7 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
     hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gemm_ms = ffn1_ms + ffn2_ms + float(stage_ms[4])
     line = {
-        "metric": METRIC, "value": w.T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
         "data": "synthetic", "config": config_of(w),
@@ -372,7 +380,7 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
                      "shared": stage_ms[4], "combine": stage_ms[5], "stats": stage_ms[6]},
         "clocks": clocks,
         "e2e": None if e2e_ms is None else {
-            "value": w.T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "value": whole_job_value(w.T, world, e2e_ms), "unit": "tokens/s",
             "h2d_bytes_per_step": int(x.numel() * x.element_size()),
             "d2h_bytes_per_step": int(out.numel() * out.element_size()), "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step(w) * args.steps,
