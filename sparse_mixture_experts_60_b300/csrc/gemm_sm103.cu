@@ -16,17 +16,18 @@
 // Linear); "moe_code.py" (Expert: ReLU FFN); the Mixtral parameter
 // arithmetic of the MoE technical survey (three-matrix SwiGLU expert).
 //
-// Structure: one persistent CTA per SM, 192 threads.
+// Structure: one persistent CTA per SM, 320 threads.
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per stage,
 //               128-byte swizzle, completion on an mbarrier (expect_tx).
 //   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma
 //               (M=128, N=BN, K=16, bf16 -> fp32) per stage, tcgen05.commit
 //               frees the stage and, after the last K block, publishes the
 //               accumulator.
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time (warp w reads
-//               TMEM lanes 32*(w%4) ..), bias/activation in fp32, staged
-//               through shared memory into row-contiguous 16-byte stores
-//               (whole sectors); then releases the accumulator.
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant (warp w reads
+//               lanes 32*(w%4) ..) on alternate 32-column chunks:
+//               tcgen05.ld, bias/activation in fp32, staged through shared
+//               memory into row-contiguous 64-byte segments (whole sectors);
+//               then they release the accumulator.
 // Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
 // the main loop of tile i+1.  Tiles are ordered group-major, then N-block,
 // then M-block, so the CTAs working at the same time share weight tiles.
@@ -38,6 +39,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "moe_internal.h"
 
@@ -75,7 +77,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;                 // one 128-byte swizzle atom of bf16
 constexpr int UMMA_K = 16;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;       // producer, MMA, epilogue
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 template <int BN>
@@ -85,7 +88,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (BN >= 64 ? 8 : 10));
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr int EPI_BYTES = 4 * 32 * 32 * 4;   // per epilogue warp: 32 rows x 32 fp32
+    static constexpr int EPI_BYTES = kEpiWarps * 32 * 64;   // per epilogue warp: 32 rows x 64 B
     static constexpr int BAR_BYTES = 256;
     static size_t smem_bytes(int G) {
         return 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
@@ -250,7 +253,8 @@ struct Tile {
     int g, row0, seg_end, n0;
 };
 
-__device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const int *pre_s, int G, int bn_out) {
+__device__ __forceinline__ Tile decode_tile_m(int tile, const int *seg_s, const int *pre_s, int G, int bn_out,
+                                              int tile_m) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -258,19 +262,105 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const in
         else hi = mid - 1;
     }
     const int rows = seg_s[lo + 1] - seg_s[lo];
-    const int mt = (rows + BM - 1) / BM;
+    const int mt = (rows + tile_m - 1) / tile_m;
     const int local = tile - pre_s[lo];
     const int nb = local / mt, mb = local - nb * mt;
     Tile t;
     t.g = lo;
-    t.row0 = seg_s[lo] + mb * BM;
+    t.row0 = seg_s[lo] + mb * tile_m;
     t.seg_end = seg_s[lo + 1];
     t.n0 = nb * bn_out;
     return t;
 }
+__device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const int *pre_s, int G, int bn_out) {
+    return decode_tile_m(tile, seg_s, pre_s, G, bn_out, BM);
+}
 
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
+
+// Epilogue of one accumulator tile for one warp: rows row_base .. +31 (the
+// warp's TMEM lane quadrant q), alternate 32-column chunks starting at
+// 32 * half.  Shared by the single-CTA and the CTA-pair kernels.
+template <int BN, bool GATED, bool OUT_F32>
+__device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, int row_base, uint32_t tbase,
+                                      int half, int lane, uint8_t *stg) {
+    constexpr int BN_OUT = GATED ? BN / 2 : BN;
+#pragma unroll 1
+    for (int c = 32 * half; c < BN_OUT; c += 64) {
+        const int col = tl.n0 + c;
+        float v[32];
+        if (GATED) {
+            float u[32];
+            tmem_ld32(tbase + c, v);
+            tmem_ld32(tbase + BN / 2 + c, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
+        } else {
+            tmem_ld32(tbase + c, v);
+            if (args.bias && col + 32 <= args.N) {
+                const uint4 *bp = reinterpret_cast<const uint4 *>(args.bias + (int64_t)tl.g * args.bias_stride + col);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const uint4 b = __ldg(bp + qq);
+                    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        v[qq * 8 + 2 * h] += __uint_as_float(w[h] << 16);
+                        v[qq * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                    }
+                }
+            }
+            if (args.act == 1) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+            } else if (args.act == 2) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+            }
+        }
+        // one or two passes of 64 B per row: 32 bf16, or 16 fp32 at a time
+        constexpr int PASSES = OUT_F32 ? 2 : 1;
+        constexpr int COLS = 32 / PASSES;                    // output columns per pass
+        uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
+#pragma unroll
+        for (int ps = 0; ps < PASSES; ++ps) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint4 unit;
+                if (OUT_F32) {
+                    const float *f = v + ps * 16 + 4 * j;
+                    unit = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                                      __float_as_uint(f[3]));
+                } else {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
+                        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    unit = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                srow[j ^ ((lane >> 1) & 3)] = unit;
+            }
+            __syncwarp();
+            const int pcol = col + ps * COLS;
+            constexpr int UNIT_COLS = OUT_F32 ? 4 : 8;
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int cidx = it * 32 + lane, r = cidx >> 2, cc = cidx & 3;
+                const uint4 val = reinterpret_cast<const uint4 *>(stg + r * 64)[cc ^ ((r >> 1) & 3)];
+                if (row_base + r < tl.seg_end && pcol + UNIT_COLS * cc < args.N) {
+                    if (OUT_F32)
+                        reinterpret_cast<uint4 *>(static_cast<float *>(args.out) + (int64_t)(row_base + r) * args.ldo + pcol)[cc] = val;
+                    else
+                        reinterpret_cast<uint4 *>(static_cast<bf16 *>(args.out) + (int64_t)(row_base + r) * args.ldo + pcol)[cc] = val;
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
 
 template <int BN, bool GATED, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -285,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * C::A_BYTES;
-    uint8_t *sEpi = smem + STAGES * C::STAGE_BYTES;      // [4 warps][32 rows][32 cols] staging
+    uint8_t *sEpi = smem + STAGES * C::STAGE_BYTES;      // [epilogue warps][32 rows][64 B] staging
     uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::EPI_BYTES);
     uint64_t *full = bars;                 // [STAGES]
     uint64_t *empty = bars + STAGES;       // [STAGES]
@@ -308,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 128);
+            mbar_init(&tempty[i], 32 * kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -428,13 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
-        // Thread = accumulator row.  Each 32-column chunk goes through a
-        // per-warp shared-memory buffer (16-byte units XOR-swizzled by row,
-        // conflict-free both ways) and leaves as row-contiguous 16-byte
-        // stores: 8 rows x 64 B (bf16) or 4 rows x 128 B (fp32) per warp
-        // instruction, i.e. whole 32-byte sectors.
+        // Thread = accumulator row.  Warps w and w+4 share a TMEM lane
+        // quadrant and take alternate 32-column chunks.  Output leaves through
+        // a per-warp shared-memory buffer of 32 rows x 64 B (16-byte units
+        // XOR-swizzled by row, conflict-free both ways) as row-contiguous
+        // 64-byte segments: whole 32-byte sectors, 8 rows per warp store.
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        uint8_t *stg = sEpi + (warp - 2) * (32 * 32 * 4);
+        const int half = (warp - 2) >> 2;       // which alternate chunks
+        uint8_t *stg = sEpi + (warp - 2) * (32 * 64);
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -444,81 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int row_base = tl.row0 + q * 32;          // first row of this warp's 32
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
-            for (int c = 0; c < BN_OUT; c += 32) {
-                const int col = tl.n0 + c;
-                float v[32];
-                if (GATED) {
-                    float u[32];
-                    tmem_ld32(tbase + c, v);
-                    tmem_ld32(tbase + BN / 2 + c, u);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
-                } else {
-                    tmem_ld32(tbase + c, v);
-                    if (args.bias && col + 32 <= args.N) {
-                        const uint4 *bp = reinterpret_cast<const uint4 *>(args.bias + (int64_t)tl.g * args.bias_stride + col);
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) {
-                            const uint4 b = __ldg(bp + qq);
-                            const uint32_t w[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                v[qq * 8 + 2 * h] += __uint_as_float(w[h] << 16);
-                                v[qq * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
-                            }
-                        }
-                    }
-                    if (args.act == 1) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-                    } else if (args.act == 2) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
-                    }
-                }
-                if (OUT_F32) {
-                    // row = lane: 8 units of 16 B, unit j stored at j ^ (row & 7)
-                    float4 *srow = reinterpret_cast<float4 *>(stg + lane * 128);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        srow[j ^ (lane & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    __syncwarp();
-                    if (col < args.N) {
-#pragma unroll
-                        for (int it = 0; it < 8; ++it) {
-                            const int cidx = it * 32 + lane, r = cidx >> 3, cc = cidx & 7;
-                            const float4 val = reinterpret_cast<const float4 *>(stg + r * 128)[cc ^ (r & 7)];
-                            if (row_base + r < tl.seg_end && col + 4 * cc < args.N)
-                                reinterpret_cast<float4 *>(static_cast<float *>(args.out) + (int64_t)(row_base + r) * args.ldo + col)[cc] = val;
-                        }
-                    }
-                } else {
-                    // row = lane: 4 units of 16 B (8 bf16), unit j stored at j ^ ((row >> 1) & 3)
-                    uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
-                            w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-                        }
-                        srow[j ^ ((lane >> 1) & 3)] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                    __syncwarp();
-                    if (col < args.N) {
-#pragma unroll
-                        for (int it = 0; it < 4; ++it) {
-                            const int cidx = it * 32 + lane, r = cidx >> 2, cc = cidx & 3;
-                            const uint4 val = reinterpret_cast<const uint4 *>(stg + r * 64)[cc ^ ((r >> 1) & 3)];
-                            if (row_base + r < tl.seg_end && col + 8 * cc < args.N)
-                                reinterpret_cast<uint4 *>(static_cast<bf16 *>(args.out) + (int64_t)(row_base + r) * args.ldo + col)[cc] = val;
-                        }
-                    }
-                }
-                __syncwarp();
-            }
+            epilogue_tile<BN, GATED, OUT_F32>(args, tl, row_base, tbase, half, lane, stg);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -542,6 +559,312 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+// The same grouped GEMM with tcgen05.mma.cta_group::2 on a cluster of two
+// CTAs (the two SMs of a TPC): the pair computes a 256-row x BN tile, each
+// CTA holding 128 rows of A and BN/2 rows of B in its shared memory, and
+// each CTA's TMEM holding the accumulator of its own 128 rows.  Per SM the
+// tensor work per stage is unchanged while the loaded bytes drop from 48 KB
+// to 32 KB, so 6 stages fit instead of 4, and A is re-read half as often.
+// The even CTA (rank 0) issues the MMAs; both CTAs' TMA loads complete on
+// the even CTA's full barriers; commits are multicast to both CTAs.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *tm, uint32_t mbar_cluster, int32_t c0,
+                                                 int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(mbar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *holder, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive once on the mbarrier at this shared offset in both CTAs of the pair
+__device__ __forceinline__ void umma_commit_pair_both(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)0x3)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait with cluster-scope acquire (arrivals may come from the peer CTA)
+__device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               int32_t *err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((++n & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(err, 6);  // MOE_ERR_DEVICE_TIMEOUT
+                return false;
+            }
+        }
+    }
+}
+
+template <int BN>
+struct PairCfg {
+    static constexpr int A_BYTES = BM * BK * 2;              // 128 rows of A
+    static constexpr int B_BYTES = (BN / 2) * BK * 2;        // BN/2 rows of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
+    static constexpr int STAGES = 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int EPI_BYTES = kEpiWarps * 32 * 64;
+    static constexpr int BAR_BYTES = 256;
+    static size_t smem_bytes(int G) {
+        return 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
+    }
+};
+
+template <int BN, bool GATED, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmB2, const Args args) {
+    using C = PairCfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int BN_OUT = GATED ? BN / 2 : BN;
+    constexpr int TILE_M = 2 * BM;
+    constexpr uint32_t IDESC = IDesc<TILE_M, BN>::value;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * C::A_BYTES;
+    uint8_t *sEpi = smem + STAGES * C::STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::EPI_BYTES);
+    uint64_t *full = bars;                 // [STAGES] used in the even CTA
+    uint64_t *empty = bars + STAGES;       // [STAGES] both CTAs
+    uint64_t *tfull = bars + 2 * STAGES;   // [2] both CTAs
+    uint64_t *tempty = tfull + 2;          // [2] used in the even CTA
+    uint64_t *drain = tempty + 2;          // [1]
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *seg_bad = abort_flag + 1;
+    int *seg_s = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES + C::BAR_BYTES);
+    int *pre_s = seg_s + (args.G + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = args.G;
+    const uint32_t rank = cluster_rank();
+    const int cid = (int)cluster_index(), ncl = (int)cluster_count();
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 2 * kEpiWarps);   // one arrival per epilogue warp of both CTAs
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (GATED) tma_prefetch_desc(&tmB2);
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+    for (int i = threadIdx.x; i <= G; i += kThreads)
+        seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
+    __syncthreads();
+    const int n_tiles = (args.N + BN_OUT - 1) / BN_OUT;
+    if (warp == 0) {
+        int carry = 0;
+        bool bad = seg_s[0] < 0 || (int64_t)seg_s[G] > args.a_rows;
+        for (int b = 0; b < G; b += 32) {
+            const int g = b + lane;
+            int v = 0;
+            if (g < G) {
+                const int rows = seg_s[g + 1] - seg_s[g];
+                bad |= rows < 0;
+                v = rows > 0 ? ((rows + TILE_M - 1) / TILE_M) * n_tiles : 0;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (g < G) pre_s[g + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            pre_s[0] = 0;
+            *seg_bad = bad ? 1 : 0;
+            if (bad && rank == 0) atomicExch(args.err, 1);  // MOE_ERR_INVALID_ARG
+        }
+    }
+    tc_fence_before();
+    cluster_sync_all();      // barriers initialised and TMEM allocated in both CTAs
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const int total = *seg_bad ? 0 : pre_s[G];
+    const int num_kb = (args.K + BK - 1) / BK;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int tile = cid; tile < total; tile += ncl) {
+            const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M);
+            const int arow = tl.row0 + BM * (int)rank;
+            const int brow = GATED ? tl.g * args.b_group_rows + tl.n0
+                                   : tl.g * args.b_group_rows + tl.n0 + (BN / 2) * (int)rank;
+            const CUtensorMap *bmap = (GATED && rank == 1) ? &tmB2 : &tmB;
+            bool ok = true;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_cluster(&empty[stage], ph ^ 1u, abort_flag, args.err)) {
+                    ok = false;
+                    break;
+                }
+                if (rank == 0) mbar_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                const uint32_t leader_full = map_to_rank(&full[stage], 0);
+                tma_load_2d_pair(sA + stage * C::A_BYTES, &tmA, leader_full, kb * BK, arow);
+                tma_load_2d_pair(sB + stage * C::B_BYTES, bmap, leader_full, kb * BK, brow);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        int stage = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int tile = cid; tile < total && ok; tile += ncl) {
+            if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait_cluster(&full[stage], ph, abort_flag, args.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t adesc = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
+                const uint64_t bdesc = sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                    umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
+                                   (kb > 0 || kk > 0) ? 1u : 0u);
+                umma_commit_pair_both(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_pair_both(&tfull[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        uint8_t *stg = sEpi + (warp - 2) * (32 * 64);
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = cid; tile < total; tile += ncl) {
+            const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M);
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tfull[acc], aph, abort_flag, args.err))) break;
+            tc_fence_after();
+            const int row_base = tl.row0 + BM * (int)rank + q * 32;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            epilogue_tile<BN, GATED, OUT_F32>(args, tl, row_base, tbase, half, lane, stg);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    }
+    // ---------------------------------------------------- teardown
+    __syncthreads();
+    if (warp == 1 && lane == 0 && rank == 0) {
+        // every MMA of the pair has completed once the drain barrier flips
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_u32(drain))
+                     : "memory");
+        mbar_wait_drain(drain, 0);
+    }
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // the copies of an aborted CTA complete on the even CTA's barriers;
+        // give any still in flight time to land before the CTA exits
+        const uint64_t t0 = global_timer();
+        while (global_timer() - t0 < 1000000ull) {
+        }
+    }
+    tc_fence_before();
+    cluster_sync_all();      // neither CTA leaves while the pair still uses its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -608,6 +931,65 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int BN, bool GATED, bool OUT_F32>
+cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
+    using C = PairCfg<BN>;
+    constexpr int BOX_B = BN / 2;   // rows of B per CTA
+    CUtensorMap ta, tb, tb2;
+    if (!make_tmap(&ta, p.A, (uint64_t)p.K, (uint64_t)p.a_rows, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, p.B, (uint64_t)p.K, (uint64_t)p.b_rows_total, BOX_B)) return cudaErrorInvalidValue;
+    if (GATED) {
+        if (!make_tmap(&tb2, p.B2, (uint64_t)p.K, (uint64_t)p.b_rows_total, BOX_B)) return cudaErrorInvalidValue;
+    } else {
+        tb2 = tb;
+    }
+    Args a;
+    a.seg = p.seg;
+    a.a_rows = p.a_rows;
+    a.G = p.seg ? p.G : 1;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.b_group_rows = p.b_group_rows;
+    a.out = p.out;
+    a.ldo = p.ldo;
+    a.bias = p.bias;
+    a.bias_stride = p.bias_stride;
+    a.act = p.act;
+    a.err = device_error_flag();
+    if (!a.err) return cudaErrorUnknown;
+    const size_t smem = C::smem_bytes(a.G);
+    auto kern = grouped_gemm_pair_kernel<BN, GATED, OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// CTA pairs pay off when groups are tall: each pair tile covers 256 rows,
+// so short expert segments would waste most of it.  MOE_B300_GEMM_PAIR=0
+// or 1 forces the choice (tests exercise both kernels on the same shapes).
+bool use_pair(const GemmProblem &p) {
+    const char *e = getenv("MOE_B300_GEMM_PAIR");
+    if (e && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+    const int groups = p.seg ? p.G : 1;
+    const int64_t rows_per_group = p.a_rows / (groups > 0 ? groups : 1);
+    return rows_per_group >= 1024;
+}
+
 }  // namespace
 
 // Columns are written in 16-byte units: N % 4 == 0 for fp32 output, N % 8
@@ -623,14 +1005,22 @@ bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias) 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
     if (!grouped_gemm_supported(p.N, p.K, p.gated, p.out_f32, p.bias != nullptr)) return cudaErrorInvalidValue;
     if (p.gated) {
+        if (use_pair(p)) return p.out_f32 ? launch_pair_t<256, true, true>(p, s) : launch_pair_t<256, true, false>(p, s);
         return p.out_f32 ? launch_t<256, true, true>(p, s) : launch_t<256, true, false>(p, s);
     }
     if (p.out_f32) {
-        if (p.N <= 32) return launch_t<32, false, true>(p, s);
-        if (p.N <= 64) return launch_t<64, false, true>(p, s);
-        if (p.N <= 128) return launch_t<128, false, true>(p, s);
+        // narrowest N tile that covers N, unless that leaves most SMs idle:
+        // then the N tile shrinks (down to 64) to make more tiles
+        const int64_t m_tiles = p.seg ? (p.a_rows + BM - 1) / BM : ((int64_t)p.M + BM - 1) / BM;
+        int bn = p.N <= 32 ? 32 : (p.N <= 64 ? 64 : (p.N <= 128 ? 128 : 256));
+        while (bn > 64 && m_tiles * ((p.N + bn - 1) / bn) < num_sms()) bn /= 2;
+        if (bn == 32) return launch_t<32, false, true>(p, s);
+        if (bn == 64) return launch_t<64, false, true>(p, s);
+        if (bn == 128) return launch_t<128, false, true>(p, s);
+        if (use_pair(p)) return launch_pair_t<256, false, true>(p, s);
         return launch_t<256, false, true>(p, s);
     }
+    if (use_pair(p)) return launch_pair_t<256, false, false>(p, s);
     return launch_t<256, false, false>(p, s);
 }
 

@@ -13,6 +13,14 @@ from tests.gpu_util import as_f32, dev, float_check, host, weights
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["0", "1"], ids=["single_cta", "cta_pair"])
+def gemm_kernel(request, monkeypatch):
+    """Run the test with the single-CTA tcgen05 kernel, then with the CTA-pair
+    (cta_group::2) kernel (the library reads MOE_B300_GEMM_PAIR per launch)."""
+    monkeypatch.setenv("MOE_B300_GEMM_PAIR", request.param)
+    return request.param
+
+
 def oracle_dispatch(w, inp):
     lg = wl.make_logits(w, ties=False)
     r = orc.route(w, lg, inp.get("sel_bias"))
@@ -68,7 +76,7 @@ CASES = [("tiny_fp32", 64, 10**9), ("quickstart_bf16", 1000, 96), ("capacity_e12
 
 
 @pytest.mark.parametrize("name,T,nrows", CASES)
-def test_expert_ffn(name, T, nrows):
+def test_expert_ffn(name, T, nrows, gemm_kernel):
     w = wl.WORKLOADS[name].scaled(T)
     inp = wl.make_inputs(w)
     _, d_ref = oracle_dispatch(w, inp)
@@ -77,9 +85,9 @@ def test_expert_ffn(name, T, nrows):
 
 
 @pytest.mark.parametrize("act", [wl.RELU, wl.GELU, wl.SWIGLU])
-def test_expert_ffn_ragged_segments(act):
-    """Segments of 0, 1, 127, 128, 129, 300 rows; weights of all experts."""
-    sizes = [0, 1, 127, 128, 129, 300, 0, 64]
+def test_expert_ffn_ragged_segments(act, gemm_kernel):
+    """Segments of 0, 1, 127, 128, 129, 255, 256, 257, 300 and 600 rows."""
+    sizes = [0, 1, 127, 128, 129, 255, 0, 256, 257, 300, 600, 64]
     E = len(sizes)
     T = sum(sizes)
     w = wl.Workload(f"rag{act}", 50 + act, T=T, d=128, E=E, k=1, F=192, activation=act, score_fn=wl.SOFTMAX,
@@ -91,7 +99,7 @@ def test_expert_ffn_ragged_segments(act):
     check_ffn(w, inp, d_ref, y, 10**9)
 
 
-def test_shared_ffn():
+def test_shared_ffn(gemm_kernel):
     w = wl.WORKLOADS["deepseek_v3"].scaled(300)
     inp = wl.make_inputs(w)
     cfg = moe.config_for(w)
