@@ -979,15 +979,17 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// CTA pairs pay off when groups are tall: each pair tile covers 256 rows,
-// so short expert segments would waste most of it.  MOE_B300_GEMM_PAIR=0
-// or 1 forces the choice (tests exercise both kernels on the same shapes).
+// CTA pairs pay off when groups are tall (a pair tile covers 256 rows, so
+// short expert segments would waste most of it); measured on B300 they win
+// for the second expert GEMM (fp32 output) and lose for the gated first one,
+// so only the former uses them by default.  MOE_B300_GEMM_PAIR=0 or 1 forces
+// the choice (the tests run both kernels on the same shapes).
 bool use_pair(const GemmProblem &p) {
     const char *e = getenv("MOE_B300_GEMM_PAIR");
     if (e && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
     const int groups = p.seg ? p.G : 1;
     const int64_t rows_per_group = p.a_rows / (groups > 0 ? groups : 1);
-    return rows_per_group >= 1024;
+    return rows_per_group >= 1024 && p.out_f32 && !p.gated;
 }
 
 }  // namespace

@@ -444,6 +444,7 @@ moe_status_t moe_permute_noalloc(const moe_config_t *cfg, const void *x, const i
     p.x_perm = x_perm;
     p.hist = scratch;
     p.base = scratch + table;
+    p.chunked = 1;
     return cuda_status(launch_permute(p, static_cast<cudaStream_t>(stream)), "moe_permute_noalloc launch");
 }
 

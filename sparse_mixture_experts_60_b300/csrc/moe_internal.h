@@ -63,7 +63,11 @@ struct PermuteParams {
     void *x_perm;
     int32_t *hist;         // [nchunk, E] scratch
     int32_t *base;         // [nchunk, E] scratch
+    int chunked;           // 1: always the chunked kernels (which use hist/base)
 };
+// Layers up to this many slots and experts dispatch in one CTA without scratch.
+constexpr int64_t kSmallSlots = 65536;
+constexpr int kSmallExperts = 256;
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
 // Device address of the file-scope scratch of the allocation-free dispatch
 // (looked up once per device, on first use, with that device current).

@@ -163,6 +163,122 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *
     }
 }
 
+// Whole integer dispatch in one CTA of 1024 threads, for layers of at most
+// kSmallSlots slots and kSmallExperts experts.  The top-k indices are first
+// copied into shared memory (16-bit, one vectorised pass), then warp w owns
+// priorities [w*span, (w+1)*span): per-warp histograms -> per-expert warp
+// bases (an exclusive scan over warps in warp order, which is priority
+// order) -> counts, kept, offsets -> match-any ranks -> perm, inv.  Same
+// result as the chunked kernels, two launches fewer.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+
+__global__ void __launch_bounds__(kSmallThreads) perm_small_kernel(const int32_t *idx, int T, int k, int E,
+                                                                   int64_t cap, int32_t *counts, int32_t *kept,
+                                                                   int32_t *offsets, int32_t *perm, int32_t *inv,
+                                                                   int32_t *err) {
+    extern __shared__ int wh[];            // [kSmallWarps][E] histograms, then warp bases; then slot experts
+    __shared__ int warp_tot[32];
+    short *es = reinterpret_cast<short *>(wh + kSmallWarps * E);   // [S] expert of slot s (-2: invalid)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int S = T * k;
+    const int span = ((S + kSmallWarps - 1) / kSmallWarps + 31) / 32 * 32;   // multiple of 32
+    for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wh[i] = 0;
+    // expert ids, slot order (t*k + j); 16-byte loads while aligned
+    const int nvec = ((S & 3) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15) == 0) ? S / 4 : 0;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+        const int4 q = __ldg(reinterpret_cast<const int4 *>(idx) + v);
+        const int a[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) es[4 * v + h] = (short)((a[h] >= 0 && a[h] < E) ? a[h] : -2);
+    }
+    for (int i = 4 * nvec + threadIdx.x; i < S; i += blockDim.x) {
+        const int a = __ldg(idx + i);
+        es[i] = (short)((a >= 0 && a < E) ? a : -2);
+    }
+    __syncthreads();
+    const int p0 = warp * span;
+    int *my = wh + warp * E;
+    // priority p = j*T + t  ->  slot s = t*k + j
+    auto slot_of = [&](int p) { const int j = p / T; return (p - j * T) * k + j; };
+    for (int g = 0; g < span; g += 32) {
+        const int p = p0 + g + lane;
+        if (p < S) {
+            const int e = es[slot_of(p)];
+            if (e >= 0) atomicAdd(&my[e], 1);
+            else atomicExch(err, 1);       // MOE_ERR_INVALID_ARG
+        }
+    }
+    __syncthreads();
+    int kp_mine = 0;
+    if ((int)threadIdx.x < E) {
+        const int e = threadIdx.x;
+        int run = 0;
+        for (int w = 0; w < kSmallWarps; ++w) {
+            const int c = wh[w * E + e];
+            wh[w * E + e] = run;
+            run += c;
+        }
+        counts[e] = run;
+        kp_mine = (int64_t)run < cap ? run : (int)cap;
+        kept[e] = kp_mine;
+    }
+    // exclusive block scan of kept -> offsets (kept in shared memory too)
+    int v = kp_mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += u;
+        }
+        warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + v - kp_mine;
+    __shared__ int off_s[kSmallExperts + 1];
+    if ((int)threadIdx.x < E) {
+        offsets[threadIdx.x] = before;
+        off_s[threadIdx.x] = before;
+    }
+    if ((int)threadIdx.x == E - 1) offsets[E] = before + kp_mine;
+    __syncthreads();
+    // ranks in priority order, 32 slots at a time
+    const unsigned lt = (1u << lane) - 1u;
+    for (int g = 0; g < span; g += 32) {
+        const int p = p0 + g + lane;
+        int s = -1, e = -1;
+        if (p < S) {
+            s = slot_of(p);
+            e = es[s];
+        }
+        const unsigned peers = __match_any_sync(kFull, e);
+        int rank = 0;
+        if (e >= 0) rank = my[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && (peers & lt) == 0) my[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            if ((int64_t)rank < cap) {
+                const int row = off_s[e] + rank;
+                perm[row] = s;
+                inv[s] = row;
+            } else {
+                inv[s] = -1;
+            }
+        } else if (e == -2) {
+            inv[s] = -1;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256) perm_copy_kernel(const uint4 *x, int64_t T, int k, int64_t nvec,
                                                         const int32_t *inv, const int32_t *offsets,
                                                         int E, int32_t *perm, int64_t S, uint4 *x_perm) {
@@ -233,6 +349,24 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
     const int64_t nchunk = ceil_div(S, kPermChunk);
     int32_t *err = device_error_flag();
     if (!err) return cudaErrorUnknown;
+    const int eb = p.dtype == 0 ? 4 : 2;
+    const int64_t nvec = (int64_t)p.d * eb / 16;
+    if (!p.chunked && S > 0 && S <= kSmallSlots && p.E <= kSmallExperts) {
+        const size_t smem = (size_t)kSmallWarps * p.E * sizeof(int) + (size_t)S * sizeof(short);
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        perm_small_kernel<<<1, kSmallThreads, smem, s>>>(p.topk_idx, (int)p.T, p.k, p.E, p.cap, p.counts, p.kept,
+                                                          p.offsets, p.perm, p.inv, err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        perm_copy_kernel<<<(unsigned)ceil_div(p.T, 8), 256, 0, s>>>(static_cast<const uint4 *>(p.x), p.T, p.k, nvec,
+                                                                   p.inv, p.offsets, p.E, p.perm, S,
+                                                                   static_cast<uint4 *>(p.x_perm));
+        return cudaGetLastError();
+    }
     if (nchunk > 0) {
         perm_hist_kernel<<<(unsigned)nchunk, kPermThreads, p.E * sizeof(int), s>>>(p.topk_idx, p.T, p.k,
                                                                                  p.E, p.hist, err);
@@ -253,8 +387,6 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
         p.topk_idx, p.T, p.k, p.E, p.cap, p.base, p.offsets, p.perm, p.inv, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int eb = p.dtype == 0 ? 4 : 2;
-    const int64_t nvec = (int64_t)p.d * eb / 16;
     const unsigned grid = (unsigned)ceil_div(p.T, 8);
     perm_copy_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(p.x), p.T, p.k, nvec, p.inv,
                                              p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));

@@ -62,7 +62,7 @@ def test_permute_bit_exact_full_size(name):
 
 
 @pytest.mark.parametrize("case", ["one_expert_capacity", "k_equals_E", "single_token", "ragged_many_chunks",
-                                  "empty_experts", "e1024_drop", "fp32_k3_drop"])
+                                  "empty_experts", "e1024_drop", "fp32_k3_drop", "chunked_80k_slots"])
 def test_permute_edge_cases(case):
     g = np.random.default_rng(len(case))
     if case == "one_expert_capacity":
@@ -95,6 +95,13 @@ def test_permute_edge_cases(case):
                         capacity_factor=2.0, min_capacity=4)
         pop = np.exp(g.standard_normal(w.E) * 1.5)
         idx = np.stack([g.choice(w.E, 4, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
+    elif case == "chunked_80k_slots":
+        # above the one-CTA dispatch limit (65536 slots): the chunked kernels
+        w = wl.Workload(case, 48, T=40000, d=64, E=64, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
+                        dtype=wl.BF16, router_bias=False, expert_bias=False, drop_tokens=True,
+                        capacity_factor=1.1, min_capacity=4)
+        pop = np.exp(g.standard_normal(w.E))
+        idx = np.stack([g.choice(w.E, 2, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
     else:
         w = wl.Workload(case, 46, T=2049, d=36, E=6, k=3, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                         dtype=wl.F32, router_bias=False, expert_bias=False, drop_tokens=True,

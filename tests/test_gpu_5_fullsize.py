@@ -11,7 +11,7 @@ from tests.test_gpu_4_layer import check_layer, run_layer
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-SAMPLES = {"tiny_fp32": None, "quickstart_bf16": 48, "capacity_e128": 64, "mixtral": 12, "deepseek_v3": 16}
+SAMPLES = {"tiny_fp32": None, "quickstart_bf16": 48, "capacity_e128": 96, "mixtral": 12, "deepseek_v3": 16}
 
 
 @pytest.mark.parametrize("name", list(wl.WORKLOADS))
