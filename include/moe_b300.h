@@ -312,6 +312,32 @@ moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *weights, 
                          const float *sel_bias, void *out, const moe_forward_io_t *io, void *ws,
                          size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * Hash routing ("MoE technical survey" page, Hash layers for large sparse
+ * models: a fixed token -> expert mapping, no gating network).  The page
+ * gives no hash function; choice j of a token is
+ *   fmix32(token_id + j * 0x9E3779B9) mod E
+ * (fmix32 = MurmurHash3's 32-bit finalizer), moved to the next expert,
+ * cyclically, if an earlier choice of the same token took it; every gate is
+ * 1/k.  token_ids [T] int32 (vocabulary ids, any value); outputs
+ * topk_idx [T,k] and topk_w [T,k] feed moe_permute / moe_forward_from_routing.
+ */
+moe_status_t moe_route_hash(const moe_config_t *cfg, const int32_t *token_ids, int32_t *topk_idx,
+                            float *topk_w, moe_stream_t stream);
+
+/*
+ * The layer forward from routing the caller already has (hash routing, or
+ * any other token -> expert assignment): permute -> routed experts (+ shared
+ * expert) -> combine -> stats, exactly as moe_forward after its router.
+ *   topk_idx [T,k] in [0, E), topk_w [T,k] fp32 (device).  io's routing
+ *   members are ignored; stats->aux_loss and z_loss are NaN (no router
+ *   probabilities).  Workspace: moe_workspace_size(MOE_WS_FORWARD).
+ */
+moe_status_t moe_forward_from_routing(const moe_config_t *cfg, const moe_weights_t *weights,
+                                      const void *x, const int32_t *topk_idx, const float *topk_w,
+                                      void *out, const moe_forward_io_t *io, void *ws,
+                                      size_t ws_bytes, moe_stream_t stream);
+
 /* Reads and clears the device error flag (host output *code: 0 = none,
  * else a moe_status_t).  Synchronises the device first. */
 moe_status_t moe_check_device_error(int32_t *code);

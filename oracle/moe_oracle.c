@@ -301,6 +301,42 @@ void orc_route(const orc_cfg *c, const float *logits, const float *sel_bias,
     }
 }
 
+/*
+ * Hash routing (MoE technical survey page, "Hash layers for large sparse
+ * models"; "hash-based route": a fixed token -> expert mapping fixed before
+ * training, no gating network).  The page names no hash function; the one
+ * used is MurmurHash3's 32-bit finalizer (fmix32) of token_id + j * 0x9E3779B9
+ * (a golden-ratio stride per choice j), taken modulo E; a choice already
+ * taken by an earlier j of the same token moves to the next expert,
+ * cyclically.  Every chosen expert gets gate 1/k.
+ */
+uint32_t orc_fmix32(uint32_t h) {
+    h ^= h >> 16;
+    h *= 0x85ebca6bu;
+    h ^= h >> 13;
+    h *= 0xc2b2ae35u;
+    h ^= h >> 16;
+    return h;
+}
+
+void orc_route_hash(int64_t T, int32_t E, int32_t k, const int32_t *token_ids, int32_t *idx, double *gate) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) {
+            uint32_t key = (uint32_t)token_ids[t] + (uint32_t)j * 0x9E3779B9u;
+            int32_t e = (int32_t)(orc_fmix32(key) % (uint32_t)E);
+            for (;;) {   /* next free expert if an earlier choice took e */
+                int taken = 0;
+                for (int32_t i = 0; i < j; ++i)
+                    if (idx[t * k + i] == e) taken = 1;
+                if (!taken) break;
+                e = (e + 1) % E;
+            }
+            idx[t * k + j] = e;
+            gate[t * k + j] = 1.0 / (double)k;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* step 3: capacity, drop, permutation                                  */
 /* ------------------------------------------------------------------ */

@@ -86,6 +86,9 @@ def lib():
             L.orc_param_counts.argtypes = [C.c_int64] * 4 + [C.c_int, P]
             L.orc_sigmoid_keys.argtypes = [P, P, C.c_int64, C.c_int64, P]
             L.orc_expert_rows.argtypes = [P, P, C.c_int64, P, P, P]
+            L.orc_fmix32.restype = C.c_uint32
+            L.orc_fmix32.argtypes = [C.c_uint32]
+            L.orc_route_hash.argtypes = [C.c_int64, C.c_int32, C.c_int32, P, P, P]
             _lib = L
     return _lib
 
@@ -171,6 +174,19 @@ def route(w, logits: np.ndarray, sel_bias: Optional[np.ndarray] = None):
     lib().orc_route(C.byref(c), logits.ctypes.data, _p(sb), idx.ctypes.data, gate.ctypes.data,
                     lse.ctypes.data, ps.ctypes.data)
     return dict(idx=idx, gate=gate, lse=lse, prob_sum=ps)
+
+
+def fmix32(h: int) -> int:
+    return int(lib().orc_fmix32(h & 0xFFFFFFFF))
+
+
+def route_hash(T: int, E: int, k: int, token_ids: np.ndarray):
+    """-> dict(idx [T,k] int32, gate [T,k] f64) of hash routing."""
+    tid = _c(token_ids, np.int32)
+    idx = np.empty((T, k), np.int32)
+    gate = np.empty((T, k), np.float64)
+    lib().orc_route_hash(T, E, k, tid.ctypes.data, idx.ctypes.data, gate.ctypes.data)
+    return dict(idx=idx, gate=gate)
 
 
 def dispatch(w, idx: np.ndarray):

@@ -170,6 +170,22 @@ def moe_forward(cfg, weights: Dict, x, sel_bias, out, io: Optional[Dict], ws, st
                             C.byref(ios) if ios is not None else None, p, n, _stream(stream)))
 
 
+def moe_forward_from_routing(cfg, weights: Dict, x, topk_idx, topk_w, out, io: Optional[Dict], ws, stream=None,
+                             stage_events=None) -> None:
+    """The layer from caller-given routing (topk_idx [T,k], topk_w [T,k])."""
+    p, n = _ws(ws)
+    wst = weights_struct(weights)
+    ios = io_struct(io, stage_events)
+    check(lib().moe_forward_from_routing(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+                                         _ptr(out), C.byref(ios) if ios is not None else None, p, n,
+                                         _stream(stream)))
+
+
+def moe_route_hash(cfg, token_ids, topk_idx, topk_w, stream=None) -> None:
+    """Hash routing of token ids [T] (int32) into topk_idx / topk_w [T,k]."""
+    check(lib().moe_route_hash(C.byref(cfg), _ptr(token_ids), _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+
+
 def moe_check_device_error() -> int:
     code = C.c_int32(0)
     check(lib().moe_check_device_error(C.byref(code)))
@@ -236,6 +252,16 @@ class MoELayer:
             out_dev = self.forward(x_dev, out_dev, st)
             out_host.copy_(out_dev, non_blocking=True)
         return out_host
+
+    def forward_hashed(self, x, token_ids, out=None, stream=None, stage_events=None):
+        """The layer with hash routing of ``token_ids`` [T] instead of the router."""
+        import torch
+        if out is None:
+            out = torch.empty(self.cfg.num_tokens, self.cfg.d_model, dtype=self.out_dtype(), device=self.device)
+        moe_route_hash(self.cfg, token_ids, self.io["topk_idx"], self.io["topk_w"], stream)
+        moe_forward_from_routing(self.cfg, self.weights, x, self.io["topk_idx"], self.io["topk_w"], out, self.io,
+                                 self.ws, stream, stage_events)
+        return out
 
     def run_host_batches(self, x_hosts, out_hosts, n_steps: int, stream=None):
         """Run ``n_steps`` batches from host memory with the copies overlapped:

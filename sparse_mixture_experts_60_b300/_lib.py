@@ -71,6 +71,8 @@ _SIGS = {
     "moe_stats": ([P] * 7 + [P], C.c_int),
     "moe_bias_update": ([P, P, P, C.c_float, P], C.c_int),
     "moe_forward": ([P] * 6 + [P, C.c_size_t, P], C.c_int),
+    "moe_forward_from_routing": ([P] * 7 + [P, C.c_size_t, P], C.c_int),
+    "moe_route_hash": ([P] * 4 + [P], C.c_int),
     "moe_check_device_error": ([C.POINTER(C.c_int32)], C.c_int),
 }
 

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
     __shared__ long long sl[32];
     const int64_t S = p.T * p.k;
     float z = 0.0f, zc = 0.0f;
-    for (int64_t i = threadIdx.x; i < p.T; i += blockDim.x) {
+    for (int64_t i = threadIdx.x; p.lse && i < p.T; i += blockDim.x) {
         const float v = p.lse[i] * p.lse[i] - zc;
         const float t = z + v;
         zc = (t - z) - v;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         const float f = S > 0 ? (float)p.counts[e] / (float)S : 0.0f;
         if (p.f) p.f[e] = f;
-        aux += f * p.prob_mean[e];
+        aux += f * (p.prob_mean ? p.prob_mean[e] : 0.0f);
         dropped += p.counts[e] - p.kept[e];
         used += p.kept[e] > 0;
         kept_tot += p.kept[e];
@@ -154,8 +154,10 @@ __global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
     kmin = block_reduce(kmin, sl, MinL());
     if (threadIdx.x == 0) {
         moe_stats_t st;
-        st.aux_loss = (float)p.E * aux;
-        st.z_loss = p.T > 0 ? z / (float)p.T : 0.0f;
+        // without router probabilities (routing given by the caller) the
+        // balance losses are undefined: NaN
+        st.aux_loss = p.prob_mean ? (float)p.E * aux : __int_as_float(0x7fc00000);
+        st.z_loss = !p.lse ? __int_as_float(0x7fc00000) : (p.T > 0 ? z / (float)p.T : 0.0f);
         st.imbalance = kmin > 0 ? (float)kmax / (float)kmin : INFINITY;
         st.utilization = (float)used / (float)p.E;
         st.drop_rate = S > 0 ? (float)dropped / (float)S : 0.0f;

@@ -526,18 +526,22 @@ moe_status_t moe_bias_update(const moe_config_t *cfg, const int32_t *counts, flo
                        "moe_bias_update launch");
 }
 
-moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const void *x, const float *sel_bias,
-                         void *out, const moe_forward_io_t *io, void *ws, size_t ws_bytes, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const void *x, const float *sel_bias,
+                          const int32_t *given_idx, const float *given_w, void *out, const moe_forward_io_t *io,
+                          void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     TRY(need(w, "weights"));
     TRY(need16(x, "x", cfg->num_tokens));
     TRY(need16(out, "out", cfg->num_tokens));
-    TRY(need16(w->w_router, "w_router"));
+    if (!given_idx) TRY(need16(w->w_router, "w_router"));
     TRY(check_weights_ffn(cfg, w->w1, w->w3, w->w2));
     TRY(check_bias(w->b1));
     TRY(check_bias(w->b2));
     if (cfg->num_shared) TRY(check_weights_ffn(cfg, w->shared_w1, w->shared_w3, w->shared_w2));
-    if (cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
+    if (!given_idx && cfg->score_fn == MOE_SCORE_SIGMOID) TRY(need(sel_bias, "sel_bias (sigmoid scoring)"));
     TRY(need_ws(ws, ws_bytes, forward_ws(cfg)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const moe_config_t *c = cfg;
@@ -582,8 +586,14 @@ moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const 
         if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
     };
     mark(0);
-    TRY(route_impl(c, x, w->w_router, w->b_router, c->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr, o.logits,
-                   nullptr, o.topk_idx, o.topk_w, o.lse, o.prob_mean, o.counts, ws_route, s));
+    if (given_idx) {
+        // routing given by the caller (hash routing or any other source)
+        o.topk_idx = const_cast<int32_t *>(given_idx);
+        o.topk_w = const_cast<float *>(given_w);
+    } else {
+        TRY(route_impl(c, x, w->w_router, w->b_router, c->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr,
+                       o.logits, nullptr, o.topk_idx, o.topk_w, o.lse, o.prob_mean, o.counts, ws_route, s));
+    }
     mark(1);
     TRY(permute_impl(c, x, o.topk_idx, o.counts, o.kept, o.offsets, o.perm, o.inv, x_perm, ws_perm, s));
     mark(2);
@@ -606,13 +616,44 @@ moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *w, const 
     sp.drop = c->drop_tokens;
     sp.counts = o.counts;
     sp.kept = o.kept;
-    sp.prob_mean = o.prob_mean;
-    sp.lse = o.lse;
+    sp.prob_mean = given_idx ? nullptr : o.prob_mean;
+    sp.lse = given_idx ? nullptr : o.lse;
     sp.f = o.f;
     sp.stats = o.stats;
     TRY(cuda_status(launch_stats(sp, s), "stats launch"));
     mark(7);
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_forward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x, const float *sel_bias,
+                         void *out, const moe_forward_io_t *io, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    return forward_impl(cfg, weights, x, sel_bias, nullptr, nullptr, out, io, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_forward_from_routing(const moe_config_t *cfg, const moe_weights_t *weights, const void *x,
+                                      const int32_t *topk_idx, const float *topk_w, void *out,
+                                      const moe_forward_io_t *io, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    const int64_t S = cfg->num_tokens * cfg->top_k;
+    TRY(need(topk_idx, "topk_idx", S));
+    TRY(need(topk_w, "topk_w", S));
+    return forward_impl(cfg, weights, x, nullptr, topk_idx, topk_w, out, io, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_route_hash(const moe_config_t *cfg, const int32_t *token_ids, int32_t *topk_idx, float *topk_w,
+                            moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    TRY(need(token_ids, "token_ids", T));
+    TRY(need(topk_idx, "topk_idx", S));
+    TRY(need(topk_w, "topk_w", S));
+    return cuda_status(launch_route_hash(T, cfg->num_experts, cfg->top_k, token_ids, topk_idx, topk_w,
+                                         static_cast<cudaStream_t>(stream)),
+                       "moe_route_hash launch");
 }
 
 moe_status_t moe_check_device_error(int32_t *code) {

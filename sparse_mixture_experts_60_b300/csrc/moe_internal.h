@@ -47,6 +47,9 @@ cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s)
 cudaError_t launch_route_logits(const RouteParams &p, cudaStream_t s);
 // logits = x w_r^T on CUDA cores (fp32, or shapes the tensor-core path does not take)
 cudaError_t launch_router_logits_simt(const RouteParams &p, int dtype, cudaStream_t s);
+// hash routing: fixed token -> expert map from token ids, gate 1/k
+cudaError_t launch_route_hash(int64_t T, int E, int k, const int32_t *token_ids, int32_t *topk_idx,
+                              float *topk_w, cudaStream_t s);
 // deterministic reduction of the per-CTA partials: prob_mean[E], counts[E]
 cudaError_t launch_route_reduce(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
                                 int E, int64_t T, float *prob_mean, int32_t *counts,
@@ -65,8 +68,10 @@ struct PermuteParams {
     int32_t *base;         // [nchunk, E] scratch
     int chunked;           // 1: always the chunked kernels (which use hist/base)
 };
-// Layers up to this many slots and experts dispatch in one CTA without scratch.
-constexpr int64_t kSmallSlots = 65536;
+// Layers up to this many slots and experts dispatch in one CTA without
+// scratch (two launches fewer); larger ones are faster on the chunked
+// kernels, which spread the integer work over many SMs.
+constexpr int64_t kSmallSlots = 8192;
 constexpr int kSmallExperts = 256;
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
 // Device address of the file-scope scratch of the allocation-free dispatch

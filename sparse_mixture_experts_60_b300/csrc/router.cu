@@ -421,7 +421,52 @@ cudaError_t launch_route_logits_t(const RouteParams &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Hash routing: one thread per token.  Choice j of a token is
+// fmix32(token_id + j * 0x9E3779B9) mod E (MurmurHash3's 32-bit finalizer,
+// a published mixing function), moved to the next free expert, cyclically,
+// when an earlier choice of the same token already took it; gate 1/k.
+__device__ __forceinline__ uint32_t fmix32(uint32_t h) {
+    h ^= h >> 16;
+    h *= 0x85ebca6bu;
+    h ^= h >> 13;
+    h *= 0xc2b2ae35u;
+    h ^= h >> 16;
+    return h;
+}
+
+__global__ void __launch_bounds__(256) route_hash_kernel(int64_t T, int E, int k, const int32_t *token_ids,
+                                                         int32_t *topk_idx, float *topk_w) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const uint32_t id = (uint32_t)token_ids[t];
+    int chosen[kMaxTopK];
+    const float g = 1.0f / (float)k;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j >= k) break;
+        int e = (int)(fmix32(id + (uint32_t)j * 0x9E3779B9u) % (uint32_t)E);
+        for (;;) {
+            bool taken = false;
+#pragma unroll
+            for (int i = 0; i < kMaxTopK; ++i)
+                if (i < j && chosen[i] == e) taken = true;
+            if (!taken) break;
+            e = (e + 1) % E;
+        }
+        chosen[j] = e;
+        topk_idx[t * k + j] = e;
+        topk_w[t * k + j] = g;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_route_hash(int64_t T, int E, int k, const int32_t *token_ids, int32_t *topk_idx, float *topk_w,
+                              cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    route_hash_kernel<<<(unsigned)ceil_div(T, 256), 256, 0, s>>>(T, E, k, token_ids, topk_idx, topk_w);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;

@@ -96,7 +96,7 @@ def test_permute_edge_cases(case):
         pop = np.exp(g.standard_normal(w.E) * 1.5)
         idx = np.stack([g.choice(w.E, 4, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
     elif case == "chunked_80k_slots":
-        # above the one-CTA dispatch limit (65536 slots): the chunked kernels
+        # far above the one-CTA dispatch limit: the chunked kernels
         w = wl.Workload(case, 48, T=40000, d=64, E=64, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                         dtype=wl.BF16, router_bias=False, expert_bias=False, drop_tokens=True,
                         capacity_factor=1.1, min_capacity=4)
@@ -131,3 +131,30 @@ def test_permute_flags_out_of_range_expert():
     assert got["err"] == 1
     assert got["inv"][17 * 2 + 1] == -1 and got["inv"][50 * 2] == -1
     assert moe.moe_check_device_error() == 0   # read clears the flag
+
+
+def test_permute_unaligned_topk_idx():
+    """topk_idx need not be 16-byte aligned: a view starting 4 bytes into a
+    buffer gives the same dispatch."""
+    w = wl.Workload("unaligned", 49, T=3001, d=64, E=16, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
+                    dtype=wl.BF16, router_bias=False, expert_bias=False)
+    g = np.random.default_rng(3)
+    idx = np.stack([g.choice(w.E, 2, replace=False) for _ in range(w.T)]).astype(np.int32)
+    x = wl.make_inputs(w, with_weights=False)["x"]
+    cfg = moe.config_for(w)
+    S = w.T * w.k
+    buf = torch.zeros(S + 4, dtype=torch.int32, device="cuda")
+    buf[1:S + 1] = torch.from_numpy(idx.reshape(-1)).cuda()
+    view = buf[1:S + 1]
+    assert view.data_ptr() % 16 == 4
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = [torch.empty(w.E, **i32), torch.empty(w.E, **i32), torch.empty(w.E + 1, **i32),
+            torch.empty(S, **i32), torch.empty(S, **i32)]
+    xd = dev(x)
+    xp = torch.zeros(S, w.d, dtype=xd.dtype, device="cuda")
+    ws = torch.empty(moe.moe_workspace_size(cfg, moe.MOE_WS_PERMUTE), dtype=torch.uint8, device="cuda")
+    moe.moe_permute(cfg, xd, view, *outs, xp, ws)
+    torch.cuda.synchronize()
+    got = dict(counts=host(outs[0]), kept=host(outs[1]), offsets=host(outs[2]), perm=host(outs[3]),
+               inv=host(outs[4]), x_perm=host(xp), err=moe.moe_check_device_error())
+    check_permute(w, x, idx, got)

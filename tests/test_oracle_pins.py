@@ -420,3 +420,58 @@ def test_expert_rows_parallel_equals_single_row():
     routed = np.stack([lay["gate"][t, 0] * orc.expert_row(w, inp, lay["idx"][t, 0], X[t]) for t in range(w.T)])
     shared_rows = np.nonzero(ex == -1)[0]
     np.testing.assert_allclose(lay["out"][shared_rows] - routed[shared_rows], y[shared_rows], atol=1e-12)
+
+
+
+# ------------------------------------------------------------ hash routing
+def test_hash_routing_properties():
+    """Hash routing is a fixed token -> expert map with no router (the
+    survey page's hash-layer digest): the same token always gets the same
+    experts, choices are distinct and in range, k = E gives every expert,
+    and the first choice is close to uniform over experts."""
+    g = np.random.default_rng(12)
+    tok = g.integers(0, 32000, 60000).astype(np.int32)
+    for E, k in [(1, 1), (8, 2), (16, 16), (128, 1), (256, 8)]:
+        r = orc.route_hash(len(tok), E, k, tok)
+        idx = r["idx"]
+        assert idx.min() >= 0 and idx.max() < E
+        assert all(len(set(row)) == k for row in idx[:2000])
+        np.testing.assert_allclose(r["gate"], 1.0 / k)
+        # same token id -> same choices
+        first = {}
+        for t in range(3000):
+            key = int(tok[t])
+            if key in first:
+                assert list(idx[t]) == first[key]
+            else:
+                first[key] = list(idx[t])
+        if k == E:
+            assert all(sorted(row) == list(range(E)) for row in idx[:500])
+        if E >= 8 and k == 1:
+            # uniformity over distinct ids (a repeated id repeats its expert by design)
+            uniq = np.arange(100000, dtype=np.int32)
+            counts = np.bincount(orc.route_hash(len(uniq), E, 1, uniq)["idx"][:, 0], minlength=E)
+            expect = len(uniq) / E
+            chi2 = float(((counts - expect) ** 2 / expect).sum())
+            assert chi2 < E + 6 * np.sqrt(2 * E)          # ~6 sigma of a chi-square(E-1)
+
+
+def test_fmix32_closed_forms():
+    # fmix32 is a bijection with fmix32(0) = 0 and no other fixed structure;
+    # check the zero point, injectivity on a block, and avalanche (one input
+    # bit flips about half of the output bits)
+    assert orc.fmix32(0) == 0
+    vals = [orc.fmix32(i) for i in range(1, 20001)]
+    assert len(set(vals)) == len(vals)
+    flips = [bin(orc.fmix32(i) ^ orc.fmix32(i ^ 1)).count("1") for i in range(1, 2001)]
+    assert 14 < float(np.mean(flips)) < 18
+
+
+def test_hash_collision_moves_to_next_free_expert():
+    """With E = 2, k = 2 the second choice must be the expert the first did
+    not take, whatever the hash of the second key is."""
+    tok = np.arange(100, dtype=np.int32)
+    r = orc.route_hash(100, 2, 2, tok)
+    assert all(sorted(row) == [0, 1] for row in r["idx"])
+    first = np.array([orc.fmix32(int(t)) % 2 for t in tok])
+    np.testing.assert_array_equal(r["idx"][:, 0], first)
