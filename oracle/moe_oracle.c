@@ -337,6 +337,63 @@ void orc_route_hash(int64_t T, int32_t E, int32_t k, const int32_t *token_ids, i
     }
 }
 
+/*
+ * Expert-choice routing ("MoE Training: Mixture of Experts", Routing
+ * Mechanisms, Expert Choice: expert_scores = router(x) transposed, each
+ * expert takes topk over tokens with k = capacity per expert).
+ *   C = min(T, max(min_capacity, ceil(T / E * capacity_factor)))
+ *   expert e takes the C tokens with the largest fp32 logit[t, e] (equal
+ *   logits: lower token index first); its rows e*C .. e*C+C-1 hold those
+ *   tokens in token order;
+ *   gate(t, e) = softmax(logits_t)_e (fp64) for a chosen pair.
+ * Outputs: row_token [E*C]; tok_row [T*E] (row of (t, e), -1 if e did not
+ * choose t); tok_gate [T*E] (0 where not chosen).
+ */
+int64_t orc_ec_capacity(int64_t T, int32_t E, double cf, int32_t min_capacity) {
+    int64_t c = (int64_t)ceil((double)T / (double)E * cf);
+    if (c < min_capacity) c = min_capacity;
+    return c < T ? c : T;
+}
+
+void orc_route_expert_choice(int64_t T, int32_t E, int64_t C, const float *logits, int32_t *row_token,
+                             int32_t *tok_row, double *tok_gate) {
+    int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
+    unsigned char *chosen = (unsigned char *)malloc((size_t)(T > 0 ? T : 1));
+    for (int64_t i = 0; i < T * E; ++i) {
+        tok_row[i] = -1;
+        tok_gate[i] = 0.0;
+    }
+    for (int32_t e = 0; e < E; ++e) {
+        /* C selection passes: each takes the best remaining token */
+        for (int64_t t = 0; t < T; ++t) chosen[t] = 0;
+        for (int64_t r = 0; r < C; ++r) {
+            int64_t best = -1;
+            for (int64_t t = 0; t < T; ++t) {
+                if (chosen[t]) continue;
+                if (best < 0 || logits[t * E + e] > logits[best * E + e]) best = t;
+            }
+            chosen[best] = 1;
+        }
+        int64_t n = 0;
+        for (int64_t t = 0; t < T; ++t)
+            if (chosen[t]) order[n++] = t;   /* token order */
+        for (int64_t r = 0; r < n; ++r) {
+            const int64_t t = order[r];
+            row_token[e * C + r] = (int32_t)t;
+            tok_row[t * E + e] = (int32_t)(e * C + r);
+        }
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        double m = -INFINITY, s = 0.0;
+        for (int32_t e = 0; e < E; ++e) m = fmax(m, (double)logits[t * E + e]);
+        for (int32_t e = 0; e < E; ++e) s += exp((double)logits[t * E + e] - m);
+        for (int32_t e = 0; e < E; ++e)
+            if (tok_row[t * E + e] >= 0) tok_gate[t * E + e] = exp((double)logits[t * E + e] - m) / s;
+    }
+    free(order);
+    free(chosen);
+}
+
 /* ------------------------------------------------------------------ */
 /* step 3: capacity, drop, permutation                                  */
 /* ------------------------------------------------------------------ */

@@ -89,6 +89,9 @@ def lib():
             L.orc_fmix32.restype = C.c_uint32
             L.orc_fmix32.argtypes = [C.c_uint32]
             L.orc_route_hash.argtypes = [C.c_int64, C.c_int32, C.c_int32, P, P, P]
+            L.orc_ec_capacity.restype = C.c_int64
+            L.orc_ec_capacity.argtypes = [C.c_int64, C.c_int32, C.c_double, C.c_int32]
+            L.orc_route_expert_choice.argtypes = [C.c_int64, C.c_int32, C.c_int64, P, P, P, P]
             _lib = L
     return _lib
 
@@ -187,6 +190,31 @@ def route_hash(T: int, E: int, k: int, token_ids: np.ndarray):
     gate = np.empty((T, k), np.float64)
     lib().orc_route_hash(T, E, k, tid.ctypes.data, idx.ctypes.data, gate.ctypes.data)
     return dict(idx=idx, gate=gate)
+
+
+def ec_capacity(w) -> int:
+    return int(lib().orc_ec_capacity(w.T, w.E, float(np.float32(w.capacity_factor)), w.min_capacity))
+
+
+def route_expert_choice(w, logits: np.ndarray):
+    """-> dict(C, row_token [E*C], tok_row [T,E], tok_gate [T,E] f64)."""
+    Cc = ec_capacity(w)
+    lg = _c(logits, np.float32)
+    row_token = np.empty(max(w.E * Cc, 1), np.int32)[: w.E * Cc]
+    tok_row = np.empty((w.T, w.E), np.int32)
+    tok_gate = np.empty((w.T, w.E), np.float64)
+    lib().orc_route_expert_choice(w.T, w.E, Cc, lg.ctypes.data, row_token.ctypes.data, tok_row.ctypes.data,
+                                  tok_gate.ctypes.data)
+    return dict(C=Cc, row_token=row_token, tok_row=tok_row, tok_gate=tok_gate)
+
+
+def forward_tokens_ec(w, inp, ec, tokens) -> np.ndarray:
+    """Layer output under expert-choice routing: out_t = sum over the experts
+    that chose t (expert order) of gate * E_e(x_t), + shared + residual."""
+    import dataclasses as _dc
+    wk = _dc.replace(w, k=w.E) if _dc.is_dataclass(w) else w
+    idx = np.tile(np.arange(w.E, dtype=np.int32), (w.T, 1))
+    return forward_tokens(wk, inp, idx, ec["tok_gate"], ec["tok_row"].reshape(-1), tokens)
 
 
 def dispatch(w, idx: np.ndarray):

@@ -475,3 +475,41 @@ def test_hash_collision_moves_to_next_free_expert():
     assert all(sorted(row) == [0, 1] for row in r["idx"])
     first = np.array([orc.fmix32(int(t)) % 2 for t in tok])
     np.testing.assert_array_equal(r["idx"][:, 0], first)
+
+
+
+# ------------------------------------------------------------ expert-choice routing
+def test_expert_choice_selection_against_sort():
+    w = _cfg(T=300, E=8, k=1, capacity_factor=2.0, min_capacity=4)
+    g = np.random.default_rng(21)
+    lg = g.standard_normal((w.T, w.E)).astype(np.float32)
+    lg[::4] = np.round(lg[::4] * 2) / 2                      # ties
+    ec = orc.route_expert_choice(w, lg)
+    C = ec["C"]
+    assert C == int(np.ceil(300 / 8 * 2.0)) == 75
+    for e in range(w.E):
+        seg = ec["row_token"][e * C:(e + 1) * C]
+        want = sorted(t for _, t in sorted((-float(lg[t, e]), t) for t in range(w.T))[:C])
+        assert list(seg) == want                              # top-C, ties to lower index, token order
+        for r, t in enumerate(seg):
+            assert ec["tok_row"][t, e] == e * C + r
+    assert np.all((ec["tok_row"] >= 0).sum(0) == C)           # every expert exactly C tokens
+    probs = sp.softmax(lg.astype(np.float64), axis=1)
+    mask = ec["tok_row"] >= 0
+    np.testing.assert_allclose(ec["tok_gate"][mask], probs[mask], rtol=1e-12)
+    assert np.all(ec["tok_gate"][~mask] == 0)
+
+
+def test_expert_choice_full_capacity_is_the_dense_soft_mixture():
+    """C = T: every expert takes every token, so the layer is the dense
+    softmax-weighted mixture of all experts (EfficientMoE-style brute force
+    with all E experts and no renormalisation)."""
+    w = _cfg(T=24, d=8, E=4, k=1, F=12, capacity_factor=4.0, min_capacity=0, renormalize=False)
+    inp = wl.make_inputs(w)
+    lg = orc.router_logits(w, inp)
+    ec = orc.route_expert_choice(w, lg)
+    assert ec["C"] == w.T and np.all(ec["tok_row"] >= 0)
+    out = orc.forward_tokens_ec(w, inp, ec, np.arange(w.T))
+    allv, _ = orc.dense_all(w, inp, np.zeros((w.T, 1), np.int32), np.ones((w.T, 1)), None)
+    probs = sp.softmax(lg.astype(np.float64), axis=1)
+    np.testing.assert_allclose(out, np.einsum("te,ted->td", probs, allv), rtol=1e-12, atol=1e-13)
