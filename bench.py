@@ -16,6 +16,11 @@ Prints one JSON line (rank 0).  With --gpus N > 1 (under torchrun) every rank
 runs an independent replica of the workload (weak scaling, no collective on
 the data path); the time is the maximum over ranks.
 
+--routing expert_choice | hash runs the same layer under expert-choice
+routing (every expert takes C = ceil(T/E * k) tokens, the compute of top-k)
+or under hash routing of Zipf-distributed token ids; the default, top-k, is
+the headline.
+
 --impl reference times the plain CPU oracle on this machine's host cores on
 a bounded sample of the same workload (full routing of every token plus the
 experts of a sample of tokens, extrapolated to the whole batch).
@@ -23,6 +28,7 @@ experts of a sample of tokens, extrapolated to the whole batch).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -56,8 +62,8 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def config_of(w):
-    return {"workload": w.name, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d_model": w.d,
+def config_of(w, routing="topk"):
+    return {"workload": w.name, "routing": routing, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d_model": w.d,
             "experts": w.E, "top_k": w.k, "d_ff": w.F, "activation": ACT_NAME[w.activation],
             "score": "sigmoid" if w.score_fn == wl.SIGMOID else "softmax",
             "shared_experts": w.num_shared, "residual": bool(w.residual),
@@ -84,10 +90,19 @@ def gemm_flops(w, kept_rows):
     return f1, f2
 
 
-def hbm_bytes(w, kept_rows):
+def hbm_bytes(w, kept_rows, routing="topk"):
     """Algorithmic bytes of the HBM-bound stages (route, dispatch, combine)."""
     eb = w.elem_bytes
     T, d, E, S = w.T, w.d, w.E, w.T * w.k
+    if routing == "expert_choice":
+        R = kept_rows
+        # logits GEMM (x, w_r in; logits out), selection (logits in; tok_row,
+        # row_token out), gates (logits, tok_row in; tok_gate out)
+        route = T * d * eb + E * d * eb + T * E * 4 + T * E * 4 + T * E * 4 + R * 4 + 3 * T * E * 4
+        permute = 2 * R * d * eb + R * 4                       # row gather: read and write each chosen row
+        combine = R * d * 4 + T * d * eb + (T * d * eb if w.residual else 0) + \
+            (T * d * 4 if w.num_shared else 0) + T * E * 8
+        return route, permute, combine
     route = T * d * eb + E * d * eb + T * E * 4 + S * 8 + T * 4
     permute = T * d * eb + kept_rows * d * eb + S * 4 * 3 + T * w.k * 4
     combine = kept_rows * d * 4 + T * d * eb + (T * d * eb if w.residual else 0) + (T * d * 4 if w.num_shared else 0) + S * 8
@@ -109,11 +124,25 @@ def whole_job_value(tokens_per_rank: int, world: int, ms_per_step: float) -> flo
     return tokens_per_rank * world / (ms_per_step * 1e-3)
 
 
-def launches_per_step(w):
-    n = 2 if (w.E <= 32 and w.dtype == wl.F32) else 3   # (logits GEMM +) routing + partial reduce
-    n += 4 if w.T * w.k > 0 else 1       # histogram, scan, rank, row copy
-    n += 2 + (2 if w.num_shared else 0)  # expert GEMMs (+ shared expert)
-    n += 2                               # combine, statistics
+def launches_per_step(w, routing="topk"):
+    S = w.T * w.k
+    if routing == "expert_choice":
+        n = 1 + (1 if w.router_bias else 0)   # logits GEMM (+ bias)
+        n += 3                                # selection, gates, row gather
+        n += 2 + (2 if w.num_shared else 0)   # expert GEMMs (+ shared expert)
+        return n + 1                          # combine
+    if routing == "hash":
+        n = 1                                 # hash routing
+    else:
+        n = 2 if (w.E <= 32 and w.dtype == wl.F32) else 3   # (logits GEMM +) routing + partial reduce
+    if S == 0:
+        n += 1
+    elif S <= 8192 and w.E <= 256:
+        n += 2                                # one-CTA dispatch, row copy
+    else:
+        n += 4                                # histogram, scan, rank, row copy
+    n += 2 + (2 if w.num_shared else 0)       # expert GEMMs (+ shared expert)
+    n += 2                                    # combine, statistics
     return n
 
 
@@ -265,7 +294,18 @@ def run_ours(args, w, rank, world, local):
     cfg = moe.config_for(w)
     wts = {k: dev[k] for k in ("w_router", "b_router", "w1", "b1", "w3", "w2", "b2", "shared_w1",
                                "shared_w3", "shared_w2") if k in dev}
-    layer = moe.MoELayer(cfg, wts, dev.get("sel_bias"))
+    if args.routing == "expert_choice":
+        layer = moe.ExpertChoiceLayer(cfg, wts)
+        fwd = layer.forward
+    elif args.routing == "hash":
+        layer = moe.MoELayer(cfg, wts, dev.get("sel_bias"))
+        token_ids = torch.from_numpy(wl.make_token_ids(w)).cuda()
+
+        def fwd(xx, oo, stream=None, stage_events=None):
+            return layer.forward_hashed(xx, token_ids, oo, stream, stage_events)
+    else:
+        layer = moe.MoELayer(cfg, wts, dev.get("sel_bias"))
+        fwd = layer.forward
     x = dev["x"]
     out = torch.empty(w.T, w.d, dtype=layer.out_dtype(), device="cuda")
     stream = torch.cuda.current_stream()
@@ -284,7 +324,7 @@ def run_ours(args, w, rank, world, local):
         return evs, [[e.cuda_event for e in row] for row in evs]
 
     for _ in range(max(3, args.warmup)):
-        layer.forward(x, out)
+        fwd(x, out)
     torch.cuda.synchronize()
     code = moe.moe_check_device_error()
     if code:
@@ -301,7 +341,7 @@ def run_ours(args, w, rank, world, local):
         with ClockSampler(uuid) as cs:
             t0.record(stream)
             for i in range(args.steps):
-                layer.forward(x, out, stage_events=handles[i])
+                fwd(x, out, stage_events=handles[i])
             t1.record(stream)
             barrier()
         return t0.elapsed_time(t1), evs, cs.summary()
@@ -315,14 +355,18 @@ def run_ours(args, w, rank, world, local):
     stage_ms = stage.mean(axis=0)               # route, permute, ffn1, ffn2, shared, combine, stats
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms = total_ms / args.steps
-    stats = layer.stats()
-    kept = int(stats["total_kept"])
+    if args.routing == "expert_choice":
+        stats = None
+        kept = w.E * layer.capacity
+    else:
+        stats = layer.stats()
+        kept = int(stats["total_kept"])
     code = moe.moe_check_device_error()
     if code:
         raise RuntimeError(f"device error flag {code} after the timed region")
 
     # ----------------------------------------------------------- end to end from host buffers
-    if args.no_e2e:
+    if args.no_e2e or args.routing == "hash":
         return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, None)
     # two pinned input and output batches, used round-robin; every step
     # uploads its whole x and downloads its whole output, overlapped with
@@ -354,7 +398,7 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
     ffn1_ms, ffn2_ms = float(stage_ms[2]), float(stage_ms[3])
     achieved = f1 / (ffn1_ms * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    rb, pb, cb = hbm_bytes(w, kept)
+    rb, pb, cb = hbm_bytes(w, kept, args.routing)
     hbm_ms = float(stage_ms[0] + stage_ms[1] + stage_ms[5])
     hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gemm_ms = ffn1_ms + ffn2_ms + float(stage_ms[4])
@@ -362,7 +406,7 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
         "metric": METRIC, "value": whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
-        "data": "synthetic", "config": config_of(w),
+        "data": "synthetic", "config": config_of(w, args.routing),
         "roofline": {"kernel": "grouped_gemm_kernel (expert W1/W3 + SwiGLU)" if w.gated
                      else "grouped_gemm_kernel (expert W1 + activation)",
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -383,9 +427,9 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
             "value": whole_job_value(w.T, world, e2e_ms), "unit": "tokens/s",
             "h2d_bytes_per_step": int(x.numel() * x.element_size()),
             "d2h_bytes_per_step": int(out.numel() * out.element_size()), "ms_per_step": e2e_ms},
-        "gpu_launches": launches_per_step(w) * args.steps,
+        "gpu_launches": launches_per_step(w, args.routing) * args.steps,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.routing == "topk":
         t, desc, cores = oracle_sample(w, inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": w.T / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
@@ -407,6 +451,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (profiling of a smaller case; not a headline)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--routing", default="topk", choices=["topk", "expert_choice", "hash"],
+                    help="token-choice top-k (the headline), expert-choice or hash routing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -418,7 +464,11 @@ def main():
     w = wl.WORKLOADS[args.workload]
     if args.tokens is not None:
         w = w.scaled(args.tokens)
+    if args.routing == "expert_choice":
+        w = dataclasses.replace(w, capacity_factor=float(w.k))
     if args.impl == "reference":
+        if args.routing != "topk":
+            ap.error("--impl reference times the top-k layer only")
         return run_reference(args, w, rank, world)
     return run_ours(args, w, rank, world, local)
 

@@ -157,11 +157,13 @@ enum {
     MOE_WS_ROUTE = 1,
     MOE_WS_PERMUTE = 2,
     MOE_WS_EXPERT_FFN = 3,
-    MOE_WS_SHARED_FFN = 4
+    MOE_WS_SHARED_FFN = 4,
+    MOE_WS_EXPERT_CHOICE = 5
 };
 
 /* Workspace bytes the given call needs (host output).  A workspace sized
- * for MOE_WS_FORWARD is large enough for every call.  Workspace contents
+ * for MOE_WS_FORWARD is large enough for every call but
+ * moe_forward_expert_choice.  Workspace contents
  * need no initialisation and carry nothing between calls. */
 moe_status_t moe_workspace_size(const moe_config_t *cfg, int32_t which, size_t *bytes);
 
@@ -337,6 +339,63 @@ moe_status_t moe_forward_from_routing(const moe_config_t *cfg, const moe_weights
                                       const void *x, const int32_t *topk_idx, const float *topk_w,
                                       void *out, const moe_forward_io_t *io, void *ws,
                                       size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Expert-choice routing ("MoE Training: Mixture of Experts" page, Core
+ * Concepts, Routing Mechanisms, Expert Choice Routing): the router's scores
+ * are transposed to [experts, tokens] and every expert keeps the C tokens
+ * with the largest score, so each expert processes exactly C tokens and a
+ * token may be taken by any number of experts, including none.
+ *
+ * Readings where the page is silent: the score is the router logit
+ * (x w_r^T + b_router, fp32); C = min(T, max(min_capacity,
+ * ceil(T / E * capacity_factor))) with cfg->capacity_factor (drop_tokens and
+ * top_k are not used); equal logits go to the lower token index; the gate
+ * of a chosen (token, expert) pair is the token's softmax probability for
+ * that expert; a token no expert chose gets only the shared expert and the
+ * residual.
+ *
+ * moe_ec_capacity: host output *capacity = C.
+ * moe_route_expert_choice: logits [T,E] fp32 (device, bias included) ->
+ *   row_token [E*C] int32: row e*C + i holds the i-th chosen token of
+ *   expert e in token order; tok_row [T,E] int32: row of (t, e), -1 if e
+ *   did not choose t; tok_gate [T,E] fp32: gate, 0 where not chosen;
+ *   offsets [E+1] int32 = e*C.  The selection is exact (no rounding enters
+ *   it), so it is reproducible bit for bit from the same logits.
+ * Errors: MOE_ERR_INVALID_ARG without a finite capacity_factor > 0;
+ *   MOE_ERR_UNSUPPORTED when T * E does not fit in int32.
+ */
+moe_status_t moe_ec_capacity(const moe_config_t *cfg, int64_t *capacity);
+moe_status_t moe_route_expert_choice(const moe_config_t *cfg, const float *logits, int32_t *row_token,
+                                     int32_t *tok_row, float *tok_gate, int32_t *offsets,
+                                     moe_stream_t stream);
+
+/* Optional outputs of moe_forward_expert_choice (device buffers, sizes as
+ * for moe_route_expert_choice; logits [T,E]); NULL members stay in the
+ * workspace.  stage_events as in moe_forward_io_t ([1] after routing, [2]
+ * after the row gather, [3]/[4] expert GEMMs, [5] shared, [6] = [7]
+ * combined: this call computes no balance statistics, as every expert
+ * takes exactly C tokens). */
+typedef struct {
+    float *logits;
+    int32_t *row_token;
+    int32_t *tok_row;
+    float *tok_gate;
+    int32_t *offsets;
+    void *const *stage_events;
+} moe_ec_io_t;
+
+/*
+ * The layer forward under expert-choice routing: router logits -> expert
+ * choice -> gather of the chosen rows (E*C rows, expert-major) -> routed
+ * experts (+ shared expert) -> gate-weighted combine (+ residual), all on
+ * `stream`.  x [T,d] and out [T,d] in cfg->dtype.
+ * Workspace: moe_workspace_size(MOE_WS_EXPERT_CHOICE) (not covered by
+ * MOE_WS_FORWARD).
+ */
+moe_status_t moe_forward_expert_choice(const moe_config_t *cfg, const moe_weights_t *weights, const void *x,
+                                       void *out, const moe_ec_io_t *io, void *ws, size_t ws_bytes,
+                                       moe_stream_t stream);
 
 /* Reads and clears the device error flag (host output *code: 0 = none,
  * else a moe_status_t).  Synchronises the device first. */

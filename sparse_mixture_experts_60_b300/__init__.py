@@ -16,8 +16,8 @@ from __future__ import annotations
 import ctypes as C
 from typing import Dict, Optional
 
-from ._lib import (MOE_STAGE_EVENTS, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD, MOE_WS_PERMUTE,  # noqa: F401
-                   MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
+from ._lib import (MOE_STAGE_EVENTS, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,  # noqa: F401
+                   MOE_WS_PERMUTE, MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEECIO, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
                    last_error, lib)
 
 SOFTMAX, SIGMOID = 0, 1
@@ -186,6 +186,42 @@ def moe_route_hash(cfg, token_ids, topk_idx, topk_w, stream=None) -> None:
     check(lib().moe_route_hash(C.byref(cfg), _ptr(token_ids), _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
 
 
+def moe_ec_capacity(cfg) -> int:
+    """Tokens per expert under expert-choice routing."""
+    c = C.c_int64(0)
+    check(lib().moe_ec_capacity(C.byref(cfg), C.byref(c)))
+    return c.value
+
+
+def moe_route_expert_choice(cfg, logits, row_token, tok_row, tok_gate, offsets, stream=None) -> None:
+    """Expert-choice routing of fp32 logits [T,E] into row_token [E*C],
+    tok_row [T,E], tok_gate [T,E] and offsets [E+1]."""
+    check(lib().moe_route_expert_choice(C.byref(cfg), _ptr(logits), _ptr(row_token), _ptr(tok_row),
+                                        _ptr(tok_gate), _ptr(offsets), _stream(stream)))
+
+
+def ec_io_struct(io: Optional[Dict], stage_events=None) -> Optional[MoEECIO]:
+    if io is None and stage_events is None:
+        return None
+    io = io or {}
+    s = MoEECIO(**{k: _ptr(io.get(k)) for k, _ in MoEECIO._fields_ if k != "stage_events"})
+    if stage_events is not None:
+        arr = (C.c_void_p * MOE_STAGE_EVENTS)(*[int(e) for e in stage_events])
+        s._events_keepalive = arr
+        s.stage_events = C.cast(arr, C.c_void_p)
+    return s
+
+
+def moe_forward_expert_choice(cfg, weights: Dict, x, out, io: Optional[Dict], ws, stream=None,
+                              stage_events=None) -> None:
+    """The layer under expert-choice routing; ``io`` keyed like ``MoEECIO``."""
+    p, n = _ws(ws)
+    wst = weights_struct(weights)
+    ios = ec_io_struct(io, stage_events)
+    check(lib().moe_forward_expert_choice(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(out),
+                                          C.byref(ios) if ios is not None else None, p, n, _stream(stream)))
+
+
 def moe_check_device_error() -> int:
     code = C.c_int32(0)
     check(lib().moe_check_device_error(C.byref(code)))
@@ -199,7 +235,55 @@ def stats_from_buffer(buf) -> Dict:
     return {k: getattr(s, k) for k, _ in MoEStats._fields_}
 
 
-class MoELayer:
+class _HostPipeline:
+    """Overlapped host-buffer batches for a layer class with ``cfg``,
+    ``device``, ``out_dtype()`` and ``forward(x, out, stream)``."""
+
+    def run_host_batches(self, x_hosts, out_hosts, n_steps: int, stream=None):
+        """Run ``n_steps`` batches from host memory with the copies overlapped:
+        batch i is uploaded on a copy stream while batch i-1 computes, and its
+        output is downloaded on another copy stream while batch i+1 computes.
+        ``x_hosts`` / ``out_hosts``: sequences of pinned host tensors, used
+        round-robin (step i reads ``x_hosts[i % len]`` and writes
+        ``out_hosts[i % len]``).  Every step copies its whole input in and its
+        whole output out.  Returns after enqueueing; synchronise to wait."""
+        import torch
+        comp = stream or torch.cuda.current_stream()
+        if not hasattr(self, "_pipe"):
+            dev = self.device
+            T, d = self.cfg.num_tokens, self.cfg.d_model
+            xdt = x_hosts[0].dtype
+            self._pipe = dict(
+                h2d=torch.cuda.Stream(device=dev), d2h=torch.cuda.Stream(device=dev),
+                xd=[torch.empty(T, d, dtype=xdt, device=dev) for _ in range(2)],
+                od=[torch.empty(T, d, dtype=self.out_dtype(), device=dev) for _ in range(2)])
+        P = self._pipe
+        P["h2d"].wait_stream(comp)       # the first upload follows earlier work on `comp`
+        x_ready = [torch.cuda.Event() for _ in range(2)]
+        x_free = [torch.cuda.Event() for _ in range(2)]
+        o_ready = [torch.cuda.Event() for _ in range(2)]
+        o_free = [torch.cuda.Event() for _ in range(2)]
+        for i in range(n_steps):
+            b = i % 2
+            if i >= 2:
+                P["h2d"].wait_event(x_free[b])            # batch i-2 no longer reads xd[b]
+            with torch.cuda.stream(P["h2d"]):
+                P["xd"][b].copy_(x_hosts[i % len(x_hosts)], non_blocking=True)
+                x_ready[b].record(P["h2d"])
+            comp.wait_event(x_ready[b])
+            if i >= 2:
+                comp.wait_event(o_free[b])                # batch i-2's output left od[b]
+            self.forward(P["xd"][b], P["od"][b], comp)
+            x_free[b].record(comp)
+            o_ready[b].record(comp)
+            P["d2h"].wait_event(o_ready[b])
+            with torch.cuda.stream(P["d2h"]):
+                out_hosts[i % len(out_hosts)].copy_(P["od"][b], non_blocking=True)
+                o_free[b].record(P["d2h"])
+        comp.wait_stream(P["d2h"])
+
+
+class MoELayer(_HostPipeline):
     """Owner of one layer's device weights, workspace and intermediate
     buffers.  ``weights``: dict of CUDA tensors (``w_router``, ``b_router``,
     ``w1``, ``b1``, ``w3``, ``w2``, ``b2``, ``shared_w1``, ``shared_w3``,
@@ -263,51 +347,40 @@ class MoELayer:
                                  self.ws, stream, stage_events)
         return out
 
-    def run_host_batches(self, x_hosts, out_hosts, n_steps: int, stream=None):
-        """Run ``n_steps`` batches from host memory with the copies overlapped:
-        batch i is uploaded on a copy stream while batch i-1 computes, and its
-        output is downloaded on another copy stream while batch i+1 computes.
-        ``x_hosts`` / ``out_hosts``: sequences of pinned host tensors, used
-        round-robin (step i reads ``x_hosts[i % len]`` and writes
-        ``out_hosts[i % len]``).  Every step copies its whole input in and its
-        whole output out.  Returns after enqueueing; synchronise to wait."""
-        import torch
-        comp = stream or torch.cuda.current_stream()
-        if not hasattr(self, "_pipe"):
-            dev = self.device
-            T, d = self.cfg.num_tokens, self.cfg.d_model
-            xdt = x_hosts[0].dtype
-            self._pipe = dict(
-                h2d=torch.cuda.Stream(device=dev), d2h=torch.cuda.Stream(device=dev),
-                xd=[torch.empty(T, d, dtype=xdt, device=dev) for _ in range(2)],
-                od=[torch.empty(T, d, dtype=self.out_dtype(), device=dev) for _ in range(2)])
-        P = self._pipe
-        P["h2d"].wait_stream(comp)       # the first upload follows earlier work on `comp`
-        x_ready = [torch.cuda.Event() for _ in range(2)]
-        x_free = [torch.cuda.Event() for _ in range(2)]
-        o_ready = [torch.cuda.Event() for _ in range(2)]
-        o_free = [torch.cuda.Event() for _ in range(2)]
-        for i in range(n_steps):
-            b = i % 2
-            if i >= 2:
-                P["h2d"].wait_event(x_free[b])            # batch i-2 no longer reads xd[b]
-            with torch.cuda.stream(P["h2d"]):
-                P["xd"][b].copy_(x_hosts[i % len(x_hosts)], non_blocking=True)
-                x_ready[b].record(P["h2d"])
-            comp.wait_event(x_ready[b])
-            if i >= 2:
-                comp.wait_event(o_free[b])                # batch i-2's output left od[b]
-            self.forward(P["xd"][b], P["od"][b], comp)
-            x_free[b].record(comp)
-            o_ready[b].record(comp)
-            P["d2h"].wait_event(o_ready[b])
-            with torch.cuda.stream(P["d2h"]):
-                out_hosts[i % len(out_hosts)].copy_(P["od"][b], non_blocking=True)
-                o_free[b].record(P["d2h"])
-        comp.wait_stream(P["d2h"])
-
     def stats(self) -> Dict:
         return stats_from_buffer(self.io["stats"])
+
+
+class ExpertChoiceLayer(_HostPipeline):
+    """One layer under expert-choice routing: device weights (as for
+    ``MoELayer``), its workspace and the routing outputs."""
+
+    def __init__(self, cfg: MoEConfig, weights: Dict, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.weights = weights
+        self.device = torch.device(device)
+        T, E = cfg.num_tokens, cfg.num_experts
+        self.capacity = moe_ec_capacity(cfg)
+        dev = self.device
+        self.ws = torch.empty(max(moe_workspace_size(cfg, MOE_WS_EXPERT_CHOICE), 1), dtype=torch.uint8, device=dev)
+        i32, f32 = torch.int32, torch.float32
+        self.io = dict(logits=torch.empty(T, E, dtype=f32, device=dev),
+                       row_token=torch.empty(max(E * self.capacity, 1), dtype=i32, device=dev),
+                       tok_row=torch.empty(T, E, dtype=i32, device=dev),
+                       tok_gate=torch.empty(T, E, dtype=f32, device=dev),
+                       offsets=torch.empty(E + 1, dtype=i32, device=dev))
+
+    def out_dtype(self):
+        import torch
+        return torch.float32 if self.cfg.dtype == F32 else torch.bfloat16
+
+    def forward(self, x, out=None, stream=None, stage_events=None):
+        import torch
+        if out is None:
+            out = torch.empty(self.cfg.num_tokens, self.cfg.d_model, dtype=self.out_dtype(), device=self.device)
+        moe_forward_expert_choice(self.cfg, self.weights, x, out, self.io, self.ws, stream, stage_events)
+        return out
 
 
 def bias_update(layer: MoELayer, gamma: float, stream=None) -> None:

@@ -16,7 +16,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_BAD_ALIGNMENT", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_DEVICE_TIMEOUT"}
-MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_SHARED_FFN = range(5)
+MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_SHARED_FFN, MOE_WS_EXPERT_CHOICE = range(6)
 
 
 class MoEConfig(C.Structure):
@@ -47,6 +47,11 @@ class MoEForwardIO(C.Structure):
                                           "stage_events")]
 
 
+class MoEECIO(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("logits", "row_token", "tok_row", "tok_gate", "offsets",
+                                          "stage_events")]
+
+
 class MoEError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -73,6 +78,9 @@ _SIGS = {
     "moe_forward": ([P] * 6 + [P, C.c_size_t, P], C.c_int),
     "moe_forward_from_routing": ([P] * 7 + [P, C.c_size_t, P], C.c_int),
     "moe_route_hash": ([P] * 4 + [P], C.c_int),
+    "moe_ec_capacity": ([P, C.POINTER(C.c_int64)], C.c_int),
+    "moe_route_expert_choice": ([P] * 6 + [P], C.c_int),
+    "moe_forward_expert_choice": ([P] * 5 + [P, C.c_size_t, P], C.c_int),
     "moe_check_device_error": ([C.POINTER(C.c_int32)], C.c_int),
 }
 

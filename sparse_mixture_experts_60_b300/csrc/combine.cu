@@ -102,6 +102,93 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, c
     }
 }
 
+// Combine for more than kMaxTopK slots per token (expert-choice routing on
+// many experts).  Warp per token: the token's kept (row, gate) pairs are
+// first compacted into a per-warp shared list in slot order (ballots over 32
+// slots at a time), then summed in that order like the narrow kernel.
+template <bool BF16>
+__global__ void __launch_bounds__(256) combine_wide_kernel(int64_t T, int d, int k, const float *__restrict__ y,
+                                                           const int32_t *__restrict__ inv,
+                                                           const float *__restrict__ topk_w,
+                                                           const float *__restrict__ z, const void *__restrict__ x,
+                                                           void *__restrict__ out) {
+    extern __shared__ int wlist[];                       // [8 warps][k] rows, then [8][k] gates
+    constexpr int V = BF16 ? 8 : 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = (int64_t)blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    int *rows = wlist + warp * k;
+    float *wts = reinterpret_cast<float *>(wlist + 8 * k) + warp * k;
+    int n = 0;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+        const int j = j0 + lane;
+        const int r = j < k ? __ldg(inv + t * k + j) : -1;
+        const unsigned b = __ballot_sync(kFull, r >= 0);
+        if (r >= 0) {
+            const int pos = n + __popc(b & ((1u << lane) - 1u));
+            rows[pos] = r;
+            wts[pos] = __ldg(topk_w + t * k + j);
+        }
+        n += __popc(b);
+    }
+    __syncwarp();
+    for (int c = lane; c < d / V; c += 32) {
+        float acc[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < n; ++i) {
+            const float4 *src = reinterpret_cast<const float4 *>(y + (int64_t)rows[i] * d) + c * (V / 4);
+            const float wv = wts[i];
+#pragma unroll
+            for (int h = 0; h < V / 4; ++h) {
+                const float4 u = __ldg(src + h);
+                acc[4 * h + 0] = fmaf(wv, u.x, acc[4 * h + 0]);
+                acc[4 * h + 1] = fmaf(wv, u.y, acc[4 * h + 1]);
+                acc[4 * h + 2] = fmaf(wv, u.z, acc[4 * h + 2]);
+                acc[4 * h + 3] = fmaf(wv, u.w, acc[4 * h + 3]);
+            }
+        }
+        if (z) {
+            const float4 *src = reinterpret_cast<const float4 *>(z + t * d) + c * (V / 4);
+#pragma unroll
+            for (int h = 0; h < V / 4; ++h) {
+                const float4 u = __ldg(src + h);
+                acc[4 * h + 0] += u.x;
+                acc[4 * h + 1] += u.y;
+                acc[4 * h + 2] += u.z;
+                acc[4 * h + 3] += u.w;
+            }
+        }
+        if (BF16) {
+            if (x) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(x) + t * d) + c);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    acc[2 * h] += __uint_as_float(w[h] << 16);
+                    acc[2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+                o[h] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + t * d)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            if (x) {
+                const float4 u = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + t * d) + c);
+                acc[0] += u.x;
+                acc[1] += u.y;
+                acc[2] += u.z;
+                acc[3] += u.w;
+            }
+            reinterpret_cast<float4 *>(static_cast<float *>(out) + t * d)[c] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
+    }
+}
+
 template <typename T, typename Op>
 __device__ T block_reduce(T v, T *sm, Op op) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
@@ -183,6 +270,16 @@ cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_pe
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const unsigned grid = (unsigned)ceil_div(T, 8);
+    if (k > kMaxTopK) {
+        const size_t smem = (size_t)16 * k * sizeof(int);
+        auto kern = dtype == 1 ? combine_wide_kernel<true> : combine_wide_kernel<false>;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<grid, 256, smem, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
+        return cudaGetLastError();
+    }
     if (dtype == 1) combine_kernel<true><<<grid, 256, 0, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
     else combine_kernel<false><<<grid, 256, 0, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
     return cudaGetLastError();

@@ -109,7 +109,66 @@ size_t forward_ws(const moe_config_t *c) {
     return n;
 }
 
+// Expert choice: C = min(T, max(min_capacity, ceil(T / E * capacity_factor))).
+int64_t ec_capacity_of(const moe_config_t *c) {
+    const int64_t T = c->num_tokens;
+    int64_t cap = (int64_t)ceil((double)T / (double)c->num_experts * (double)c->capacity_factor);
+    if (cap < c->min_capacity) cap = c->min_capacity;
+    return cap < T ? cap : T;
+}
+
+size_t ec_ws(const moe_config_t *c) {
+    const size_t T = (size_t)c->num_tokens, E = (size_t)c->num_experts, d = (size_t)c->d_model;
+    const size_t R = E * (size_t)ec_capacity_of(c), F = (size_t)c->d_ff;
+    size_t n = align256(T * E * 4) * 3 + align256(R * 4) + align256((E + 1) * 4);   // logits, tok_row, gate, ...
+    n += align256(R * d * elem_bytes(c)) + align256(R * F * elem_bytes(c)) + align256(R * d * 4);
+    if (c->num_shared) n += shared_ws(c) + align256(T * d * 4);
+    return n;
+}
+
 // ------------------------------------------------------------------ step bodies (no validation)
+// logits [T,E] = x w_r^T + b_router (tensor cores for bf16 where the GEMM takes the shape)
+moe_status_t router_logits_impl(const moe_config_t *c, const void *x, const void *w_router, const float *b_router,
+                                float *logits, cudaStream_t s) {
+    if (c->num_tokens == 0) return MOE_OK;
+    cudaError_t e;
+    if (c->dtype == MOE_DTYPE_BF16 && grouped_gemm_supported(c->num_experts, c->d_model, 0, 1, 0)) {
+        GemmProblem g{};
+        g.A = static_cast<const bf16 *>(x);
+        g.a_rows = c->num_tokens;
+        g.B = static_cast<const bf16 *>(w_router);
+        g.b_rows_total = c->num_experts;
+        g.b_group_rows = c->num_experts;
+        g.G = 1;
+        g.M = (int)c->num_tokens;
+        g.N = c->num_experts;
+        g.K = c->d_model;
+        g.out = logits;
+        g.ldo = c->num_experts;
+        g.out_f32 = 1;
+        e = launch_grouped_gemm(g, s);
+    } else {
+        RouteParams p{};
+        p.T = c->num_tokens;
+        p.E = c->num_experts;
+        p.d = c->d_model;
+        p.x = x;
+        p.w_router = w_router;
+        p.logits = logits;
+        e = launch_router_logits_simt(p, c->dtype, s);
+    }
+    if (e == cudaSuccess) e = launch_add_bias(logits, b_router, c->num_tokens, c->num_experts, s);
+    return cuda_status(e, "router logits launch");
+}
+
+moe_status_t ec_route_impl(const moe_config_t *c, const float *logits, int32_t *row_token, int32_t *tok_row,
+                           float *tok_gate, int32_t *offsets, cudaStream_t s) {
+    cudaError_t e = launch_ec_select(logits, c->num_tokens, c->num_experts, ec_capacity_of(c), row_token, tok_row,
+                                     offsets, s);
+    if (e == cudaSuccess) e = launch_ec_gates(logits, tok_row, c->num_tokens, c->num_experts, tok_gate, s);
+    return cuda_status(e, "expert-choice routing launch");
+}
+
 moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_router, const float *b_router,
                         const float *sel_bias, float *logits, const float *logits_in, int32_t *topk_idx,
                         float *topk_w, float *lse, float *prob_mean, int32_t *counts, void *ws,
@@ -325,6 +384,14 @@ moe_status_t check_bias(const void *b) {
     return (b && !aligned16(b)) ? fail(MOE_ERR_BAD_ALIGNMENT, "expert bias is not 16-byte aligned") : MOE_OK;
 }
 
+moe_status_t check_ec(const moe_config_t *c) {
+    if (!(c->capacity_factor > 0.0f && isfinite(c->capacity_factor)))
+        return fail(MOE_ERR_INVALID_ARG, "expert choice needs a finite capacity_factor > 0");
+    if (c->num_tokens * (int64_t)c->num_experts > INT32_MAX)
+        return fail(MOE_ERR_UNSUPPORTED, "expert choice needs num_tokens * num_experts to fit in int32");
+    return MOE_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -346,6 +413,7 @@ moe_status_t moe_workspace_size(const moe_config_t *cfg, int32_t which, size_t *
         case MOE_WS_PERMUTE: *bytes = permute_ws(cfg); return MOE_OK;
         case MOE_WS_EXPERT_FFN: *bytes = ffn_ws(cfg); return MOE_OK;
         case MOE_WS_SHARED_FFN: *bytes = shared_ws(cfg); return MOE_OK;
+        case MOE_WS_EXPERT_CHOICE: TRY(check_ec(cfg)); *bytes = ec_ws(cfg); return MOE_OK;
         default: return fail(MOE_ERR_INVALID_ARG, "unknown workspace kind %d", which);
     }
 }
@@ -654,6 +722,89 @@ moe_status_t moe_route_hash(const moe_config_t *cfg, const int32_t *token_ids, i
     return cuda_status(launch_route_hash(T, cfg->num_experts, cfg->top_k, token_ids, topk_idx, topk_w,
                                          static_cast<cudaStream_t>(stream)),
                        "moe_route_hash launch");
+}
+
+moe_status_t moe_ec_capacity(const moe_config_t *cfg, int64_t *capacity) {
+    TRY(check_cfg(cfg));
+    TRY(check_ec(cfg));
+    TRY(need(capacity, "capacity"));
+    *capacity = ec_capacity_of(cfg);
+    return MOE_OK;
+}
+
+moe_status_t moe_route_expert_choice(const moe_config_t *cfg, const float *logits, int32_t *row_token,
+                                     int32_t *tok_row, float *tok_gate, int32_t *offsets, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(check_ec(cfg));
+    const int64_t T = cfg->num_tokens, TE = T * cfg->num_experts;
+    TRY(need(logits, "logits", TE));
+    TRY(need(row_token, "row_token", ec_capacity_of(cfg) * cfg->num_experts));
+    TRY(need(tok_row, "tok_row", TE));
+    TRY(need(tok_gate, "tok_gate", TE));
+    TRY(need(offsets, "offsets"));
+    return ec_route_impl(cfg, logits, row_token, tok_row, tok_gate, offsets, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward_expert_choice(const moe_config_t *cfg, const moe_weights_t *w, const void *x, void *out,
+                                       const moe_ec_io_t *io, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    TRY(check_ec(cfg));
+    TRY(need(w, "weights"));
+    TRY(need16(x, "x", cfg->num_tokens));
+    TRY(need16(out, "out", cfg->num_tokens));
+    TRY(need16(w->w_router, "w_router"));
+    TRY(check_weights_ffn(cfg, w->w1, w->w3, w->w2));
+    TRY(check_bias(w->b1));
+    TRY(check_bias(w->b2));
+    if (cfg->num_shared) TRY(check_weights_ffn(cfg, w->shared_w1, w->shared_w3, w->shared_w2));
+    TRY(need_ws(ws, ws_bytes, ec_ws(cfg)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const moe_config_t *c = cfg;
+    const size_t T = (size_t)c->num_tokens, E = (size_t)c->num_experts, d = (size_t)c->d_model;
+    const int64_t Cap = ec_capacity_of(c);
+    const size_t R = E * (size_t)Cap;
+    Carve cv{static_cast<uint8_t *>(ws)};
+    moe_ec_io_t o{};
+    if (io) o = *io;
+    float *logits_ws = cv.take<float>(T * E * 4);
+    int32_t *tok_row_ws = cv.take<int32_t>(T * E * 4);
+    float *gate_ws = cv.take<float>(T * E * 4);
+    int32_t *row_token_ws = cv.take<int32_t>(R * 4);
+    int32_t *off_ws = cv.take<int32_t>((E + 1) * 4);
+    void *x_perm = cv.take<uint8_t>(R * d * elem_bytes(c));
+    void *H = cv.take<uint8_t>(R * (size_t)c->d_ff * elem_bytes(c));
+    float *y_perm = cv.take<float>(R * d * 4);
+    void *ws_shared = c->num_shared ? cv.take<uint8_t>(shared_ws(c)) : nullptr;
+    float *z = c->num_shared ? cv.take<float>(T * d * 4) : nullptr;
+    if (!o.logits) o.logits = logits_ws;
+    if (!o.tok_row) o.tok_row = tok_row_ws;
+    if (!o.tok_gate) o.tok_gate = gate_ws;
+    if (!o.row_token) o.row_token = row_token_ws;
+    if (!o.offsets) o.offsets = off_ws;
+    void *const *ev = o.stage_events;
+    auto mark = [&](int i) {
+        if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+    };
+    mark(0);
+    TRY(router_logits_impl(c, x, w->w_router, w->b_router, o.logits, s));
+    TRY(ec_route_impl(c, o.logits, o.row_token, o.tok_row, o.tok_gate, o.offsets, s));
+    mark(1);
+    TRY(cuda_status(launch_gather_rows(x, c->num_tokens, o.row_token, (int64_t)R, c->d_model, c->dtype, x_perm, s),
+                    "expert-choice gather launch"));
+    mark(2);
+    TRY(ffn_impl(c, x_perm, (int64_t)R, o.offsets, c->num_experts, 0, w->w1, w->b1, w->w3, w->w2, w->b2, H, y_perm,
+                 s, ev ? ev[3] : nullptr));
+    mark(4);
+    if (c->num_shared)
+        TRY(ffn_impl(c, x, (int64_t)T, nullptr, 1, (int)T, w->shared_w1, nullptr, w->shared_w3, w->shared_w2,
+                     nullptr, ws_shared, z, s));
+    mark(5);
+    TRY(cuda_status(launch_combine(c->num_tokens, c->d_model, c->num_experts, c->dtype, y_perm, o.tok_row,
+                                   o.tok_gate, z, c->residual ? x : nullptr, out, s),
+                    "expert-choice combine launch"));
+    mark(6);
+    mark(7);
+    return MOE_OK;
 }
 
 moe_status_t moe_check_device_error(int32_t *code) {

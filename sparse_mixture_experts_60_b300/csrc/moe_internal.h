@@ -79,6 +79,20 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
 constexpr int64_t kPermStaticScratchInts = 131072;
 int32_t *permute_static_scratch();
 
+// ----------------------------------------------------------------- expert choice
+// Each expert takes the C tokens with the largest logit (ties: lower token
+// index); rows e*C .. e*C+C-1 hold its tokens in token order.
+//   row_token [E*C], tok_row [T,E] (row or -1), offsets [E+1] = e*C.
+cudaError_t launch_ec_select(const float *logits, int64_t T, int E, int64_t C, int32_t *row_token, int32_t *tok_row,
+                             int32_t *offsets, cudaStream_t s);
+// tok_gate [T,E] = softmax(logits[t])[e] where tok_row >= 0, else 0
+cudaError_t launch_ec_gates(const float *logits, const int32_t *tok_row, int64_t T, int E, float *tok_gate,
+                            cudaStream_t s);
+// x_perm[r] = x[row_token[r]] for r < rows (a token outside [0, T) raises the error flag)
+cudaError_t launch_gather_rows(const void *x, int64_t T, const int32_t *row_token, int64_t rows, int d, int dtype,
+                               void *x_perm, cudaStream_t s);
+cudaError_t launch_add_bias(float *logits, const float *b, int64_t T, int E, cudaStream_t s);
+
 // ----------------------------------------------------------------- experts
 // Grouped GEMM with fused epilogue on the tensor cores (bf16 in, fp32 acc).
 //   out[r, n] = epi( sum_k A[r, k] * B[g*b_rows + n, k] )   for rows r of group g

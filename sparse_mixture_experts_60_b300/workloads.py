@@ -111,7 +111,7 @@ WORKLOADS: Dict[str, Workload] = {
 # tensor ids for the seed sequence
 _TID = {"x": 1, "w_router": 2, "b_router": 3, "w1": 4, "b1": 5, "w3": 6, "w2": 7, "b2": 8,
         "sel_bias": 9, "shared_w1": 10, "shared_w3": 11, "shared_w2": 12, "logits": 13,
-        "zipf_rank": 14, "sample": 15}
+        "zipf_rank": 14, "sample": 15, "token_ids": 16}
 
 
 def bf16_round(a: np.ndarray) -> np.ndarray:
@@ -221,6 +221,16 @@ def make_logits(w: Workload, ties: bool = True) -> np.ndarray:
         sl = slice(0, w.T, 7)
         lg[sl] = np.round(lg[sl] * 4.0) / 4.0
     return np.ascontiguousarray(lg, dtype=np.float32)
+
+
+def make_token_ids(w: Workload, vocab: int = 32000) -> np.ndarray:
+    """Seeded vocabulary ids [T] int32 for hash routing: ranks drawn with
+    Zipf frequencies (p(r) proportional to 1/r over a 32000-entry vocabulary,
+    the Mixtral tokenizer's size), mapped to ids by a fixed permutation."""
+    g = _rng(w, "token_ids")
+    p = 1.0 / np.arange(1, vocab + 1, dtype=np.float64)
+    ranks = g.choice(vocab, size=w.T, p=p / p.sum())
+    return g.permutation(vocab).astype(np.int32)[ranks]
 
 
 def sample_tokens(w: Workload, n: int) -> np.ndarray:

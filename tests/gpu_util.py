@@ -6,6 +6,10 @@ Tolerances (floating point):
                a max relative error of 1e-4 with the output RMS as the floor
                for elements near zero;
   bf16 layers: max |gpu - ref| <= 2e-2 * rms(ref).
+  bf16 layers with heavy-tailed outputs (expert-choice routing, where a few
+  tokens are taken by many experts): |gpu - ref| <= 2e-2 * rms(ref) +
+  half_ulp_bf16(ref) per element, the second term being the rounding of the
+  stored bf16 output itself, which no implementation avoids.
 Integer outputs are compared for equality.
 """
 from __future__ import annotations
@@ -43,7 +47,14 @@ def as_f32(a: np.ndarray) -> np.ndarray:
     return wl.bf16_to_f32(a) if a.dtype == np.uint16 else np.asarray(a, np.float32)
 
 
-def float_check(gpu, ref, w, what="", report=None):
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 8)
+
+
+def float_check(gpu, ref, w, what="", report=None, out_rounding=False):
     """Assert the layer's float tolerance; returns (max_err, rms, ratio)."""
     g = np.asarray(gpu, np.float64)
     r = np.asarray(ref, np.float64)
@@ -56,6 +67,9 @@ def float_check(gpu, ref, w, what="", report=None):
         worst = float(np.max(err / np.maximum(bound, 1e-300))) if r.size else 0.0
         ok = bool(np.all(err <= bound))
         ratio = worst * FP32_REL
+    elif out_rounding:
+        ratio = float(err.max() / rms) if r.size else 0.0
+        ok = bool(np.all(err <= BF16_OF_RMS * rms + half_ulp_bf16(r)))
     else:
         ratio = float(err.max() / rms) if r.size else 0.0
         ok = ratio <= BF16_OF_RMS
