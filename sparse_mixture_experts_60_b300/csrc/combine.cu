@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, c
                                                       const float *__restrict__ topk_w,
                                                       const float *__restrict__ z, const void *__restrict__ x,
                                                       void *__restrict__ out) {
+    PDL_ENTER();
     constexpr int V = BF16 ? 8 : 4;
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int64_t T, int d, int
                                                            const float *__restrict__ topk_w,
                                                            const float *__restrict__ z, const void *__restrict__ x,
                                                            void *__restrict__ out) {
+    PDL_ENTER();
     extern __shared__ int wlist[];                       // [8 warps][k] rows, then [8][k] gates
     constexpr int V = BF16 ? 8 : 4;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -190,16 +192,10 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int64_t T, int d, int
 }
 
 template <typename T, typename Op>
-__device__ T block_reduce(T v, T *sm, Op op) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+__device__ __forceinline__ T warp_reduce(T v, Op op) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(kFull, v, o));
-    __syncthreads();
-    if (lane == 0) sm[warp] = v;
-    __syncthreads();
-    T r = sm[0];
-    for (int w = 1; w < nw; ++w) r = op(r, sm[w]);
-    return r;
+    return v;
 }
 
 struct AddF { __device__ float operator()(float a, float b) const { return a + b; } };
@@ -207,44 +203,93 @@ struct AddL { __device__ long long operator()(long long a, long long b) const { 
 struct MaxL { __device__ long long operator()(long long a, long long b) const { return a > b ? a : b; } };
 struct MinL { __device__ long long operator()(long long a, long long b) const { return a < b ? a : b; } };
 
-// Single CTA, fp32 throughout (Kahan-compensated per-thread sums, then
-// fixed-order tree reductions): deterministic and free of fp64.
-__global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
-    __shared__ float sf[32];
-    __shared__ long long sl[32];
+// Single CTA, fp32 throughout, deterministic and free of fp64: per-thread
+// strided sums (Kahan-compensated over lse), xor butterflies inside warps,
+// then one shared-memory round folded by thread 0 in warp order.  P and z
+// come from the router's per-block partials in the layer forward (a warp
+// per expert over the blocks), from prob_mean / lse in moe_stats.
+__global__ void __launch_bounds__(512) stats_kernel(StatsParams p) {
+    PDL_ENTER();
+    __shared__ float sP[kMaxExperts];
+    __shared__ float red_f[32][2];
+    __shared__ long long red_l[32][5];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t S = p.T * p.k;
-    float z = 0.0f, zc = 0.0f;
-    for (int64_t i = threadIdx.x; p.lse && i < p.T; i += blockDim.x) {
-        const float v = p.lse[i] * p.lse[i] - zc;
-        const float t = z + v;
-        zc = (t - z) - v;
-        z = t;
+    const bool parts = p.part_prob != nullptr;
+    const bool have_p = parts || p.prob_mean;
+    const bool have_z = (parts && p.part_z) || p.lse;
+    float z = 0.0f;
+    if (parts && p.part_z) {
+        for (int64_t b = threadIdx.x; b < p.nblk; b += blockDim.x) z += p.part_z[b];
+    } else if (p.lse) {
+        float zc = 0.0f;
+        for (int64_t i = threadIdx.x; i < p.T; i += blockDim.x) {
+            const float v = p.lse[i] * p.lse[i] - zc;
+            const float t = z + v;
+            zc = (t - z) - v;
+            z = t;
+        }
     }
-    z = block_reduce(z, sf, AddF());
+    if (parts) {
+        for (int e = warp; e < p.E; e += (int)(blockDim.x >> 5)) {
+            float acc = 0.0f;
+            for (int64_t b = lane; b < p.nblk; b += 32) acc += p.part_prob[(int64_t)e * p.nblk + b];
+            acc = warp_reduce(acc, AddF());
+            if (lane == 0) {
+                const float P = p.T > 0 ? acc / (float)p.T : 0.0f;
+                sP[e] = P;
+                if (p.prob_out) p.prob_out[e] = P;
+            }
+        }
+    } else if (p.prob_mean) {
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) sP[e] = p.prob_mean[e];
+    }
+    __syncthreads();
     float aux = 0.0f;
     long long dropped = 0, used = 0, kept_tot = 0, kmax = 0, kmin = 0x7fffffffffffffffLL;
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         const float f = S > 0 ? (float)p.counts[e] / (float)S : 0.0f;
         if (p.f) p.f[e] = f;
-        aux += f * (p.prob_mean ? p.prob_mean[e] : 0.0f);
+        if (have_p) aux += f * sP[e];
         dropped += p.counts[e] - p.kept[e];
         used += p.kept[e] > 0;
         kept_tot += p.kept[e];
         kmax = p.kept[e] > kmax ? p.kept[e] : kmax;
         kmin = p.kept[e] < kmin ? p.kept[e] : kmin;
     }
-    aux = block_reduce(aux, sf, AddF());
-    dropped = block_reduce(dropped, sl, AddL());
-    used = block_reduce(used, sl, AddL());
-    kept_tot = block_reduce(kept_tot, sl, AddL());
-    kmax = block_reduce(kmax, sl, MaxL());
-    kmin = block_reduce(kmin, sl, MinL());
+    z = warp_reduce(z, AddF());
+    aux = warp_reduce(aux, AddF());
+    dropped = warp_reduce(dropped, AddL());
+    used = warp_reduce(used, AddL());
+    kept_tot = warp_reduce(kept_tot, AddL());
+    kmax = warp_reduce(kmax, MaxL());
+    kmin = warp_reduce(kmin, MinL());
+    if (lane == 0) {
+        red_f[warp][0] = z;
+        red_f[warp][1] = aux;
+        red_l[warp][0] = dropped;
+        red_l[warp][1] = used;
+        red_l[warp][2] = kept_tot;
+        red_l[warp][3] = kmax;
+        red_l[warp][4] = kmin;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
+        const int nw = (blockDim.x + 31) >> 5;
+        for (int w = 1; w < nw; ++w) {
+            z += red_f[w][0];
+            aux += red_f[w][1];
+            dropped += red_l[w][0];
+            used += red_l[w][1];
+            kept_tot += red_l[w][2];
+            kmax = red_l[w][3] > kmax ? red_l[w][3] : kmax;
+            kmin = red_l[w][4] < kmin ? red_l[w][4] : kmin;
+        }
         moe_stats_t st;
         // without router probabilities (routing given by the caller) the
         // balance losses are undefined: NaN
-        st.aux_loss = p.prob_mean ? (float)p.E * aux : __int_as_float(0x7fc00000);
-        st.z_loss = !p.lse ? __int_as_float(0x7fc00000) : (p.T > 0 ? z / (float)p.T : 0.0f);
+        st.aux_loss = have_p ? (float)p.E * aux : __int_as_float(0x7fc00000);
+        st.z_loss = !have_z ? __int_as_float(0x7fc00000) : (p.T > 0 ? z / (float)p.T : 0.0f);
         st.imbalance = kmin > 0 ? (float)kmax / (float)kmin : INFINITY;
         st.utilization = (float)used / (float)p.E;
         st.drop_rate = S > 0 ? (float)dropped / (float)S : 0.0f;
@@ -256,6 +301,7 @@ __global__ void __launch_bounds__(1024) stats_kernel(StatsParams p) {
 }
 
 __global__ void bias_update_kernel(int64_t S, int E, const int32_t *counts, float *b, float gamma) {
+    PDL_ENTER();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     const long long diff = (long long)S - (long long)E * counts[e];  // sign of S/E - counts_e
@@ -277,23 +323,21 @@ cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_pe
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
         }
-        kern<<<grid, 256, smem, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
-        return cudaGetLastError();
+        return launch_pdl(kern, dim3(grid), dim3(256), smem, s, T, d, k, y_perm, inv, topk_w, shared_out, x_res,
+                          out);
     }
-    if (dtype == 1) combine_kernel<true><<<grid, 256, 0, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
-    else combine_kernel<false><<<grid, 256, 0, s>>>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
-    return cudaGetLastError();
+    auto kern = dtype == 1 ? combine_kernel<true> : combine_kernel<false>;
+    return launch_pdl(kern, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
 }
 
 cudaError_t launch_stats(const StatsParams &p, cudaStream_t s) {
-    stats_kernel<<<1, 1024, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(stats_kernel, dim3(1), dim3(512), 0, s, p);
 }
 
 cudaError_t launch_bias_update(int64_t T, int E, int k, const int32_t *counts, float *bias, float gamma,
                                cudaStream_t s) {
-    bias_update_kernel<<<(unsigned)ceil_div(E, 256), 256, 0, s>>>(T * k, E, counts, bias, gamma);
-    return cudaGetLastError();
+    return launch_pdl(bias_update_kernel, dim3((unsigned)ceil_div(E, 256)), dim3(256), 0, s, T * k, E, counts, bias,
+                      gamma);
 }
 
 }  // namespace moe

@@ -64,6 +64,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *total, int *warp
 __global__ void __launch_bounds__(kThreadsEC) ec_select_kernel(const float *__restrict__ logits, int64_t T, int E,
                                                               int64_t C, int cache, int32_t *row_token,
                                                               int32_t *tok_row, int32_t *offsets) {
+    PDL_ENTER();
     extern __shared__ uint32_t skey[];
     __shared__ unsigned int hist[256];
     __shared__ uint32_t s_prefix;
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kThreadsEC) ec_select_kernel(const float *__re
 __global__ void __launch_bounds__(256) ec_gate_kernel(const float *__restrict__ logits,
                                                       const int32_t *__restrict__ tok_row, int64_t T, int E,
                                                       float *__restrict__ tok_gate) {
+    PDL_ENTER();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -158,6 +160,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
                                                           const int32_t *__restrict__ row_token, int64_t rows,
                                                           int64_t T, int nvec, uint4 *__restrict__ x_perm,
                                                           int32_t *err) {
+    PDL_ENTER();
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= rows) return;
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
 }
 
 __global__ void add_bias_kernel(float *logits, const float *b, int64_t T, int E) {
+    PDL_ENTER();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < T * E) logits[i] += b[i % E];
 }
@@ -196,31 +200,28 @@ cudaError_t launch_ec_select(const float *logits, int64_t T, int E, int64_t C, i
                                                (int)(kEcSmemKeys * sizeof(uint32_t)));
         if (err != cudaSuccess) return err;
     }
-    ec_select_kernel<<<(unsigned)E, kThreadsEC, smem, s>>>(logits, T, E, C, cache, row_token, tok_row, offsets);
-    return cudaGetLastError();
+    return launch_pdl(ec_select_kernel, dim3((unsigned)E), dim3(kThreadsEC), smem, s, logits, T, E, C, cache,
+                      row_token, tok_row, offsets);
 }
 
 cudaError_t launch_ec_gates(const float *logits, const int32_t *tok_row, int64_t T, int E, float *tok_gate,
                             cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    ec_gate_kernel<<<(unsigned)ceil_div(T, 8), 256, 0, s>>>(logits, tok_row, T, E, tok_gate);
-    return cudaGetLastError();
+    return launch_pdl(ec_gate_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, logits, tok_row, T, E, tok_gate);
 }
 
 cudaError_t launch_gather_rows(const void *x, int64_t T, const int32_t *row_token, int64_t rows, int d, int dtype,
                                void *x_perm, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
     const int nvec = d * (dtype == 0 ? 4 : 2) / 16;
-    gather_rows_kernel<<<(unsigned)ceil_div(rows, 8), 256, 0, s>>>(static_cast<const uint4 *>(x), row_token, rows, T,
-                                                                   nvec, static_cast<uint4 *>(x_perm),
-                                                                   device_error_flag());
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3((unsigned)ceil_div(rows, 8)), dim3(256), 0, s,
+                      static_cast<const uint4 *>(x), row_token, rows, T, nvec, static_cast<uint4 *>(x_perm),
+                      device_error_flag());
 }
 
 cudaError_t launch_add_bias(float *logits, const float *b, int64_t T, int E, cudaStream_t s) {
     if (T == 0 || !b) return cudaSuccess;
-    add_bias_kernel<<<(unsigned)ceil_div(T * E, 256), 256, 0, s>>>(logits, b, T, E);
-    return cudaGetLastError();
+    return launch_pdl(add_bias_kernel, dim3((unsigned)ceil_div(T * E, 256)), dim3(256), 0, s, logits, b, T, E);
 }
 
 }  // namespace moe

@@ -19,6 +19,7 @@ constexpr int TM = 64, TN = 64, TK = 16;
 
 template <bool GATED>
 __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtProblem p) {
+    PDL_ENTER();
     __shared__ float As[TK][TM + 4];
     __shared__ float Bs[TK][TN + 4];
     __shared__ float B2s[GATED ? TK : 1][TN + 4];
@@ -90,9 +91,8 @@ cudaError_t launch_ffn_simt(const SimtProblem &p, cudaStream_t s) {
     const int64_t max_rows = p.seg ? p.max_rows : p.M;
     if (max_rows <= 0 || G <= 0) return cudaSuccess;
     dim3 grid((unsigned)ceil_div(p.N, TN), (unsigned)ceil_div(max_rows, TM), (unsigned)G);
-    if (p.gated) ffn_simt_kernel<true><<<grid, 256, 0, s>>>(p);
-    else ffn_simt_kernel<false><<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    if (p.gated) return launch_pdl(ffn_simt_kernel<true>, grid, dim3(256), 0, s, p);
+    return launch_pdl(ffn_simt_kernel<false>, grid, dim3(256), 0, s, p);
 }
 
 }  // namespace moe

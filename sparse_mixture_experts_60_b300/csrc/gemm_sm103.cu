@@ -42,6 +42,7 @@
 #include <stdlib.h>
 
 #include "moe_internal.h"
+#include "route_device.cuh"
 
 namespace moe {
 
@@ -58,6 +59,11 @@ int32_t *device_error_flag() {
         ptr[dev] = static_cast<int32_t *>(p);
     }
     return ptr[dev];
+}
+
+bool pdl_enabled() {
+    const char *e = getenv("MOE_B300_PDL");
+    return !(e && e[0] == '0');
 }
 
 int num_sms() {
@@ -247,6 +253,7 @@ struct Args {
     int64_t bias_stride;
     int act;
     int32_t *err;
+    RouteEpilogue route;   // router GEMM with the routing epilogue
 };
 
 struct Tile {
@@ -362,7 +369,59 @@ __device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, 
     }
 }
 
-template <int BN, bool GATED, bool OUT_F32>
+// Routing epilogue of the router GEMM (N = E <= EP <= 32, one 32-column
+// chunk): thread = token.  The logits (+ router bias) are written, the
+// token is routed in registers (route_row), and each warp, whose 32 rows are
+// one 32-token block, writes that block's partials: the per-expert sums of
+// the softmax probabilities and the expert counts (xor butterflies and
+// ballots; lane e keeps expert e) and the sum of lse^2.
+template <int EP>
+__device__ __forceinline__ void route_epilogue(const Args &args, const Tile &tl, int row_base, uint32_t tbase,
+                                               int lane) {
+    const RouteEpilogue &re = args.route;
+    const int E = args.N;
+    float v[32];
+    tmem_ld32(tbase, v);
+    const int64_t t = row_base + lane;
+    const bool valid = t < tl.seg_end;
+    float l[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) l[e] = (e < E && re.b_router) ? v[e] + __ldg(re.b_router + e) : v[e];
+    if (valid) {
+        float *dst = static_cast<float *>(args.out) + t * args.ldo;
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+            if (e < E) dst[e] = l[e];
+    }
+    float lse;
+    const uint32_t chosen = route_row<EP>(l, E, re.k, re.score_fn, re.renormalize, re.sel_bias, valid, t,
+                                          re.topk_idx, re.topk_w, re.lse, &lse);
+    if (row_base >= tl.seg_end) return;                  // warp-uniform: no token of this block exists
+    const int64_t blk = row_base / 32;
+    float ps = 0.0f;
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+        float x = (valid && e < E) ? expf(l[e] - lse) : 0.0f;   // softmax probability
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        const int c = __popc(__ballot_sync(0xffffffffu, (chosen >> e) & 1u));
+        if (lane == e) {
+            ps = x;
+            cnt = c;
+        }
+    }
+    float z = valid ? lse * lse : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < E) {
+        re.part_prob[(int64_t)lane * re.nblk + blk] = ps;
+        re.part_cnt[(int64_t)lane * re.nblk + blk] = cnt;
+    }
+    if (lane == 0 && re.part_z) re.part_z[blk] = z;
+}
+
+template <int BN, bool GATED, bool OUT_F32, int ROUTE_EP = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const Args args) {
@@ -409,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATED) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+    PDL_ENTER();   // the segment offsets and A are the previous kernel's output
     for (int i = threadIdx.x; i <= G; i += kThreads)
         seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
@@ -535,7 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int row_base = tl.row0 + q * 32;          // first row of this warp's 32
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN, GATED, OUT_F32>(args, tl, row_base, tbase, half, lane, stg);
+            if constexpr (ROUTE_EP > 0) {
+                if (half == 0) route_epilogue<ROUTE_EP>(args, tl, row_base, tbase, lane);
+            } else {
+                epilogue_tile<BN, GATED, OUT_F32>(args, tl, row_base, tbase, half, lane, stg);
+            }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -725,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATED) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+    PDL_ENTER();   // the segment offsets and A are the previous kernel's output
     for (int i = threadIdx.x; i <= G; i += kThreads)
         seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
@@ -896,7 +961,7 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool GATED, bool OUT_F32>
+template <int BN, bool GATED, bool OUT_F32, int ROUTE_EP = 0>
 cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     using C = Cfg<BN>;
     constexpr int BN_B = GATED ? BN / 2 : BN;   // rows per TMA box of B
@@ -923,12 +988,12 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     a.act = p.act;
     a.err = device_error_flag();
     if (!a.err) return cudaErrorUnknown;
+    a.route = p.route ? *p.route : RouteEpilogue{};
     const size_t smem = C::smem_bytes(a.G);
-    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32>;
+    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, ROUTE_EP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<num_sms(), kThreads, smem, s>>>(ta, tb, tb2, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, s, ta, tb, tb2, a);
 }
 
 template <int BN, bool GATED, bool OUT_F32>
@@ -967,13 +1032,15 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1006,6 +1073,12 @@ bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias) 
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
     if (!grouped_gemm_supported(p.N, p.K, p.gated, p.out_f32, p.bias != nullptr)) return cudaErrorInvalidValue;
+    if (p.route) {
+        if (p.N > 32 || p.gated || !p.out_f32 || p.seg || p.bias) return cudaErrorInvalidValue;
+        if (p.N <= 8) return launch_t<32, false, true, 8>(p, s);
+        if (p.N <= 16) return launch_t<32, false, true, 16>(p, s);
+        return launch_t<32, false, true, 32>(p, s);
+    }
     if (p.gated) {
         if (use_pair(p)) return p.out_f32 ? launch_pair_t<256, true, true>(p, s) : launch_pair_t<256, true, false>(p, s);
         return p.out_f32 ? launch_t<256, true, true>(p, s) : launch_t<256, true, false>(p, s);

@@ -75,7 +75,7 @@ int64_t route_blocks(const moe_config_t *c) { return ceil_div(c->num_tokens, kRo
 int64_t perm_chunks(const moe_config_t *c) { return ceil_div(c->num_tokens * c->top_k, kPermChunk); }
 
 size_t route_ws(const moe_config_t *c) {
-    return 2 * align256((size_t)route_blocks(c) * c->num_experts * 4);
+    return 2 * align256((size_t)route_blocks(c) * c->num_experts * 4) + align256((size_t)route_blocks(c) * 4);
 }
 size_t permute_ws(const moe_config_t *c) { return 2 * align256((size_t)perm_chunks(c) * c->num_experts * 4); }
 size_t ffn_ws(const moe_config_t *c) {
@@ -169,14 +169,33 @@ moe_status_t ec_route_impl(const moe_config_t *c, const float *logits, int32_t *
     return cuda_status(e, "expert-choice routing launch");
 }
 
+// Per-32-token routing partials in the route workspace.
+struct RoutePartials {
+    float *prob;       // [E, nblk]
+    int32_t *cnt;      // [E, nblk]
+    float *z;          // [nblk]
+    int64_t nblk;
+};
+RoutePartials route_partials(const moe_config_t *c, void *ws) {
+    Carve cv{static_cast<uint8_t *>(ws)};
+    RoutePartials r;
+    r.nblk = route_blocks(c);
+    r.prob = cv.take<float>((size_t)r.nblk * c->num_experts * 4);
+    r.cnt = cv.take<int32_t>((size_t)r.nblk * c->num_experts * 4);
+    r.z = cv.take<float>((size_t)r.nblk * 4);
+    return r;
+}
+
+// reduce = false (the layer forward): prob_mean / counts are not reduced
+// here; the statistics kernel reads the partials.
 moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_router, const float *b_router,
                         const float *sel_bias, float *logits, const float *logits_in, int32_t *topk_idx,
                         float *topk_w, float *lse, float *prob_mean, int32_t *counts, void *ws,
-                        cudaStream_t s) {
-    Carve cv{static_cast<uint8_t *>(ws)};
-    const int64_t nblk = route_blocks(c);
-    float *part_prob = cv.take<float>((size_t)nblk * c->num_experts * 4);
-    int32_t *part_cnt = cv.take<int32_t>((size_t)nblk * c->num_experts * 4);
+                        cudaStream_t s, bool reduce = true) {
+    const RoutePartials rp = route_partials(c, ws);
+    const int64_t nblk = rp.nblk;
+    float *part_prob = rp.prob;
+    int32_t *part_cnt = rp.cnt;
     RouteParams p{};
     p.T = c->num_tokens;
     p.E = c->num_experts;
@@ -193,14 +212,50 @@ moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_rout
     p.lse = lse;
     p.part_prob = part_prob;
     p.part_cnt = part_cnt;
+    p.part_z = rp.z;
     cudaError_t e = cudaSuccess;
-    if (logits_in) {
+    const bool fused_gemm = !logits_in && c->dtype == MOE_DTYPE_BF16 && c->num_experts <= 32 &&
+                            grouped_gemm_supported(c->num_experts, c->d_model, 0, 1, 0);
+    if (fused_gemm) {
+        // bf16, E <= 32: logits on the tensor cores with the routing in the
+        // GEMM's epilogue (one launch)
+        if (c->num_tokens > 0) {
+            RouteEpilogue re{};
+            re.b_router = b_router;
+            re.sel_bias = sel_bias;
+            re.k = c->top_k;
+            re.score_fn = c->score_fn;
+            re.renormalize = c->renormalize;
+            re.topk_idx = topk_idx;
+            re.topk_w = topk_w;
+            re.lse = lse;
+            re.part_prob = part_prob;
+            re.part_cnt = part_cnt;
+            re.part_z = rp.z;
+            re.nblk = nblk;
+            GemmProblem g{};
+            g.A = static_cast<const bf16 *>(x);
+            g.a_rows = c->num_tokens;
+            g.B = static_cast<const bf16 *>(w_router);
+            g.b_rows_total = c->num_experts;
+            g.b_group_rows = c->num_experts;
+            g.G = 1;
+            g.M = (int)c->num_tokens;
+            g.N = c->num_experts;
+            g.K = c->d_model;
+            g.out = logits;
+            g.ldo = c->num_experts;
+            g.out_f32 = 1;
+            g.route = &re;
+            e = launch_grouped_gemm(g, s);
+        }
+    } else if (logits_in) {
         p.logits = const_cast<float *>(logits_in);
         p.logits_add_bias = 0;
         e = launch_route_logits(p, s);
     } else if (c->dtype == MOE_DTYPE_F32 && c->num_experts <= 32) {
         p.logits = logits;
-        e = launch_router_fused(p, c->dtype, s);
+        e = launch_router_fused(p, s);
     } else {
         // bf16: logits on the tensor cores (x streamed once by TMA), then the
         // routing kernel adds the router bias and selects
@@ -229,7 +284,7 @@ moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_rout
         }
         if (e == cudaSuccess) e = launch_route_logits(p, s);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && reduce)
         e = launch_route_reduce(part_prob, part_cnt, nblk, c->num_experts, c->num_tokens, prob_mean, counts, s);
     return cuda_status(e, "moe_route launch");
 }
@@ -660,7 +715,8 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
         o.topk_w = const_cast<float *>(given_w);
     } else {
         TRY(route_impl(c, x, w->w_router, w->b_router, c->score_fn == MOE_SCORE_SIGMOID ? sel_bias : nullptr,
-                       o.logits, nullptr, o.topk_idx, o.topk_w, o.lse, o.prob_mean, o.counts, ws_route, s));
+                       o.logits, nullptr, o.topk_idx, o.topk_w, o.lse, o.prob_mean, o.counts, ws_route, s,
+                       /*reduce=*/false));
     }
     mark(1);
     TRY(permute_impl(c, x, o.topk_idx, o.counts, o.kept, o.offsets, o.perm, o.inv, x_perm, ws_perm, s));
@@ -684,8 +740,14 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
     sp.drop = c->drop_tokens;
     sp.counts = o.counts;
     sp.kept = o.kept;
-    sp.prob_mean = given_idx ? nullptr : o.prob_mean;
-    sp.lse = given_idx ? nullptr : o.lse;
+    if (!given_idx) {
+        // P and z from the router's per-block partials (prob_mean written here)
+        const RoutePartials rp = route_partials(c, ws_route);
+        sp.part_prob = rp.prob;
+        sp.part_z = rp.z;
+        sp.nblk = rp.nblk;
+        sp.prob_out = o.prob_mean;
+    }
     sp.f = o.f;
     sp.stats = o.stats;
     TRY(cuda_status(launch_stats(sp, s), "stats launch"));

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
 
 using bf16 = __nv_bfloat16;
@@ -22,6 +24,40 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int32_t *device_error_flag();
 
 int num_sms();
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with launch_pdl and starts with PDL_ENTER() (pdl_wait before its first
+// global-memory access, then pdl_trigger): the next kernel on the stream is
+// launched as soon as every CTA of this one has started, so its launch and
+// prologue overlap this kernel's tail, and griddepcontrol.wait still holds it
+// until this grid has completed and its writes are visible.  Without the
+// launch attribute (MOE_B300_PDL=0, or launches from other code) both
+// instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#define PDL_ENTER()       \
+    do {                  \
+        ::moe::pdl_wait();    \
+        ::moe::pdl_trigger(); \
+    } while (0)
+
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------- router
 struct RouteParams {
@@ -40,9 +76,10 @@ struct RouteParams {
     float *lse;
     float *part_prob;      // [E, nblk] per-CTA sums of softmax probabilities
     int32_t *part_cnt;     // [E, nblk] per-CTA expert counts
+    float *part_z;         // [nblk] per-CTA sums of lse^2, or null
 };
-// E <= 32: one kernel computes logits from x and routes (dtype 0 f32, 1 bf16)
-cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s);
+// fp32 layers, E <= 32: one kernel computes logits from x on the CUDA cores and routes
+cudaError_t launch_router_fused(const RouteParams &p, cudaStream_t s);
 // logits given in p.logits (optionally + bias, written back): route only
 cudaError_t launch_route_logits(const RouteParams &p, cudaStream_t s);
 // logits = x w_r^T on CUDA cores (fp32, or shapes the tensor-core path does not take)
@@ -98,6 +135,20 @@ cudaError_t launch_add_bias(float *logits, const float *b, int64_t T, int E, cud
 //   out[r, n] = epi( sum_k A[r, k] * B[g*b_rows + n, k] )   for rows r of group g
 // gated: B2 is the second weight; epi = silu(acc1) * acc2.
 // act: 0 none, 1 GELU, 2 ReLU.  out is bf16 (out_f32 = 0) or fp32.
+// Routing epilogue of the router GEMM (E <= 32, one thread per token):
+// bias, logits written, top-k, gates, lse and the per-32-token partials.
+struct RouteEpilogue {
+    const float *b_router;
+    const float *sel_bias;
+    int k, score_fn, renormalize;
+    int32_t *topk_idx;
+    float *topk_w, *lse;
+    float *part_prob;      // [E, nblk]
+    int32_t *part_cnt;     // [E, nblk]
+    float *part_z;         // [nblk]
+    int64_t nblk;          // ceil(T / kRouteTokPerCta)
+};
+
 struct GemmProblem {
     const bf16 *A; int64_t a_rows;           // A [a_rows, K]
     const bf16 *B; const bf16 *B2; int64_t b_rows_total; int b_group_rows;
@@ -107,6 +158,7 @@ struct GemmProblem {
     void *out; int64_t ldo; int out_f32;
     const bf16 *bias; int64_t bias_stride;   // per group, or null
     int act; int gated;
+    const RouteEpilogue *route;              // router GEMM with the routing epilogue, or null
 };
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
 bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias);
@@ -127,6 +179,10 @@ cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_pe
 struct StatsParams {
     int64_t T; int E, k; int64_t cap; int drop;
     const int32_t *counts, *kept; const float *prob_mean, *lse;
+    // router partials instead of prob_mean / lse (the layer forward):
+    // P_e = sum_blk part_prob[e, blk] / T (written to prob_out when not
+    // null), z = sum_blk part_z[blk] / T
+    const float *part_prob, *part_z; int64_t nblk; float *prob_out;
     float *f; void *stats;
 };
 cudaError_t launch_stats(const StatsParams &p, cudaStream_t s);

@@ -49,6 +49,7 @@ __device__ __forceinline__ int slot_expert(const int32_t *idx, int64_t p, int64_
 
 __global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *idx, int64_t T, int k,
                                                                  int E, int32_t *hist, int32_t *err) {
+    PDL_ENTER();
     extern __shared__ int h[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
     __syncthreads();
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const int32_t *hist, in
                                                          int64_t nchunk, int E, int64_t cap,
                                                          int32_t *counts, int32_t *kept,
                                                          int32_t *offsets) {
+    PDL_ENTER();
     __shared__ int warp_tot[32];
     const int e = threadIdx.x;
     int kp = 0;
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *
                                                                  const int32_t *offsets,
                                                                  int32_t *perm, int32_t *inv,
                                                                  int32_t *err) {
+    PDL_ENTER();
     extern __shared__ int wh[];  // [8][E] warp histograms, then warp running bases
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nw = kPermThreads / 32;
@@ -177,6 +180,7 @@ __global__ void __launch_bounds__(kSmallThreads) perm_small_kernel(const int32_t
                                                                    int64_t cap, int32_t *counts, int32_t *kept,
                                                                    int32_t *offsets, int32_t *perm, int32_t *inv,
                                                                    int32_t *err) {
+    PDL_ENTER();
     extern __shared__ int wh[];            // [kSmallWarps][E] histograms, then warp bases; then slot experts
     __shared__ int warp_tot[32];
     short *es = reinterpret_cast<short *>(wh + kSmallWarps * E);   // [S] expert of slot s (-2: invalid)
@@ -282,6 +286,7 @@ __global__ void __launch_bounds__(kSmallThreads) perm_small_kernel(const int32_t
 __global__ void __launch_bounds__(256) perm_copy_kernel(const uint4 *x, int64_t T, int k, int64_t nvec,
                                                         const int32_t *inv, const int32_t *offsets,
                                                         int E, int32_t *perm, int64_t S, uint4 *x_perm) {
+    PDL_ENTER();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     // unused tail of perm -> -1
@@ -351,46 +356,38 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
     if (!err) return cudaErrorUnknown;
     const int eb = p.dtype == 0 ? 4 : 2;
     const int64_t nvec = (int64_t)p.d * eb / 16;
+    const dim3 copy_grid((unsigned)ceil_div(p.T, 8));
+    cudaError_t e;
     if (!p.chunked && S > 0 && S <= kSmallSlots && p.E <= kSmallExperts) {
         const size_t smem = (size_t)kSmallWarps * p.E * sizeof(int) + (size_t)S * sizeof(short);
         if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
+            e = cudaFuncSetAttribute(perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
         }
-        perm_small_kernel<<<1, kSmallThreads, smem, s>>>(p.topk_idx, (int)p.T, p.k, p.E, p.cap, p.counts, p.kept,
-                                                          p.offsets, p.perm, p.inv, err);
-        cudaError_t e = cudaGetLastError();
+        e = launch_pdl(perm_small_kernel, dim3(1), dim3(kSmallThreads), smem, s, p.topk_idx, (int)p.T, p.k, p.E,
+                       p.cap, p.counts, p.kept, p.offsets, p.perm, p.inv, err);
         if (e != cudaSuccess) return e;
-        perm_copy_kernel<<<(unsigned)ceil_div(p.T, 8), 256, 0, s>>>(static_cast<const uint4 *>(p.x), p.T, p.k, nvec,
-                                                                   p.inv, p.offsets, p.E, p.perm, S,
-                                                                   static_cast<uint4 *>(p.x_perm));
-        return cudaGetLastError();
+        return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k,
+                          nvec, p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
     }
     if (nchunk > 0) {
-        perm_hist_kernel<<<(unsigned)nchunk, kPermThreads, p.E * sizeof(int), s>>>(p.topk_idx, p.T, p.k,
-                                                                                 p.E, p.hist, err);
-        cudaError_t e = cudaGetLastError();
+        e = launch_pdl(perm_hist_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), p.E * sizeof(int), s,
+                       p.topk_idx, p.T, p.k, p.E, p.hist, err);
         if (e != cudaSuccess) return e;
     }
-    perm_scan_kernel<<<1, 1024, 0, s>>>(p.hist, p.base, nchunk, p.E, p.cap, p.counts, p.kept,
-                                        p.offsets);
-    cudaError_t e = cudaGetLastError();
+    e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, p.hist, p.base, nchunk, p.E, p.cap, p.counts,
+                   p.kept, p.offsets);
     if (e != cudaSuccess || nchunk == 0) return e;
     const size_t rank_smem = (size_t)(kPermThreads / 32) * p.E * sizeof(int);
     if (rank_smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)rank_smem);
+        e = cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rank_smem);
         if (e != cudaSuccess) return e;
     }
-    perm_rank_kernel<<<(unsigned)nchunk, kPermThreads, rank_smem, s>>>(
-        p.topk_idx, p.T, p.k, p.E, p.cap, p.base, p.offsets, p.perm, p.inv, err);
-    e = cudaGetLastError();
+    e = launch_pdl(perm_rank_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), rank_smem, s, p.topk_idx, p.T,
+                   p.k, p.E, p.cap, p.base, p.offsets, p.perm, p.inv, err);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)ceil_div(p.T, 8);
-    perm_copy_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(p.x), p.T, p.k, nvec, p.inv,
-                                             p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
-    return cudaGetLastError();
+    return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k, nvec,
+                      p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
 }
 
 }  // namespace moe

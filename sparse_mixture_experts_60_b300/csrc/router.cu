@@ -17,44 +17,12 @@
 #include <stdint.h>
 
 #include "moe_internal.h"
+#include "route_device.cuh"
 
 namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-
-// ---------------------------------------------------------------- fp32 key
-// The sigmoid selection key must be reproducible bit for bit, so it is a
-// fixed sequence of correctly rounded fp32 operations (explicit _rn
-// intrinsics: no contraction, no reassociation):
-//   exp: Cody-Waite reduction n = rint(a log2e), r = a - n ln2 with ln 2
-//        split into a 16-bit head (exact products) and an fp32 tail, then
-//        the degree-7 Taylor polynomial of e^r in Horner form, then one
-//        multiply by the exact power of two 2^n;  a > 88 -> +inf,
-//        a < -87 -> 0.
-//   sigmoid(x) = 1 / (1 + exp(-x));  key = sigmoid(logit) + b_i.
-__device__ __forceinline__ float exp_key(float a) {
-    if (a != a) return a;
-    if (a > 88.0f) return __int_as_float(0x7f800000);
-    if (a < -87.0f) return 0.0f;
-    const float n = rintf(__fmul_rn(a, 0x1.715476p+0f));
-    float r = __fmaf_rn(-n, 0x1.62e4p-1f, a);
-    r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
-    float q = 0x1.a01a02p-13f;           // 1/7!
-    q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);  // 1/6!
-    q = __fmaf_rn(q, r, 0x1.111112p-7f);   // 1/5!
-    q = __fmaf_rn(q, r, 0x1.555556p-5f);   // 1/4!
-    q = __fmaf_rn(q, r, 0x1.555556p-3f);   // 1/3!
-    q = __fmaf_rn(q, r, 0x1p-1f);          // 1/2!
-    q = __fmaf_rn(q, r, 1.0f);
-    q = __fmaf_rn(q, r, 1.0f);
-    const int ni = (int)n;                 // -126 .. 127
-    return __fmul_rn(q, __int_as_float((ni + 127) << 23));
-}
-
-__device__ __forceinline__ float sigmoid_key(float x) {
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_key(-x)));
-}
 
 template <int G>
 __device__ __forceinline__ float group_max(float v) {
@@ -69,15 +37,10 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
-// (key descending, expert ascending)
-__device__ __forceinline__ bool ranks_before(float ka, int ea, float kb, int eb) {
-    return ka > kb || (ka == kb && ea < eb);
-}
-
 // Route one token held by a group of G lanes (VPL logits per lane).
 template <int G, int VPL>
 __device__ __forceinline__ void route_group(const RouteParams &p, const float (&l)[VPL], int r,
-                                            bool tok_ok, int64_t t, float (&psum)[VPL],
+                                            bool tok_ok, int64_t t, float (&psum)[VPL], float &zsum,
                                             int *s_cnt) {
     const int E = p.E, k = p.k;
     float key[VPL];
@@ -108,6 +71,7 @@ __device__ __forceinline__ void route_group(const RouteParams &p, const float (&
 #pragma unroll
         for (int i = 0; i < VPL; ++i)
             if (r + G * i < E) psum[i] += expf(l[i] - lse);
+        if (r == 0) zsum += lse * lse;
     }
     // top-k: k rounds of a group arg-max over the keys not yet taken
     unsigned taken = 0u;
@@ -162,10 +126,14 @@ __device__ __forceinline__ void route_group(const RouteParams &p, const float (&
 // Per-CTA partials: psum is summed over the groups of a warp (xor
 // butterfly), then over the 8 warps in warp order.
 template <int G, int VPL>
-__device__ __forceinline__ void write_partials(const RouteParams &p, float (&psum)[VPL], int r,
+__device__ __forceinline__ void write_partials(const RouteParams &p, float (&psum)[VPL], float zsum, int r,
                                                int grp, float *s_prob, const int *s_cnt) {
+    __shared__ float s_z[8];
     const int warp = threadIdx.x >> 5;
     const int EP = G * VPL;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zsum += __shfl_xor_sync(kFull, zsum, o);
+    if ((threadIdx.x & 31) == 0) s_z[warp] = zsum;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
 #pragma unroll
@@ -178,6 +146,11 @@ __device__ __forceinline__ void write_partials(const RouteParams &p, float (&psu
         for (int w = 0; w < 8; ++w) acc += s_prob[w * EP + e];
         p.part_prob[(int64_t)e * gridDim.x + blockIdx.x] = acc;   // [E][blocks]
         p.part_cnt[(int64_t)e * gridDim.x + blockIdx.x] = s_cnt[e];
+    }
+    if (threadIdx.x == 0 && p.part_z) {
+        float z = 0.0f;
+        for (int w = 0; w < 8; ++w) z += s_z[w];
+        p.part_z[blockIdx.x] = z;
     }
 }
 
@@ -202,39 +175,12 @@ struct Vec<float> {
         f[3] = __uint_as_float(u.w);
     }
 };
-template <>
-struct Vec<bf16> {
-    static constexpr int N = 8;
-    __device__ static void unpack(const uint4 &u, float *f) {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-};
-
-// After the loop, lane l holds the warp-wide sum of v[l] (a reduce-scatter
-// by recursive halving: 31 shuffles for 32 values).
-__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = upper ? v[i] : v[i + s];
-            const float keep = upper ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(kFull, send, s);
-        }
-    }
-    return v[0];
-}
 
 // E <= EP <= 32: logits from x on the CUDA cores (the router is read from
 // L1, x streamed once with 16-byte loads), then routing in registers.
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(256, EP <= 16 ? 2 : 1) router_fused_kernel(RouteParams p) {
+    PDL_ENTER();
     constexpr int TPW = 32 / EP;            // tokens per warp per round
     constexpr int VN = Vec<Tin>::N;
     __shared__ float s_prob[8 * EP];
@@ -247,6 +193,7 @@ __global__ void __launch_bounds__(256, EP <= 16 ? 2 : 1) router_fused_kernel(Rou
     if (threadIdx.x < EP) s_cnt[threadIdx.x] = 0;
     __syncthreads();
     float psum[1] = {0.0f};
+    float zsum = 0.0f;
     const int nvec = d / VN;
     const int64_t cta_t0 = (int64_t)blockIdx.x * kRouteTokPerCta;
 #pragma unroll 1
@@ -299,16 +246,17 @@ __global__ void __launch_bounds__(256, EP <= 16 ? 2 : 1) router_fused_kernel(Rou
             if (tok_ok) p.logits[t * E + r] = logit;
         }
         const float l1[1] = {logit};
-        route_group<EP, 1>(p, l1, r, tok_ok, t, psum, s_cnt);
+        route_group<EP, 1>(p, l1, r, tok_ok, t, psum, zsum, s_cnt);
     }
     __syncthreads();
-    write_partials<EP, 1>(p, psum, r, grp, s_prob, s_cnt);
+    write_partials<EP, 1>(p, psum, zsum, r, grp, s_prob, s_cnt);
 }
 
 // Routing from logits in memory (optionally adding the router bias and
 // writing the biased logits back).
 template <int G, int VPL>
 __global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
+    PDL_ENTER();
     constexpr int TPR = 32 / G;             // tokens per warp per round
     extern __shared__ float dyn[];
     float *s_prob = dyn;                                  // [8][G*VPL]
@@ -321,6 +269,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
     float psum[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) psum[i] = 0.0f;
+    float zsum = 0.0f;
     const int64_t cta_t0 = (int64_t)blockIdx.x * kRouteTokPerCta;
 #pragma unroll 1
     for (int round = 0; round < 4 / TPR; ++round) {
@@ -340,10 +289,10 @@ __global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
             }
             l[i] = v;
         }
-        route_group<G, VPL>(p, l, r, tok_ok, t, psum, s_cnt);
+        route_group<G, VPL>(p, l, r, tok_ok, t, psum, zsum, s_cnt);
     }
     __syncthreads();
-    write_partials<G, VPL>(p, psum, r, grp, s_prob, s_cnt);
+    write_partials<G, VPL>(p, psum, zsum, r, grp, s_prob, s_cnt);
 }
 
 // logits = x W^T on CUDA cores, 32x32 output tiles (no bias).
@@ -351,6 +300,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(256) router_logits_simt_kernel(const Tin *x, const Tin *W,
                                                                  float *logits, int64_t T, int E,
                                                                  int d) {
+    PDL_ENTER();
     __shared__ float xs[32][33], ws[32][33];
     const int64_t t0 = (int64_t)blockIdx.x * 32;
     const int e0 = blockIdx.y * 32;
@@ -383,6 +333,7 @@ __global__ void __launch_bounds__(256) router_logits_simt_kernel(const Tin *x, c
 __global__ void __launch_bounds__(256) route_reduce_kernel(const float *part_prob, const int32_t *part_cnt,
                                                            int64_t nblk, int E, int64_t T, float *prob_mean,
                                                            int32_t *counts) {
+    PDL_ENTER();
     __shared__ float sp[256];
     __shared__ int sc[256];
     const int e = blockIdx.x;
@@ -417,8 +368,7 @@ cudaError_t launch_route_logits_t(const RouteParams &p, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kern<<<(unsigned)nblk, 256, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)nblk), dim3(256), smem, s, p);
 }
 
 // Hash routing: one thread per token.  Choice j of a token is
@@ -436,6 +386,7 @@ __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
 
 __global__ void __launch_bounds__(256) route_hash_kernel(int64_t T, int E, int k, const int32_t *token_ids,
                                                          int32_t *topk_idx, float *topk_w) {
+    PDL_ENTER();
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     const uint32_t id = (uint32_t)token_ids[t];
@@ -464,23 +415,16 @@ __global__ void __launch_bounds__(256) route_hash_kernel(int64_t T, int E, int k
 cudaError_t launch_route_hash(int64_t T, int E, int k, const int32_t *token_ids, int32_t *topk_idx, float *topk_w,
                               cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    route_hash_kernel<<<(unsigned)ceil_div(T, 256), 256, 0, s>>>(T, E, k, token_ids, topk_idx, topk_w);
-    return cudaGetLastError();
+    return launch_pdl(route_hash_kernel, dim3((unsigned)ceil_div(T, 256)), dim3(256), 0, s, T, E, k, token_ids,
+                      topk_idx, topk_w);
 }
 
-cudaError_t launch_router_fused(const RouteParams &p, int dtype, cudaStream_t s) {
+cudaError_t launch_router_fused(const RouteParams &p, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
-    const unsigned nblk = (unsigned)ceil_div(p.T, kRouteTokPerCta);
-    if (dtype == 0) {
-        if (p.E <= 8) router_fused_kernel<float, 8><<<nblk, 256, 0, s>>>(p);
-        else if (p.E <= 16) router_fused_kernel<float, 16><<<nblk, 256, 0, s>>>(p);
-        else router_fused_kernel<float, 32><<<nblk, 256, 0, s>>>(p);
-    } else {
-        if (p.E <= 8) router_fused_kernel<bf16, 8><<<nblk, 256, 0, s>>>(p);
-        else if (p.E <= 16) router_fused_kernel<bf16, 16><<<nblk, 256, 0, s>>>(p);
-        else router_fused_kernel<bf16, 32><<<nblk, 256, 0, s>>>(p);
-    }
-    return cudaGetLastError();
+    const dim3 grid((unsigned)ceil_div(p.T, kRouteTokPerCta)), block(256);
+    if (p.E <= 8) return launch_pdl(router_fused_kernel<float, 8>, grid, block, 0, s, p);
+    if (p.E <= 16) return launch_pdl(router_fused_kernel<float, 16>, grid, block, 0, s, p);
+    return launch_pdl(router_fused_kernel<float, 32>, grid, block, 0, s, p);
 }
 
 cudaError_t launch_route_logits(const RouteParams &p, cudaStream_t s) {
@@ -498,21 +442,19 @@ cudaError_t launch_route_logits(const RouteParams &p, cudaStream_t s) {
 
 cudaError_t launch_router_logits_simt(const RouteParams &p, int dtype, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
-    dim3 grid((unsigned)ceil_div(p.T, 32), (unsigned)ceil_div(p.E, 32));
+    const dim3 grid((unsigned)ceil_div(p.T, 32), (unsigned)ceil_div(p.E, 32));
     if (dtype == 0)
-        router_logits_simt_kernel<float><<<grid, 256, 0, s>>>(
-            static_cast<const float *>(p.x), static_cast<const float *>(p.w_router), p.logits, p.T, p.E, p.d);
-    else
-        router_logits_simt_kernel<bf16><<<grid, 256, 0, s>>>(
-            static_cast<const bf16 *>(p.x), static_cast<const bf16 *>(p.w_router), p.logits, p.T, p.E, p.d);
-    return cudaGetLastError();
+        return launch_pdl(router_logits_simt_kernel<float>, grid, dim3(256), 0, s, static_cast<const float *>(p.x),
+                          static_cast<const float *>(p.w_router), p.logits, p.T, p.E, p.d);
+    return launch_pdl(router_logits_simt_kernel<bf16>, grid, dim3(256), 0, s, static_cast<const bf16 *>(p.x),
+                      static_cast<const bf16 *>(p.w_router), p.logits, p.T, p.E, p.d);
 }
 
 cudaError_t launch_route_reduce(const float *part_prob, const int32_t *part_cnt, int64_t nblk,
                                 int E, int64_t T, float *prob_mean, int32_t *counts,
                                 cudaStream_t s) {
-    route_reduce_kernel<<<(unsigned)E, 256, 0, s>>>(part_prob, part_cnt, nblk, E, T, prob_mean, counts);
-    return cudaGetLastError();
+    return launch_pdl(route_reduce_kernel, dim3((unsigned)E), dim3(256), 0, s, part_prob, part_cnt, nblk, E, T,
+                      prob_mean, counts);
 }
 
 }  // namespace moe

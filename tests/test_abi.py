@@ -60,7 +60,7 @@ def _ws_expect(w):
     eb = 4 if w.dtype == wl.F32 else 2
     nblk = -(-T // 32)
     nch = -(-S // 2048)
-    route = 2 * a(nblk * E * 4)
+    route = 2 * a(nblk * E * 4) + a(nblk * 4)
     perm = 2 * a(nch * E * 4)
     ffn = a(S * F * eb)
     shared = a(T * F * eb) if w.num_shared else 0

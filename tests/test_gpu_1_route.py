@@ -153,3 +153,16 @@ def test_route_from_x_other_paths(E, dtype):
                     score_fn=wl.SOFTMAX, dtype=dtype, router_bias=True, expert_bias=False)
     inp = wl.make_inputs(w, with_weights=False)
     check_route_from_x(w, inp, _route_from_x(w, inp))
+
+
+@pytest.mark.parametrize("E,k,score,renorm,bias,T", [
+    (5, 2, wl.SOFTMAX, 1, True, 333), (8, 1, wl.SOFTMAX, 0, False, 4097), (13, 3, wl.SIGMOID, 1, True, 1000),
+    (16, 4, wl.SOFTMAX, 1, False, 129), (24, 6, wl.SIGMOID, 1, False, 777), (32, 8, wl.SOFTMAX, 0, True, 2048),
+    (32, 16, wl.SIGMOID, 0, True, 95)])
+def test_route_from_x_fused_gemm_epilogue(E, k, score, renorm, bias, T):
+    """bf16 with E <= 32: the router GEMM routes in its epilogue (one thread
+    per token, expert bound 8 / 16 / 32), including its per-block partials."""
+    w = wl.Workload(f"rf{E}_{k}", 50 + E, T=T, d=256, E=E, k=k, F=64, activation=wl.GELU, score_fn=score,
+                    dtype=wl.BF16, router_bias=bias, expert_bias=False, renormalize=renorm)
+    inp = wl.make_inputs(w, with_weights=False)
+    check_route_from_x(w, inp, _route_from_x(w, inp))
