@@ -372,6 +372,7 @@ void orc_route_expert_choice(int64_t T, int32_t E, int64_t C, const float *logit
                 if (chosen[t]) continue;
                 if (best < 0 || logits[t * E + e] > logits[best * E + e]) best = t;
             }
+            if (best < 0) break;   /* C <= T: never */
             chosen[best] = 1;
         }
         int64_t n = 0;
@@ -648,4 +649,293 @@ void orc_param_counts(int64_t d, int64_t F, int64_t E, int64_t k, int gated, int
     out[1] = router;
     out[2] = E * expert + router;
     out[3] = k * expert + router;
+}
+
+/* ------------------------------------------------------------------ */
+/* backward                                                              */
+/* ------------------------------------------------------------------ */
+/*
+ * Gradients of the training objective of one layer,
+ *   L = sum_t <dout_t, out_t> + aux_coef * L_aux + z_coef * L_z,
+ * with out, L_aux = E sum_e f_e P_e and L_z = mean_t lse_t^2 as in the
+ * forward above.  No page prints a backward: the "MoE Training: Mixture of
+ * Experts" page adds the auxiliary loss (and the router z-loss) to the main
+ * loss of a training step, and the chain rule through the forward's
+ * definitions gives every term below.
+ *
+ * Experts (slot j of token t kept in row inv[t,j], expert e, gate g):
+ *   dy      = g * dout_t
+ *   dW2_e  += dy h^T,  db2_e += dy,  dh = W2_e^T dy
+ *   SwiGLU  h = silu(a1) * a3:  da1 = dh * a3 * silu'(a1),  da3 = dh * silu(a1)
+ *   GELU / ReLU  h = act(a):    da = dh * act'(a)  (ReLU'(0) = 0)
+ *   dW1_e  += da1 x^T,  dW3_e += da3 x^T,  db1_e += da,
+ *   dx_t   += W1_e^T da1 (+ W3_e^T da3)
+ *   dgate[t,j] = <dout_t, y>   (y the expert output; 0 for a dropped slot)
+ * Shared experts: the same with g = 1 for every token.  Residual: dx += dout.
+ * Router (fp64 from the fp32 logits l_t, p = softmax(l_t)):
+ *   softmax, renormalised: w_j = p_j / sum_S p  ->  dl_j = w_j (dg_j - sum_i w_i dg_i)
+ *   softmax, raw:          w_j = p_j             ->  dl_c = p_c (dg_c - sum_j p_j dg_j)
+ *   sigmoid s = sigma(l), renormalised: w_j = s_j / sum_S s
+ *                          ->  dl_j = s_j (1 - s_j) (dg_j - sum_i w_i dg_i) / sum_S s
+ *   sigmoid, raw:          dl_j = s_j (1 - s_j) dg_j
+ *   L_aux (f_e = counts_e / (T k) held constant, as a count has no gradient):
+ *                          dl_c += aux_coef (E / T) p_c (f_c - sum_e f_e p_e)
+ *   L_z:                   dl_c += z_coef (2 / T) lse_t p_c
+ *   dW_r += dl x^T,  db_r += dl,  dx_t += W_r^T dl.
+ *   The selection bias b_i enters only the choice, so it gets no gradient.
+ * For bf16 layers the operands the tensor cores consume are rounded to bf16
+ * at the points where they are stored: H (as in the forward), dy and
+ * da1 / da3 / da; everything else is fp64.
+ *
+ * Outputs (fp64, overwritten): dx [T,d], dw_router [E,d], db_router [E],
+ * dw1 [E,F,d], db1 [E,F], dw3 [E,F,d], dw2 [E,d,F], db2 [E,d], dsw1 / dsw3
+ * [S,F,d], dsw2 [S,d,F], dgate [T,k], dlogits [T,E]; NULL skips one.
+ */
+typedef struct {
+    double *dx, *dw_router, *db_router, *dw1, *db1, *dw3, *dw2, *db2, *dsw1, *dsw3, *dsw2, *dgate, *dlogits;
+} orc_grads;
+
+static double rnd(const orc_cfg *c, double v) { return c->dtype == 1 ? orc_round_bf16(v) : v; }
+
+static double act_grad(int activation, double a) {
+    if (activation == 0) return 0.5 * (1.0 + erf(a / sqrt(2.0))) + a * exp(-0.5 * a * a) / sqrt(2.0 * acos(-1.0));
+    return a > 0.0 ? 1.0 : 0.0;
+}
+
+/* Row f of one expert at input x: pre-activations (a1, a3 or a) and h_f. */
+static void expert_unit(const orc_cfg *c, const void *W1, const void *B1, const void *W3, int64_t e, int64_t f,
+                        const double *xv, double *a1, double *a3, double *h) {
+    const int64_t d = c->d, F = c->F;
+    *a1 = dot_row(W1, c->dtype, e * F * d + f * d, xv, d);
+    if (c->activation == 2) {
+        *a3 = dot_row(W3, c->dtype, e * F * d + f * d, xv, d);
+        *h = rnd(c, act_silu(*a1) * *a3);
+    } else {
+        if (B1) *a1 += elem(B1, c->dtype, e * F + f);
+        *a3 = 0.0;
+        *h = rnd(c, c->activation == 0 ? act_gelu(*a1) : act_relu(*a1));
+    }
+}
+
+/* d(pre-activations) of row f from dh_f (rounded like the stored operand). */
+static void expert_unit_grad(const orc_cfg *c, double a1, double a3, double dh, double *da1, double *da3) {
+    if (c->activation == 2) {
+        const double sg = 1.0 / (1.0 + exp(-a1));
+        const double dsilu = sg * (1.0 + a1 * (1.0 - sg));
+        *da1 = rnd(c, dh * a3 * dsilu);
+        *da3 = rnd(c, dh * act_silu(a1));
+    } else {
+        *da1 = rnd(c, dh * act_grad(c->activation, a1));
+        *da3 = 0.0;
+    }
+}
+
+/* Data path of one (expert, token): y (expert output) and dx += W^T da. */
+static void expert_backward_row(const orc_cfg *c, const void *W1, const void *B1, const void *W3, const void *W2,
+                                const void *B2, int64_t e, const double *xv, const double *dy, double *a1,
+                                double *a3, double *h, double *y, double *dx) {
+    const int64_t d = c->d, F = c->F;
+    const int dt = c->dtype;
+    for (int64_t f = 0; f < F; ++f) expert_unit(c, W1, B1, W3, e, f, xv, &a1[f], &a3[f], &h[f]);
+    for (int64_t n = 0; n < d; ++n) {
+        double acc = dot_row(W2, dt, e * d * F + n * F, h, F);
+        if (c->activation != 2 && B2) acc += elem(B2, dt, e * d + n);
+        y[n] = acc;
+    }
+    for (int64_t f = 0; f < F; ++f) {
+        double dh = 0.0;
+        for (int64_t n = 0; n < d; ++n) dh += elem(W2, dt, e * d * F + n * F + f) * dy[n];
+        double da1, da3;
+        expert_unit_grad(c, a1[f], a3[f], dh, &da1, &da3);
+        for (int64_t i = 0; i < d; ++i) {
+            dx[i] += elem(W1, dt, e * F * d + f * d + i) * da1;
+            if (c->activation == 2) dx[i] += elem(W3, dt, e * F * d + f * d + i) * da3;
+        }
+    }
+}
+
+void orc_backward(const orc_cfg *c, const orc_tensors *w, const float *logits, const int32_t *idx,
+                  const double *gate, const int32_t *inv, const int32_t *counts, const double *dout,
+                  double aux_coef, double z_coef, orc_grads *g) {
+    const int64_t T = c->T, d = c->d, E = c->E, k = c->k, F = c->F, S = c->num_shared;
+    const int dt = c->dtype;
+    double *dx = (double *)calloc((size_t)(T * d + 1), sizeof(double));
+    double *dgate = (double *)calloc((size_t)(T * k + 1), sizeof(double));
+    double *dl = (double *)calloc((size_t)(T * E + 1), sizeof(double));
+
+    /* A: per token, experts' data path, dgate, residual */
+#pragma omp parallel
+    {
+        double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dy = (double *)malloc(sizeof(double) * (size_t)d);
+        double *y = (double *)malloc(sizeof(double) * (size_t)d);
+        double *a1 = (double *)malloc(sizeof(double) * (size_t)F);
+        double *a3 = (double *)malloc(sizeof(double) * (size_t)F);
+        double *h = (double *)malloc(sizeof(double) * (size_t)F);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            decode_row(w->x, dt, t * d, d, xv);
+            const double *go = dout + t * d;
+            double *dxt = dx + t * d;
+            for (int64_t j = 0; j < k; ++j) {
+                const int64_t s = t * k + j;
+                if (inv && inv[s] < 0) continue;
+                for (int64_t n = 0; n < d; ++n) dy[n] = rnd(c, gate[s] * go[n]);
+                expert_backward_row(c, w->w1, w->b1, w->w3, w->w2, w->b2, idx[s], xv, dy, a1, a3, h, y, dxt);
+                double acc = 0.0;
+                for (int64_t n = 0; n < d; ++n) acc += go[n] * y[n];
+                dgate[s] = acc;
+            }
+            for (int64_t sh = 0; sh < S; ++sh) {
+                for (int64_t n = 0; n < d; ++n) dy[n] = rnd(c, go[n]);
+                expert_backward_row(c, w->sw1, NULL, w->sw3, w->sw2, NULL, sh, xv, dy, a1, a3, h, y, dxt);
+            }
+            if (c->residual)
+                for (int64_t n = 0; n < d; ++n) dxt[n] += go[n];
+        }
+        free(xv);
+        free(dy);
+        free(y);
+        free(a1);
+        free(a3);
+        free(h);
+    }
+
+    /* B: router, per token */
+    double *fe = (double *)malloc(sizeof(double) * (size_t)(E + 1));
+    for (int64_t e = 0; e < E; ++e) fe[e] = T * k > 0 ? (double)counts[e] / (double)(T * k) : 0.0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)E);
+        double *wr = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            const float *l = logits + t * E;
+            double *dlt = dl + t * E;
+            double m = -INFINITY;
+            for (int64_t e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+            double ssum = 0.0;
+            for (int64_t e = 0; e < E; ++e) ssum += exp((double)l[e] - m);
+            const double lse = m + log(ssum);
+            for (int64_t e = 0; e < E; ++e) p[e] = exp((double)l[e] - lse);
+            const int32_t *it = idx + t * k;
+            const double *dg = dgate + t * k;
+            if (c->score_fn == 0) {
+                if (c->renormalize) {
+                    double tot = 0.0, wdg = 0.0;
+                    for (int64_t j = 0; j < k; ++j) tot += p[it[j]];
+                    for (int64_t j = 0; j < k; ++j) wdg += p[it[j]] / tot * dg[j];
+                    for (int64_t j = 0; j < k; ++j) dlt[it[j]] += p[it[j]] / tot * (dg[j] - wdg);
+                } else {
+                    double pdg = 0.0;
+                    for (int64_t j = 0; j < k; ++j) pdg += p[it[j]] * dg[j];
+                    for (int64_t e = 0; e < E; ++e) dlt[e] -= p[e] * pdg;
+                    for (int64_t j = 0; j < k; ++j) dlt[it[j]] += p[it[j]] * dg[j];
+                }
+            } else {
+                double tot = 0.0, wdg = 0.0;
+                for (int64_t j = 0; j < k; ++j) tot += 1.0 / (1.0 + exp(-(double)l[it[j]]));
+                for (int64_t j = 0; j < k; ++j) {
+                    const double sj = 1.0 / (1.0 + exp(-(double)l[it[j]]));
+                    wdg += sj / tot * dg[j];
+                }
+                for (int64_t j = 0; j < k; ++j) {
+                    const double sj = 1.0 / (1.0 + exp(-(double)l[it[j]]));
+                    const double ds = c->renormalize ? (dg[j] - wdg) / tot : dg[j];
+                    dlt[it[j]] += sj * (1.0 - sj) * ds;
+                }
+            }
+            double fp = 0.0;
+            for (int64_t e = 0; e < E; ++e) fp += fe[e] * p[e];
+            for (int64_t e = 0; e < E; ++e) {
+                dlt[e] += aux_coef * ((double)E / (double)T) * p[e] * (fe[e] - fp);
+                dlt[e] += z_coef * (2.0 / (double)T) * lse * p[e];
+            }
+            double *dxt = dx + t * d;
+            for (int64_t e = 0; e < E; ++e) {
+                decode_row(w->w_router, dt, e * d, d, wr);
+                for (int64_t i = 0; i < d; ++i) dxt[i] += dlt[e] * wr[i];
+            }
+        }
+        free(p);
+        free(wr);
+    }
+
+    /* C: weight gradients, per (expert, row f); the expert's tokens in
+     * token order */
+    const int64_t n_units = (E + S) * F;
+    if (g->dw1 || g->dw2 || g->dw3 || g->db1 || g->db2 || g->dsw1 || g->dsw2 || g->dsw3) {
+        if (g->dw1) memset(g->dw1, 0, sizeof(double) * (size_t)(E * F * d));
+        if (g->dw3) memset(g->dw3, 0, sizeof(double) * (size_t)(E * F * d));
+        if (g->dw2) memset(g->dw2, 0, sizeof(double) * (size_t)(E * d * F));
+        if (g->db1) memset(g->db1, 0, sizeof(double) * (size_t)(E * F));
+        if (g->db2) memset(g->db2, 0, sizeof(double) * (size_t)(E * d));
+        if (g->dsw1) memset(g->dsw1, 0, sizeof(double) * (size_t)(S * F * d));
+        if (g->dsw3) memset(g->dsw3, 0, sizeof(double) * (size_t)(S * F * d));
+        if (g->dsw2) memset(g->dsw2, 0, sizeof(double) * (size_t)(S * d * F));
+#pragma omp parallel
+        {
+            double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+            double *dy = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t u = 0; u < n_units; ++u) {
+                const int64_t ee = u / F, f = u % F;
+                const int shared = ee >= E;
+                const int64_t e = shared ? ee - E : ee;
+                const void *W1 = shared ? w->sw1 : w->w1, *W3 = shared ? w->sw3 : w->w3;
+                const void *W2 = shared ? w->sw2 : w->w2, *B1 = shared ? NULL : w->b1;
+                double *dW1 = shared ? g->dsw1 : g->dw1, *dW3 = shared ? g->dsw3 : g->dw3;
+                double *dW2 = shared ? g->dsw2 : g->dw2;
+                for (int64_t t = 0; t < T; ++t) {
+                    double gt = 1.0;
+                    if (!shared) {
+                        int64_t jj = -1;
+                        for (int64_t j = 0; j < k; ++j)
+                            if (idx[t * k + j] == e && !(inv && inv[t * k + j] < 0)) jj = j;
+                        if (jj < 0) continue;
+                        gt = gate[t * k + jj];
+                    }
+                    decode_row(w->x, dt, t * d, d, xv);
+                    for (int64_t n = 0; n < d; ++n) dy[n] = rnd(c, gt * dout[t * d + n]);
+                    double a1, a3, h;
+                    expert_unit(c, W1, B1, W3, e, f, xv, &a1, &a3, &h);
+                    double dh = 0.0;
+                    for (int64_t n = 0; n < d; ++n) dh += elem(W2, dt, e * d * F + n * F + f) * dy[n];
+                    double da1, da3;
+                    expert_unit_grad(c, a1, a3, dh, &da1, &da3);
+                    if (dW1)
+                        for (int64_t i = 0; i < d; ++i) dW1[e * F * d + f * d + i] += da1 * xv[i];
+                    if (dW3 && c->activation == 2)
+                        for (int64_t i = 0; i < d; ++i) dW3[e * F * d + f * d + i] += da3 * xv[i];
+                    if (dW2)
+                        for (int64_t n = 0; n < d; ++n) dW2[e * d * F + n * F + f] += dy[n] * h;
+                    if (!shared && g->db1) g->db1[e * F + f] += da1;
+                    if (!shared && g->db2 && f == 0)
+                        for (int64_t n = 0; n < d; ++n) g->db2[e * d + n] += dy[n];
+                }
+            }
+            free(xv);
+            free(dy);
+        }
+    }
+    if (g->dw_router || g->db_router) {
+        if (g->dw_router) memset(g->dw_router, 0, sizeof(double) * (size_t)(E * d));
+        if (g->db_router) memset(g->db_router, 0, sizeof(double) * (size_t)E);
+#pragma omp parallel for schedule(static)
+        for (int64_t e = 0; e < E; ++e) {
+            for (int64_t t = 0; t < T; ++t) {
+                const double v = dl[t * E + e];
+                if (g->db_router) g->db_router[e] += v;
+                if (g->dw_router)
+                    for (int64_t i = 0; i < d; ++i) g->dw_router[e * d + i] += v * elem(w->x, dt, t * d + i);
+            }
+        }
+    }
+    if (g->dx) memcpy(g->dx, dx, sizeof(double) * (size_t)(T * d));
+    if (g->dgate) memcpy(g->dgate, dgate, sizeof(double) * (size_t)(T * k));
+    if (g->dlogits) memcpy(g->dlogits, dl, sizeof(double) * (size_t)(T * E));
+    free(dx);
+    free(dgate);
+    free(dl);
+    free(fe);
 }

@@ -92,6 +92,7 @@ def lib():
             L.orc_ec_capacity.restype = C.c_int64
             L.orc_ec_capacity.argtypes = [C.c_int64, C.c_int32, C.c_double, C.c_int32]
             L.orc_route_expert_choice.argtypes = [C.c_int64, C.c_int32, C.c_int64, P, P, P, P]
+            L.orc_backward.argtypes = [P] * 8 + [C.c_double, C.c_double, P]
             _lib = L
     return _lib
 
@@ -304,6 +305,46 @@ def param_counts(d: int, F: int, E: int, k: int, gated: bool):
     out = np.empty(4, np.int64)
     lib().orc_param_counts(d, F, E, k, int(gated), out.ctypes.data)
     return dict(expert=int(out[0]), router=int(out[1]), total=int(out[2]), active=int(out[3]))
+
+
+class _Grads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("dx", "dw_router", "db_router", "dw1", "db1", "dw3", "dw2", "db2",
+                                          "dsw1", "dsw3", "dsw2", "dgate", "dlogits")]
+
+
+def backward(w, inp, fwd, dout, aux_coef: float = 0.0, z_coef: float = 0.0):
+    """Gradients (fp64) of sum_t <dout_t, out_t> + aux_coef * L_aux +
+    z_coef * L_z for the forward ``fwd`` (``layer``'s routing and dispatch:
+    logits, idx, gate, inv, counts).  Returns a dict keyed like the C
+    orc_grads fields; weight gradients of absent weights are None."""
+    c, tn = _cfg(w), _tensors(inp)
+    T, d, E, k, F, S = w.T, w.d, w.E, w.k, w.F, w.num_shared
+    gated = w.activation == 2
+    out = dict(dx=np.zeros((T, d)), dw_router=np.zeros((E, d)), db_router=np.zeros(E),
+               dw1=np.zeros((E, F, d)), db1=np.zeros((E, F)) if "b1" in inp else None,
+               dw3=np.zeros((E, F, d)) if gated else None, dw2=np.zeros((E, d, F)),
+               db2=np.zeros((E, d)) if "b2" in inp else None,
+               dsw1=np.zeros((S, F, d)) if S else None, dsw3=np.zeros((S, F, d)) if S and gated else None,
+               dsw2=np.zeros((S, d, F)) if S else None, dgate=np.zeros((T, k)), dlogits=np.zeros((T, E)))
+    g = _Grads(**{n: _p(out[n]) for n, _ in _Grads._fields_})
+    lg = _c(fwd["logits"], np.float32)
+    idx = _c(fwd["idx"], np.int32)
+    gate = _c(fwd["gate"], np.float64)
+    inv = _c(fwd["inv"], np.int32)
+    counts = _c(fwd["counts"], np.int32)
+    dout = _c(dout, np.float64)
+    lib().orc_backward(C.byref(c), C.byref(tn), lg.ctypes.data, idx.ctypes.data, gate.ctypes.data,
+                       inv.ctypes.data, counts.ctypes.data, dout.ctypes.data, float(aux_coef), float(z_coef),
+                       C.byref(g))
+    return out
+
+
+def loss(w, inp, dout, aux_coef: float = 0.0, z_coef: float = 0.0) -> float:
+    """sum_t <dout_t, out_t> + aux_coef * L_aux + z_coef * L_z of the layer
+    (the scalar the backward differentiates)."""
+    r = layer(w, inp)
+    return float(np.sum(np.asarray(dout, np.float64) * r["out"]) + aux_coef * r["stats"]["aux"]
+                 + z_coef * r["stats"]["z"])
 
 
 def layer(w, inp, tokens=None):
