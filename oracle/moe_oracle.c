@@ -683,9 +683,12 @@ void orc_param_counts(int64_t d, int64_t F, int64_t E, int64_t k, int gated, int
  *   L_z:                   dl_c += z_coef (2 / T) lse_t p_c
  *   dW_r += dl x^T,  db_r += dl,  dx_t += W_r^T dl.
  *   The selection bias b_i enters only the choice, so it gets no gradient.
- * For bf16 layers the operands the tensor cores consume are rounded to bf16
- * at the points where they are stored: H (as in the forward), dy and
- * da1 / da3 / da; everything else is fp64.
+ * For bf16 layers the values the backward reads from bf16 storage are
+ * rounded to bf16 at the points where they are stored: H (as in the
+ * forward), the pre-activations a1 / a3 / a the forward keeps for the
+ * backward (used by the activation derivative; H itself is formed from the
+ * unrounded ones, as in the forward), dy and da1 / da3 / da; everything
+ * else is fp64.
  *
  * Outputs (fp64, overwritten): dx [T,d], dw_router [E,d], db_router [E],
  * dw1 [E,F,d], db1 [E,F], dw3 [E,F,d], dw2 [E,d,F], db2 [E,d], dsw1 / dsw3
@@ -746,7 +749,7 @@ static void expert_backward_row(const orc_cfg *c, const void *W1, const void *B1
         double dh = 0.0;
         for (int64_t n = 0; n < d; ++n) dh += elem(W2, dt, e * d * F + n * F + f) * dy[n];
         double da1, da3;
-        expert_unit_grad(c, a1[f], a3[f], dh, &da1, &da3);
+        expert_unit_grad(c, rnd(c, a1[f]), rnd(c, a3[f]), dh, &da1, &da3);
         for (int64_t i = 0; i < d; ++i) {
             dx[i] += elem(W1, dt, e * F * d + f * d + i) * da1;
             if (c->activation == 2) dx[i] += elem(W3, dt, e * F * d + f * d + i) * da3;
@@ -902,7 +905,7 @@ void orc_backward(const orc_cfg *c, const orc_tensors *w, const float *logits, c
                     double dh = 0.0;
                     for (int64_t n = 0; n < d; ++n) dh += elem(W2, dt, e * d * F + n * F + f) * dy[n];
                     double da1, da3;
-                    expert_unit_grad(c, a1, a3, dh, &da1, &da3);
+                    expert_unit_grad(c, rnd(c, a1), rnd(c, a3), dh, &da1, &da3);
                     if (dW1)
                         for (int64_t i = 0; i < d; ++i) dW1[e * F * d + f * d + i] += da1 * xv[i];
                     if (dW3 && c->activation == 2)
