@@ -133,7 +133,14 @@ typedef struct {
  * (created by the caller) that moe_forward records on its stream at the
  * stage boundaries: [0] start, [1] routed, [2] dispatched, [3] expert
  * first GEMM (W1/W3 + activation) done, [4] expert second GEMM done,
- * [5] shared expert done, [6] combined, [7] statistics done.  NULL: none. */
+ * [5] shared expert done, [6] combined, [7] statistics done.  NULL: none.
+ * Training members (bf16 layers; what moe_backward needs besides the
+ * routing members above): x_perm [T*k, d] and hidden [T*k, F] (H, the
+ * input of the second expert GEMM) in the layer dtype; pre_act, the first
+ * GEMM's pre-activations in bf16: [T*k, 2F] holding W1 x | W3 x for SwiGLU,
+ * [T*k, F] holding W1 x + b1 for GELU / ReLU; y_perm [T*k, d] fp32 expert
+ * outputs; shared_pre_act [T, 2F or F] and shared_hidden [T, F] for the
+ * shared expert.  Rows past offsets[E] are not written. */
 #define MOE_STAGE_EVENTS 8
 typedef struct {
     float *logits;
@@ -149,6 +156,12 @@ typedef struct {
     float *f;
     moe_stats_t *stats;
     void *const *stage_events;
+    void *x_perm;
+    void *pre_act;
+    void *hidden;
+    float *y_perm;
+    void *shared_pre_act;
+    void *shared_hidden;
 } moe_forward_io_t;
 
 /* Which call a workspace is sized for. */
@@ -158,12 +171,13 @@ enum {
     MOE_WS_PERMUTE = 2,
     MOE_WS_EXPERT_FFN = 3,
     MOE_WS_SHARED_FFN = 4,
-    MOE_WS_EXPERT_CHOICE = 5
+    MOE_WS_EXPERT_CHOICE = 5,
+    MOE_WS_BACKWARD = 6
 };
 
 /* Workspace bytes the given call needs (host output).  A workspace sized
  * for MOE_WS_FORWARD is large enough for every call but
- * moe_forward_expert_choice.  Workspace contents
+ * moe_forward_expert_choice and moe_backward.  Workspace contents
  * need no initialisation and carry nothing between calls. */
 moe_status_t moe_workspace_size(const moe_config_t *cfg, int32_t which, size_t *bytes);
 
@@ -396,6 +410,62 @@ typedef struct {
 moe_status_t moe_forward_expert_choice(const moe_config_t *cfg, const moe_weights_t *weights, const void *x,
                                        void *out, const moe_ec_io_t *io, void *ws, size_t ws_bytes,
                                        moe_stream_t stream);
+
+/*
+ * Backward of the layer.  No page prints one; the objective is the one the
+ * "MoE Training: Mixture of Experts" page trains: the layer output plus the
+ * auxiliary load-balancing loss (Load Balancing: loss = main + coef * aux)
+ * and the router z-loss,
+ *   L = sum_t <dout_t, out_t> + aux_coef * L_aux + z_coef * L_z,
+ * differentiated through the forward: gate-weighted combine, expert FFNs
+ * (GELU / ReLU / SwiGLU, biases), shared expert, residual, gate function
+ * (softmax or sigmoid, renormalised or raw; the selection and the selection
+ * bias b_i are piecewise constant and get no gradient), L_aux with the
+ * token fractions f_e held fixed, L_z.  Dropped slots pass no gradient.
+ *
+ * saved: the routing and training members a forward wrote through
+ *   moe_forward_io_t (device buffers); counts are the pre-drop counts.
+ * x, dout [T, d] bf16.  grads (device, fp32, overwritten): dx [T, d];
+ *   dw_router [E, d]; db_router [E] (NULL without router bias); dw1 [E,F,d],
+ *   db1 [E,F] (GELU / ReLU with biases), dw3 [E,F,d] (SwiGLU), dw2 [E,d,F],
+ *   db2 [E,d]; shared_dw1 / shared_dw3 [F,d], shared_dw2 [d,F].  A NULL
+ *   weight gradient is not computed; dx must be given.
+ * bf16 layers only (MOE_ERR_UNSUPPORTED for fp32).  The operands the tensor
+ * cores consume are stored in bf16 (dy = gate * dout, da); accumulation is
+ * fp32.  Workspace: moe_workspace_size(MOE_WS_BACKWARD).
+ */
+typedef struct {
+    const int32_t *topk_idx;
+    const float *topk_w;
+    const float *logits;
+    const int32_t *inv;
+    const int32_t *offsets;
+    const int32_t *counts;
+    const void *x_perm;
+    const void *pre_act;
+    const void *hidden;
+    const float *y_perm;
+    const void *shared_pre_act;
+    const void *shared_hidden;
+} moe_saved_t;
+
+typedef struct {
+    float *dx;
+    float *dw_router;
+    float *db_router;
+    float *dw1;
+    float *db1;
+    float *dw3;
+    float *dw2;
+    float *db2;
+    float *shared_dw1;
+    float *shared_dw3;
+    float *shared_dw2;
+} moe_grads_t;
+
+moe_status_t moe_backward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x, const void *dout,
+                          const moe_saved_t *saved, float aux_coef, float z_coef, const moe_grads_t *grads,
+                          void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Reads and clears the device error flag (host output *code: 0 = none,
  * else a moe_status_t).  Synchronises the device first. */

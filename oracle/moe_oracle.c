@@ -757,6 +757,69 @@ static void expert_backward_row(const orc_cfg *c, const void *W1, const void *B1
     }
 }
 
+/* Weight gradients of one unit: row f of routed expert ee (ee < E) or of
+ * shared expert ee - E, summed over the tokens the expert processed, in
+ * token order.  Writes (when not NULL) dW1 row f [d], dW3 row f [d],
+ * column f of dW2 [d], db1[f]; db2 [d] (the whole expert's, accumulated). */
+static void wgrad_unit(const orc_cfg *c, const orc_tensors *w, const int32_t *idx, const double *gate,
+                       const int32_t *inv, const double *dout, int64_t ee, int64_t f, double *dw1_row,
+                       double *dw3_row, double *dw2_col, double *db1, double *db2) {
+    const int64_t T = c->T, d = c->d, E = c->E, k = c->k, F = c->F;
+    const int dt = c->dtype;
+    const int shared = ee >= E;
+    const int64_t e = shared ? ee - E : ee;
+    const void *W1 = shared ? w->sw1 : w->w1, *W3 = shared ? w->sw3 : w->w3;
+    const void *W2 = shared ? w->sw2 : w->w2, *B1 = shared ? NULL : w->b1;
+    double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+    double *dy = (double *)malloc(sizeof(double) * (size_t)d);
+    if (dw1_row) memset(dw1_row, 0, sizeof(double) * (size_t)d);
+    if (dw3_row) memset(dw3_row, 0, sizeof(double) * (size_t)d);
+    if (dw2_col) memset(dw2_col, 0, sizeof(double) * (size_t)d);
+    *db1 = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        double gt = 1.0;
+        if (!shared) {
+            int64_t jj = -1;
+            for (int64_t j = 0; j < k; ++j)
+                if (idx[t * k + j] == e && !(inv && inv[t * k + j] < 0)) jj = j;
+            if (jj < 0) continue;
+            gt = gate[t * k + jj];
+        }
+        decode_row(w->x, dt, t * d, d, xv);
+        for (int64_t n = 0; n < d; ++n) dy[n] = rnd(c, gt * dout[t * d + n]);
+        double a1, a3, h;
+        expert_unit(c, W1, B1, W3, e, f, xv, &a1, &a3, &h);
+        double dh = 0.0;
+        for (int64_t n = 0; n < d; ++n) dh += elem(W2, dt, e * d * F + n * F + f) * dy[n];
+        double da1, da3;
+        expert_unit_grad(c, rnd(c, a1), rnd(c, a3), dh, &da1, &da3);
+        if (dw1_row)
+            for (int64_t i = 0; i < d; ++i) dw1_row[i] += da1 * xv[i];
+        if (dw3_row && c->activation == 2)
+            for (int64_t i = 0; i < d; ++i) dw3_row[i] += da3 * xv[i];
+        if (dw2_col)
+            for (int64_t n = 0; n < d; ++n) dw2_col[n] += dy[n] * h;
+        *db1 += da1;
+        if (db2)
+            for (int64_t n = 0; n < d; ++n) db2[n] += dy[n];
+    }
+    free(xv);
+    free(dy);
+}
+
+/* Weight gradients of the listed units only (u = ee * F + f, ee >= E for a
+ * shared expert), each row [d]: dw1 / dw3 rows, dw2 columns, db1 values.
+ * Same sums as orc_backward; for layers too large for full fp64 arrays. */
+void orc_backward_units(const orc_cfg *c, const orc_tensors *w, const int32_t *idx, const double *gate,
+                        const int32_t *inv, const double *dout, const int64_t *units, int64_t n, double *dw1,
+                        double *dw3, double *dw2, double *db1) {
+    const int64_t d = c->d, F = c->F;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i)
+        wgrad_unit(c, w, idx, gate, inv, dout, units[i] / F, units[i] % F, dw1 + i * d, dw3 ? dw3 + i * d : NULL,
+                   dw2 + i * d, db1 + i, NULL);
+}
+
 void orc_backward(const orc_cfg *c, const orc_tensors *w, const float *logits, const int32_t *idx,
                   const double *gate, const int32_t *inv, const int32_t *counts, const double *dout,
                   double aux_coef, double z_coef, orc_grads *g) {
@@ -878,47 +941,23 @@ void orc_backward(const orc_cfg *c, const orc_tensors *w, const float *logits, c
         if (g->dsw2) memset(g->dsw2, 0, sizeof(double) * (size_t)(S * d * F));
 #pragma omp parallel
         {
-            double *xv = (double *)malloc(sizeof(double) * (size_t)d);
-            double *dy = (double *)malloc(sizeof(double) * (size_t)d);
+            double *col = (double *)malloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(dynamic, 1)
             for (int64_t u = 0; u < n_units; ++u) {
                 const int64_t ee = u / F, f = u % F;
                 const int shared = ee >= E;
                 const int64_t e = shared ? ee - E : ee;
-                const void *W1 = shared ? w->sw1 : w->w1, *W3 = shared ? w->sw3 : w->w3;
-                const void *W2 = shared ? w->sw2 : w->w2, *B1 = shared ? NULL : w->b1;
                 double *dW1 = shared ? g->dsw1 : g->dw1, *dW3 = shared ? g->dsw3 : g->dw3;
                 double *dW2 = shared ? g->dsw2 : g->dw2;
-                for (int64_t t = 0; t < T; ++t) {
-                    double gt = 1.0;
-                    if (!shared) {
-                        int64_t jj = -1;
-                        for (int64_t j = 0; j < k; ++j)
-                            if (idx[t * k + j] == e && !(inv && inv[t * k + j] < 0)) jj = j;
-                        if (jj < 0) continue;
-                        gt = gate[t * k + jj];
-                    }
-                    decode_row(w->x, dt, t * d, d, xv);
-                    for (int64_t n = 0; n < d; ++n) dy[n] = rnd(c, gt * dout[t * d + n]);
-                    double a1, a3, h;
-                    expert_unit(c, W1, B1, W3, e, f, xv, &a1, &a3, &h);
-                    double dh = 0.0;
-                    for (int64_t n = 0; n < d; ++n) dh += elem(W2, dt, e * d * F + n * F + f) * dy[n];
-                    double da1, da3;
-                    expert_unit_grad(c, rnd(c, a1), rnd(c, a3), dh, &da1, &da3);
-                    if (dW1)
-                        for (int64_t i = 0; i < d; ++i) dW1[e * F * d + f * d + i] += da1 * xv[i];
-                    if (dW3 && c->activation == 2)
-                        for (int64_t i = 0; i < d; ++i) dW3[e * F * d + f * d + i] += da3 * xv[i];
-                    if (dW2)
-                        for (int64_t n = 0; n < d; ++n) dW2[e * d * F + n * F + f] += dy[n] * h;
-                    if (!shared && g->db1) g->db1[e * F + f] += da1;
-                    if (!shared && g->db2 && f == 0)
-                        for (int64_t n = 0; n < d; ++n) g->db2[e * d + n] += dy[n];
-                }
+                double db1 = 0.0;
+                wgrad_unit(c, w, idx, gate, inv, dout, ee, f, dW1 ? dW1 + e * F * d + f * d : NULL,
+                           dW3 ? dW3 + e * F * d + f * d : NULL, col, &db1,
+                           (!shared && g->db2 && f == 0) ? g->db2 + e * d : NULL);
+                if (dW2)
+                    for (int64_t n = 0; n < d; ++n) dW2[e * d * F + n * F + f] = col[n];
+                if (!shared && g->db1) g->db1[e * F + f] = db1;
             }
-            free(xv);
-            free(dy);
+            free(col);
         }
     }
     if (g->dw_router || g->db_router) {

@@ -93,6 +93,7 @@ def lib():
             L.orc_ec_capacity.argtypes = [C.c_int64, C.c_int32, C.c_double, C.c_int32]
             L.orc_route_expert_choice.argtypes = [C.c_int64, C.c_int32, C.c_int64, P, P, P, P]
             L.orc_backward.argtypes = [P] * 8 + [C.c_double, C.c_double, P]
+            L.orc_backward_units.argtypes = [P] * 7 + [C.c_int64] + [P] * 4
             _lib = L
     return _lib
 
@@ -312,20 +313,25 @@ class _Grads(C.Structure):
                                           "dsw1", "dsw3", "dsw2", "dgate", "dlogits")]
 
 
-def backward(w, inp, fwd, dout, aux_coef: float = 0.0, z_coef: float = 0.0):
+def backward(w, inp, fwd, dout, aux_coef: float = 0.0, z_coef: float = 0.0, units=None):
     """Gradients (fp64) of sum_t <dout_t, out_t> + aux_coef * L_aux +
     z_coef * L_z for the forward ``fwd`` (``layer``'s routing and dispatch:
     logits, idx, gate, inv, counts).  Returns a dict keyed like the C
-    orc_grads fields; weight gradients of absent weights are None."""
+    orc_grads fields; weight gradients of absent weights are None.
+    ``units``: compute the expert weight gradients only for these units
+    (u = expert * F + f, experts >= E being shared experts) and return them
+    as rows: dw1_rows / dw3_rows [n, d], dw2_cols [n, d], db1_units [n]."""
     c, tn = _cfg(w), _tensors(inp)
     T, d, E, k, F, S = w.T, w.d, w.E, w.k, w.F, w.num_shared
     gated = w.activation == 2
+    full = units is None
+    z = lambda *shape: np.zeros(shape) if full else None
     out = dict(dx=np.zeros((T, d)), dw_router=np.zeros((E, d)), db_router=np.zeros(E),
-               dw1=np.zeros((E, F, d)), db1=np.zeros((E, F)) if "b1" in inp else None,
-               dw3=np.zeros((E, F, d)) if gated else None, dw2=np.zeros((E, d, F)),
+               dw1=z(E, F, d), db1=z(E, F) if "b1" in inp else None,
+               dw3=z(E, F, d) if gated else None, dw2=z(E, d, F),
                db2=np.zeros((E, d)) if "b2" in inp else None,
-               dsw1=np.zeros((S, F, d)) if S else None, dsw3=np.zeros((S, F, d)) if S and gated else None,
-               dsw2=np.zeros((S, d, F)) if S else None, dgate=np.zeros((T, k)), dlogits=np.zeros((T, E)))
+               dsw1=z(S, F, d) if S else None, dsw3=z(S, F, d) if S and gated else None,
+               dsw2=z(S, d, F) if S else None, dgate=np.zeros((T, k)), dlogits=np.zeros((T, E)))
     g = _Grads(**{n: _p(out[n]) for n, _ in _Grads._fields_})
     lg = _c(fwd["logits"], np.float32)
     idx = _c(fwd["idx"], np.int32)
@@ -336,6 +342,14 @@ def backward(w, inp, fwd, dout, aux_coef: float = 0.0, z_coef: float = 0.0):
     lib().orc_backward(C.byref(c), C.byref(tn), lg.ctypes.data, idx.ctypes.data, gate.ctypes.data,
                        inv.ctypes.data, counts.ctypes.data, dout.ctypes.data, float(aux_coef), float(z_coef),
                        C.byref(g))
+    if not full:
+        u = _c(units, np.int64)
+        n = len(u)
+        out.update(units=u, dw1_rows=np.zeros((n, d)), dw3_rows=np.zeros((n, d)) if gated else None,
+                   dw2_cols=np.zeros((n, d)), db1_units=np.zeros(n))
+        lib().orc_backward_units(C.byref(c), C.byref(tn), idx.ctypes.data, gate.ctypes.data, inv.ctypes.data,
+                                 dout.ctypes.data, u.ctypes.data, n, out["dw1_rows"].ctypes.data,
+                                 _p(out["dw3_rows"]), out["dw2_cols"].ctypes.data, out["db1_units"].ctypes.data)
     return out
 
 

@@ -16,8 +16,9 @@ from __future__ import annotations
 import ctypes as C
 from typing import Dict, Optional
 
-from ._lib import (MOE_STAGE_EVENTS, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,  # noqa: F401
-                   MOE_WS_PERMUTE, MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEECIO, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
+from ._lib import (MOE_STAGE_EVENTS, MOE_WS_BACKWARD, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN,  # noqa: F401
+                   MOE_WS_FORWARD, MOE_WS_PERMUTE, MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEECIO, MoEGrads,
+                   MoESaved, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
                    last_error, lib)
 
 SOFTMAX, SIGMOID = 0, 1
@@ -222,6 +223,18 @@ def moe_forward_expert_choice(cfg, weights: Dict, x, out, io: Optional[Dict], ws
                                           C.byref(ios) if ios is not None else None, p, n, _stream(stream)))
 
 
+def moe_backward(cfg, weights: Dict, x, dout, saved: Dict, aux_coef: float, z_coef: float, grads: Dict, ws,
+                 stream=None) -> None:
+    """Layer backward; ``saved`` keyed like ``MoESaved``, ``grads`` (fp32
+    output tensors) keyed like ``MoEGrads`` (missing keys: not computed)."""
+    p, n = _ws(ws)
+    wst = weights_struct(weights)
+    sv = MoESaved(**{k: _ptr(saved.get(k)) for k, _ in MoESaved._fields_})
+    gr = MoEGrads(**{k: _ptr(grads.get(k)) for k, _ in MoEGrads._fields_})
+    check(lib().moe_backward(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(dout), C.byref(sv), float(aux_coef),
+                             float(z_coef), C.byref(gr), p, n, _stream(stream)))
+
+
 def moe_check_device_error() -> int:
     code = C.c_int32(0)
     check(lib().moe_check_device_error(C.byref(code)))
@@ -349,6 +362,64 @@ class MoELayer(_HostPipeline):
 
     def stats(self) -> Dict:
         return stats_from_buffer(self.io["stats"])
+
+
+class TrainingLayer(MoELayer):
+    """A layer whose forward keeps what the backward needs (x_perm, the
+    first GEMM's pre-activations, H, the expert outputs) and whose backward
+    returns fp32 gradients of sum <dout, out> + aux_coef L_aux + z_coef L_z."""
+
+    def __init__(self, cfg: MoEConfig, weights: Dict, sel_bias=None, device="cuda"):
+        import torch
+        super().__init__(cfg, weights, sel_bias, device)
+        T, k, d, F = cfg.num_tokens, cfg.top_k, cfg.d_model, cfg.d_ff
+        nF = 2 * F if cfg.activation == SWIGLU else F
+        dt, dev = self.out_dtype(), self.device
+        R = max(T * k, 1)
+        self.io.update(x_perm=torch.empty(R, d, dtype=dt, device=dev),
+                       pre_act=torch.empty(R, nF, dtype=torch.bfloat16, device=dev),
+                       hidden=torch.empty(R, F, dtype=dt, device=dev),
+                       y_perm=torch.empty(R, d, dtype=torch.float32, device=dev))
+        if cfg.num_shared:
+            self.io.update(shared_pre_act=torch.empty(max(T, 1), nF, dtype=torch.bfloat16, device=dev),
+                           shared_hidden=torch.empty(max(T, 1), F, dtype=dt, device=dev))
+        self.bws = torch.empty(max(moe_workspace_size(cfg, MOE_WS_BACKWARD), 1), dtype=torch.uint8, device=dev)
+        self._x = None
+
+    def forward(self, x, out=None, stream=None, stage_events=None):
+        self._x = x
+        return super().forward(x, out, stream, stage_events)
+
+    def saved(self) -> Dict:
+        return {k: self.io.get(k) for k, _ in MoESaved._fields_}
+
+    def new_grads(self) -> Dict:
+        import torch
+        cfg, w = self.cfg, self.weights
+        T, d, E, F = cfg.num_tokens, cfg.d_model, cfg.num_experts, cfg.d_ff
+        f32 = dict(dtype=torch.float32, device=self.device)
+        g = dict(dx=torch.empty(max(T, 1), d, **f32), dw_router=torch.empty(E, d, **f32),
+                 dw1=torch.empty(E, F, d, **f32), dw2=torch.empty(E, d, F, **f32))
+        if w.get("b_router") is not None:
+            g["db_router"] = torch.empty(E, **f32)
+        if cfg.activation == SWIGLU:
+            g["dw3"] = torch.empty(E, F, d, **f32)
+        if w.get("b1") is not None:
+            g["db1"] = torch.empty(E, F, **f32)
+        if w.get("b2") is not None:
+            g["db2"] = torch.empty(E, d, **f32)
+        if cfg.num_shared:
+            g["shared_dw1"] = torch.empty(F, d, **f32)
+            g["shared_dw2"] = torch.empty(d, F, **f32)
+            if cfg.activation == SWIGLU:
+                g["shared_dw3"] = torch.empty(F, d, **f32)
+        return g
+
+    def backward(self, dout, aux_coef: float = 0.0, z_coef: float = 0.0, grads: Optional[Dict] = None,
+                 stream=None) -> Dict:
+        g = grads if grads is not None else self.new_grads()
+        moe_backward(self.cfg, self.weights, self._x, dout, self.saved(), aux_coef, z_coef, g, self.bws, stream)
+        return g
 
 
 class ExpertChoiceLayer(_HostPipeline):

@@ -16,7 +16,8 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_BAD_ALIGNMENT", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_DEVICE_TIMEOUT"}
-MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_SHARED_FFN, MOE_WS_EXPERT_CHOICE = range(6)
+(MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_SHARED_FFN, MOE_WS_EXPERT_CHOICE,
+ MOE_WS_BACKWARD) = range(7)
 
 
 class MoEConfig(C.Structure):
@@ -44,7 +45,18 @@ MOE_STAGE_EVENTS = 8
 class MoEForwardIO(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("logits", "topk_idx", "topk_w", "lse", "prob_mean",
                                           "counts", "kept", "offsets", "perm", "inv", "f", "stats",
-                                          "stage_events")]
+                                          "stage_events", "x_perm", "pre_act", "hidden", "y_perm",
+                                          "shared_pre_act", "shared_hidden")]
+
+
+class MoESaved(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("topk_idx", "topk_w", "logits", "inv", "offsets", "counts", "x_perm",
+                                          "pre_act", "hidden", "y_perm", "shared_pre_act", "shared_hidden")]
+
+
+class MoEGrads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("dx", "dw_router", "db_router", "dw1", "db1", "dw3", "dw2", "db2",
+                                          "shared_dw1", "shared_dw3", "shared_dw2")]
 
 
 class MoEECIO(C.Structure):
@@ -79,6 +91,7 @@ _SIGS = {
     "moe_forward_from_routing": ([P] * 7 + [P, C.c_size_t, P], C.c_int),
     "moe_route_hash": ([P] * 4 + [P], C.c_int),
     "moe_ec_capacity": ([P, C.POINTER(C.c_int64)], C.c_int),
+    "moe_backward": ([P] * 5 + [C.c_float, C.c_float, P, P, C.c_size_t, P], C.c_int),
     "moe_route_expert_choice": ([P] * 6 + [P], C.c_int),
     "moe_forward_expert_choice": ([P] * 5 + [P, C.c_size_t, P], C.c_int),
     "moe_check_device_error": ([C.POINTER(C.c_int32)], C.c_int),

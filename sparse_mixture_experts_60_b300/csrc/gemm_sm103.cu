@@ -254,6 +254,10 @@ struct Args {
     int act;
     int32_t *err;
     RouteEpilogue route;   // router GEMM with the routing epilogue
+    bf16 *pre;             // forward: pre-activations written (or null); backward: pre-activations read
+    int64_t ld_pre;
+    int kgroup;            // 1: groups split K (weight gradients), seg = per-group K offsets
+    int64_t out_group_stride;  // K-grouped: elements between the groups' outputs
 };
 
 struct Tile {
@@ -286,85 +290,190 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const in
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 
+// One 32-column chunk of a warp's 32 rows (thread = row) to global memory:
+// staged through the warp's 32-row x 64-byte shared buffer (16-byte units
+// XOR-swizzled by row, conflict-free both ways) and stored as row-contiguous
+// 64-byte segments: whole 32-byte sectors, 8 rows per warp store.  Rows
+// from row_end and columns from ncols (in 16-byte units) are not written.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_chunk(const float (&v)[32], void *out, int64_t ldo, int col, int ncols,
+                                            int row_base, int row_end, uint8_t *stg, int lane) {
+    // one or two passes of 64 B per row: 32 bf16, or 16 fp32 at a time
+    constexpr int PASSES = OUT_F32 ? 2 : 1;
+    constexpr int COLS = 32 / PASSES;                    // output columns per pass
+    uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 unit;
+            if (OUT_F32) {
+                const float *f = v + ps * 16 + 4 * j;
+                unit = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                                  __float_as_uint(f[3]));
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
+                    w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                unit = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            srow[j ^ ((lane >> 1) & 3)] = unit;
+        }
+        __syncwarp();
+        const int pcol = col + ps * COLS;
+        constexpr int UNIT_COLS = OUT_F32 ? 4 : 8;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int cidx = it * 32 + lane, r = cidx >> 2, cc = cidx & 3;
+            const uint4 val = reinterpret_cast<const uint4 *>(stg + r * 64)[cc ^ ((r >> 1) & 3)];
+            if (row_base + r < row_end && pcol + UNIT_COLS * cc < ncols) {
+                if (OUT_F32)
+                    reinterpret_cast<uint4 *>(static_cast<float *>(out) + (int64_t)(row_base + r) * ldo + pcol)[cc] = val;
+                else
+                    reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + (int64_t)(row_base + r) * ldo + pcol)[cc] = val;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// 32 bf16 of this thread's row (row < row_end) as fp32, else zeros.
+__device__ __forceinline__ void load_row32_bf16(const bf16 *base, int64_t ld, int row, int row_end, int col,
+                                                float (&v)[32]) {
+    if (row < row_end) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(base + (int64_t)row * ld + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 u = __ldg(p + q);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[8 * q + 2 * h] = __uint_as_float(w[h] << 16);
+                v[8 * q + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+}
+
+__device__ __forceinline__ float gelu_erf_grad(float a) {
+    return 0.5f * (1.0f + erff(a * 0.70710678118654752f)) + a * 0.39894228040143268f * expf(-0.5f * a * a);
+}
+
+// Tile of either kind of problem: M-grouped (rows of A split into groups,
+// decode_tile) or K-grouped (every group a full M x N output over its own
+// K range; tiles group-major, then N block, then M block).
+__device__ __forceinline__ Tile tile_of(const Args &args, int tile, const int *seg_s, const int *pre_s, int G,
+                                        int bn_out, int kg_tiles) {
+    if (!args.kgroup) return decode_tile(tile, seg_s, pre_s, G, bn_out);
+    const int mt = (args.M + BM - 1) / BM;
+    Tile t;
+    t.g = tile / kg_tiles;
+    const int local = tile - t.g * kg_tiles;
+    const int nb = local / mt, mb = local - nb * mt;
+    t.row0 = mb * BM;
+    t.seg_end = args.M;
+    t.n0 = nb * bn_out;
+    return t;
+}
+
+// Epilogue modes beyond the forward FFN: the activation backward of the
+// first expert GEMM, fused into the GEMM that produces dh = dy W2.
+constexpr int kEpiBwdGated = 100;   // SwiGLU: da1 = dh a3 silu'(a1), da3 = dh silu(a1)
+constexpr int kEpiBwdAct = 101;     // GELU / ReLU: da = dh act'(a)
+
 // Epilogue of one accumulator tile for one warp: rows row_base .. +31 (the
 // warp's TMEM lane quadrant q), alternate 32-column chunks starting at
-// 32 * half.  Shared by the single-CTA and the CTA-pair kernels.
-template <int BN, bool GATED, bool OUT_F32>
-__device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, int row_base, uint32_t tbase,
-                                      int half, int lane, uint8_t *stg) {
+// 32 * half.  `out` is this tile's output base (the group's, for K-grouped
+// problems); zero_acc: the tile had no K blocks, so its result is zero.
+// Shared by the single-CTA and the CTA-pair kernels.
+//   forward:  [bias], [pre-activations stored], activation or SwiGLU gating
+//   kEpiBwdGated / kEpiBwdAct: the activation backward from the stored
+//             pre-activations (args.pre), dh being the accumulator.
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0>
+__device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, void *out, int row_base,
+                                              uint32_t tbase, int half, int lane, uint8_t *stg, bool zero_acc) {
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
+    const int row = row_base + lane;
 #pragma unroll 1
     for (int c = 32 * half; c < BN_OUT; c += 64) {
         const int col = tl.n0 + c;
         float v[32];
-        if (GATED) {
-            float u[32];
-            tmem_ld32(tbase + c, v);
-            tmem_ld32(tbase + BN / 2 + c, u);
+        if (zero_acc) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
         } else {
             tmem_ld32(tbase + c, v);
-            if (args.bias && col + 32 <= args.N) {
-                const uint4 *bp = reinterpret_cast<const uint4 *>(args.bias + (int64_t)tl.g * args.bias_stride + col);
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const uint4 b = __ldg(bp + qq);
-                    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        v[qq * 8 + 2 * h] += __uint_as_float(w[h] << 16);
-                        v[qq * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
-                    }
-                }
-            }
-            if (args.act == 1) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-            } else if (args.act == 2) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
-            }
         }
-        // one or two passes of 64 B per row: 32 bf16, or 16 fp32 at a time
-        constexpr int PASSES = OUT_F32 ? 2 : 1;
-        constexpr int COLS = 32 / PASSES;                    // output columns per pass
-        uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
+        if constexpr (EPI == kEpiBwdGated) {
+            float a1[32], a3[32];
+            load_row32_bf16(args.pre, args.ld_pre, row, tl.seg_end, col, a1);
+            load_row32_bf16(args.pre, args.ld_pre, row, tl.seg_end, args.N + col, a3);
 #pragma unroll
-        for (int ps = 0; ps < PASSES; ++ps) {
+            for (int i = 0; i < 32; ++i) {
+                const float sg = 1.0f / (1.0f + expf(-a1[i]));
+                const float dh = v[i];
+                v[i] = dh * a3[i] * (sg * (1.0f + a1[i] * (1.0f - sg)));   // da1
+                a3[i] = dh * a1[i] * sg;                                    // da3 = dh silu(a1)
+            }
+            store_chunk<false>(v, out, args.ldo, col, args.N, row_base, tl.seg_end, stg, lane);
+            store_chunk<false>(a3, out, args.ldo, args.N + col, 2 * args.N, row_base, tl.seg_end, stg, lane);
+            continue;
+        } else if constexpr (EPI == kEpiBwdAct) {
+            float a[32];
+            load_row32_bf16(args.pre, args.ld_pre, row, tl.seg_end, col, a);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint4 unit;
-                if (OUT_F32) {
-                    const float *f = v + ps * 16 + 4 * j;
-                    unit = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                                      __float_as_uint(f[3]));
+            for (int i = 0; i < 32; ++i)
+                v[i] = args.act == 1 ? v[i] * gelu_erf_grad(a[i]) : (a[i] > 0.0f ? v[i] : 0.0f);
+            store_chunk<false>(v, out, args.ldo, col, args.N, row_base, tl.seg_end, stg, lane);
+            continue;
+        } else {
+            if (GATED) {
+                float u[32];
+                if (zero_acc) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u[i] = 0.0f;
                 } else {
-                    uint32_t w[4];
+                    tmem_ld32(tbase + BN / 2 + c, u);
+                }
+                if (args.pre) {   // training forward: a1 | a3 kept for the backward
+                    store_chunk<false>(v, args.pre, args.ld_pre, col, args.N, row_base, tl.seg_end, stg, lane);
+                    store_chunk<false>(u, args.pre, args.ld_pre, args.N + col, 2 * args.N, row_base, tl.seg_end,
+                                       stg, lane);
+                }
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
-                        w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
+            } else {
+                if (args.bias && col + 32 <= args.N) {
+                    const uint4 *bp =
+                        reinterpret_cast<const uint4 *>(args.bias + (int64_t)tl.g * args.bias_stride + col);
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const uint4 b = __ldg(bp + qq);
+                        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            v[qq * 8 + 2 * h] += __uint_as_float(w[h] << 16);
+                            v[qq * 8 + 2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                        }
                     }
-                    unit = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                srow[j ^ ((lane >> 1) & 3)] = unit;
-            }
-            __syncwarp();
-            const int pcol = col + ps * COLS;
-            constexpr int UNIT_COLS = OUT_F32 ? 4 : 8;
+                if (args.pre && args.act != 0)   // training forward: the pre-activation a
+                    store_chunk<false>(v, args.pre, args.ld_pre, col, args.N, row_base, tl.seg_end, stg, lane);
+                if (args.act == 1) {
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int cidx = it * 32 + lane, r = cidx >> 2, cc = cidx & 3;
-                const uint4 val = reinterpret_cast<const uint4 *>(stg + r * 64)[cc ^ ((r >> 1) & 3)];
-                if (row_base + r < tl.seg_end && pcol + UNIT_COLS * cc < args.N) {
-                    if (OUT_F32)
-                        reinterpret_cast<uint4 *>(static_cast<float *>(args.out) + (int64_t)(row_base + r) * args.ldo + pcol)[cc] = val;
-                    else
-                        reinterpret_cast<uint4 *>(static_cast<bf16 *>(args.out) + (int64_t)(row_base + r) * args.ldo + pcol)[cc] = val;
+                    for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                } else if (args.act == 2) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
                 }
             }
-            __syncwarp();
+            store_chunk<OUT_F32>(v, out, args.ldo, col, args.N, row_base, tl.seg_end, stg, lane);
         }
     }
 }
@@ -421,7 +530,9 @@ __device__ __forceinline__ void route_epilogue(const Args &args, const Tile &tl,
     if (lane == 0 && re.part_z) re.part_z[blk] = z;
 }
 
-template <int BN, bool GATED, bool OUT_F32, int ROUTE_EP = 0>
+// EPI: 0 forward FFN epilogue; 8 / 16 / 32 routing epilogue (router GEMM,
+// E <= EPI); kEpiBwdGated / kEpiBwdAct activation backward.
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const Args args) {
@@ -472,19 +583,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i <= G; i += kThreads)
         seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
-    // tile prefix over groups: n_tiles * ceil(rows_g / BM)
+    // tile prefix over groups: n_tiles * ceil(rows_g / BM); K-grouped: every
+    // group has ceil(M / BM) * n_tiles tiles, and its K offsets must be
+    // multiples of BK (whole, 16-byte aligned TMA boxes) inside K
     const int n_tiles = (args.N + BN_OUT - 1) / BN_OUT;
+    const int kg_tiles = ((args.M + BM - 1) / BM) * n_tiles;
     volatile int *seg_bad = consumed + 1;
     if (warp == 0) {
         int carry = 0;
-        bool bad = seg_s[0] < 0 || (int64_t)seg_s[G] > args.a_rows;
+        bool bad = seg_s[0] < 0 || (int64_t)seg_s[G] > (args.kgroup ? (int64_t)args.K : args.a_rows);
         for (int b = 0; b < G; b += 32) {
             const int g = b + lane;
             int v = 0;
             if (g < G) {
                 const int rows = seg_s[g + 1] - seg_s[g];
                 bad |= rows < 0;
-                v = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+                if (args.kgroup) {
+                    bad |= (seg_s[g] % BK) != 0 || (seg_s[g + 1] % BK) != 0;
+                    v = kg_tiles;
+                } else {
+                    v = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
+                }
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -515,10 +634,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t ph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile tl = decode_tile(tile, seg_s, pre_s, G, BN_OUT);
-            const int brow = tl.g * args.b_group_rows + tl.n0;
+            const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
+            const int brow = args.kgroup ? tl.n0 : tl.g * args.b_group_rows + tl.n0;
+            const int kb0 = args.kgroup ? seg_s[tl.g] / BK : 0;
+            const int kb1 = args.kgroup ? seg_s[tl.g + 1] / BK : num_kb;
             bool ok = true;
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, args.err)) {
                     ok = false;
                     break;
@@ -550,7 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < num_kb; ++kb) {
+            int kb0 = 0, kb1 = num_kb;
+            if (args.kgroup) {
+                const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
+                kb0 = seg_s[tl.g] / BK;
+                kb1 = seg_s[tl.g + 1] / BK;
+            }
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(&full[stage], ph, abort_flag, args.err)) {
                     ok = false;
                     break;
@@ -563,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                     // +32 bytes per K step inside the swizzle atom (encoded >> 4)
                     umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
-                              (kb > 0 || kk > 0) ? 1u : 0u);
+                              (kb > kb0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty[stage]);
                 if (++stage == STAGES) {
@@ -589,16 +716,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile tl = decode_tile(tile, seg_s, pre_s, G, BN_OUT);
+            const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
             // tcgen05.ld below is warp-collective: leave only as a whole warp
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag, args.err))) break;
             tc_fence_after();
             const int row_base = tl.row0 + q * 32;          // first row of this warp's 32
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if constexpr (ROUTE_EP > 0) {
-                if (half == 0) route_epilogue<ROUTE_EP>(args, tl, row_base, tbase, lane);
+            if constexpr (EPI > 0 && EPI <= 32) {
+                if (half == 0) route_epilogue<EPI>(args, tl, row_base, tbase, lane);
             } else {
-                epilogue_tile<BN, GATED, OUT_F32>(args, tl, row_base, tbase, half, lane, stg);
+                void *out = args.out;
+                bool zero_acc = false;
+                if (args.kgroup) {
+                    out = static_cast<uint8_t *>(args.out) +
+                          tl.g * args.out_group_stride * (int64_t)(OUT_F32 ? 4 : 2);
+                    zero_acc = seg_s[tl.g + 1] == seg_s[tl.g];
+                }
+                epilogue_tile<BN, GATED, OUT_F32, EPI>(args, tl, out, row_base, tbase, half, lane, stg, zero_acc);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -901,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int row_base = tl.row0 + BM * (int)rank + q * 32;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN, GATED, OUT_F32>(args, tl, row_base, tbase, half, lane, stg);
+            epilogue_tile<BN, GATED, OUT_F32>(args, tl, args.out, row_base, tbase, half, lane, stg, false);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
@@ -961,7 +1095,7 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool GATED, bool OUT_F32, int ROUTE_EP = 0>
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0>
 cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     using C = Cfg<BN>;
     constexpr int BN_B = GATED ? BN / 2 : BN;   // rows per TMA box of B
@@ -973,7 +1107,7 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     } else {
         tb2 = tb;
     }
-    Args a;
+    Args a{};
     a.seg = p.seg;
     a.a_rows = p.a_rows;
     a.G = p.seg ? p.G : 1;
@@ -989,8 +1123,12 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     a.err = device_error_flag();
     if (!a.err) return cudaErrorUnknown;
     a.route = p.route ? *p.route : RouteEpilogue{};
+    a.pre = p.pre;
+    a.ld_pre = p.ld_pre;
+    a.kgroup = p.kgroup;
+    a.out_group_stride = p.out_group_stride;
     const size_t smem = C::smem_bytes(a.G);
-    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, ROUTE_EP>;
+    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, s, ta, tb, tb2, a);
@@ -1008,7 +1146,7 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     } else {
         tb2 = tb;
     }
-    Args a;
+    Args a{};
     a.seg = p.seg;
     a.a_rows = p.a_rows;
     a.G = p.seg ? p.G : 1;
@@ -1073,6 +1211,17 @@ bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias) 
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
     if (!grouped_gemm_supported(p.N, p.K, p.gated, p.out_f32, p.bias != nullptr)) return cudaErrorInvalidValue;
+    if (p.epi_bwd) {
+        // dh = dy W2 with the activation backward in the epilogue (bf16 da out)
+        if (p.out_f32 || p.gated || p.kgroup || !p.pre || p.bias) return cudaErrorInvalidValue;
+        return p.epi_bwd == 1 ? launch_t<256, false, false, kEpiBwdGated>(p, s)
+                              : launch_t<256, false, false, kEpiBwdAct>(p, s);
+    }
+    if (p.kgroup) {
+        // weight gradients: fp32 out, one full M x N output per group
+        if (p.gated || !p.out_f32 || p.bias || !p.seg) return cudaErrorInvalidValue;
+        return launch_t<256, false, true>(p, s);
+    }
     if (p.route) {
         if (p.N > 32 || p.gated || !p.out_f32 || p.seg || p.bias) return cudaErrorInvalidValue;
         if (p.N <= 8) return launch_t<32, false, true, 8>(p, s);

@@ -126,6 +126,40 @@ size_t ec_ws(const moe_config_t *c) {
     return n;
 }
 
+// Backward workspace: R = T k expert rows; every expert's rows padded to a
+// multiple of 64 in the packed transposes (Rp columns), the shared expert's
+// T tokens to Tp.
+struct BwdDims {
+    int64_t T, d, E, k, F, nF, R, Rp, Tp;
+};
+BwdDims bwd_dims(const moe_config_t *c) {
+    BwdDims b;
+    b.T = c->num_tokens;
+    b.d = c->d_model;
+    b.E = c->num_experts;
+    b.k = c->top_k;
+    b.F = c->d_ff;
+    b.nF = c->activation == MOE_ACT_SWIGLU ? 2 * b.F : b.F;
+    b.R = b.T * b.k;
+    b.Rp = (b.R + 64 * b.E + 63) / 64 * 64;
+    b.Tp = (b.T + 63) / 64 * 64;
+    return b;
+}
+size_t bwd_ws(const moe_config_t *c) {
+    const BwdDims b = bwd_dims(c);
+    size_t n = align256(b.R * b.d * 2) + align256(b.T * b.k * 4) + align256(b.T * b.E * 4) +
+               align256((b.E + 1) * 4) + align256(2 * 4);
+    n += align256(b.E * b.F * b.d * 2) + align256(b.E * b.d * b.nF * 2);      // W2^T, [W1 | W3]^T
+    n += align256(b.R * b.nF * 2) + align256(b.R * b.d * 4);                  // da, dx_perm
+    n += 2 * align256(b.d * b.Rp * 2) + align256(b.F * b.Rp * 2) + align256(b.nF * b.Rp * 2);
+    n += align256((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
+    if (c->num_shared) {
+        n += align256(b.T * b.nF * 2) + align256(b.T * b.d * 4) + align256(b.F * b.d * 2) + align256(b.d * b.nF * 2);
+        n += 2 * align256(b.d * b.Tp * 2) + align256(b.F * b.Tp * 2) + align256(b.nF * b.Tp * 2);
+    }
+    return n;
+}
+
 // ------------------------------------------------------------------ step bodies (no validation)
 // logits [T,E] = x w_r^T + b_router (tensor cores for bf16 where the GEMM takes the shape)
 moe_status_t router_logits_impl(const moe_config_t *c, const void *x, const void *w_router, const float *b_router,
@@ -317,7 +351,7 @@ moe_status_t permute_impl(const moe_config_t *c, const void *x, const int32_t *t
 // Two-layer FFN over row groups (routed: seg = offsets, G = E; shared: seg = null).
 moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, const int32_t *seg, int G, int M,
                       const void *w1, const void *b1, const void *w3, const void *w2, const void *b2, void *H,
-                      float *y, cudaStream_t s, void *mid_event = nullptr) {
+                      float *y, cudaStream_t s, void *mid_event = nullptr, void *pre = nullptr) {
     const int d = c->d_model, F = c->d_ff;
     const int gated = c->activation == MOE_ACT_SWIGLU;
     const int act = c->activation == MOE_ACT_GELU ? 1 : (c->activation == MOE_ACT_RELU ? 2 : 0);
@@ -343,6 +377,8 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
         g1.bias_stride = F;
         g1.act = act;
         g1.gated = gated;
+        g1.pre = static_cast<bf16 *>(pre);
+        g1.ld_pre = gated ? 2 * (int64_t)F : F;
         e = launch_grouped_gemm(g1, s);
         if (e != cudaSuccess) return cuda_status(e, "expert FFN1 launch");
         if (mid_event) cudaEventRecord(static_cast<cudaEvent_t>(mid_event), s);
@@ -367,6 +403,7 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
         e = launch_grouped_gemm(g2, s);
         return cuda_status(e, "expert FFN2 launch");
     }
+    if (pre) return fail(MOE_ERR_UNSUPPORTED, "training members (pre-activations) need a bf16 layer");
     SimtProblem p1{};
     p1.A = static_cast<const float *>(A);
     p1.B = static_cast<const float *>(w1);
@@ -469,6 +506,7 @@ moe_status_t moe_workspace_size(const moe_config_t *cfg, int32_t which, size_t *
         case MOE_WS_EXPERT_FFN: *bytes = ffn_ws(cfg); return MOE_OK;
         case MOE_WS_SHARED_FFN: *bytes = shared_ws(cfg); return MOE_OK;
         case MOE_WS_EXPERT_CHOICE: TRY(check_ec(cfg)); *bytes = ec_ws(cfg); return MOE_OK;
+        case MOE_WS_BACKWARD: *bytes = bwd_ws(cfg); return MOE_OK;
         default: return fail(MOE_ERR_INVALID_ARG, "unknown workspace kind %d", which);
     }
 }
@@ -703,6 +741,10 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
     if (!o.f) o.f = f_ws;
     if (!o.offsets) o.offsets = off_ws;
     if (!o.stats) o.stats = st_ws;
+    if (o.x_perm) x_perm = o.x_perm;
+    if (o.hidden) ws_ffn = o.hidden;
+    if (o.y_perm) y_perm = o.y_perm;
+    if (o.shared_hidden) ws_shared = o.shared_hidden;
 
     void *const *ev = o.stage_events;
     auto mark = [&](int i) {
@@ -722,11 +764,11 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
     TRY(permute_impl(c, x, o.topk_idx, o.counts, o.kept, o.offsets, o.perm, o.inv, x_perm, ws_perm, s));
     mark(2);
     TRY(ffn_impl(c, x_perm, (int64_t)S, o.offsets, c->num_experts, 0, w->w1, w->b1, w->w3, w->w2, w->b2, ws_ffn,
-                 y_perm, s, ev ? ev[3] : nullptr));
+                 y_perm, s, ev ? ev[3] : nullptr, o.pre_act));
     mark(4);
     if (c->num_shared)
         TRY(ffn_impl(c, x, (int64_t)T, nullptr, 1, (int)T, w->shared_w1, nullptr, w->shared_w3, w->shared_w2,
-                     nullptr, ws_shared, z, s));
+                     nullptr, ws_shared, z, s, nullptr, o.shared_pre_act));
     mark(5);
     TRY(cuda_status(launch_combine(c->num_tokens, c->d_model, c->top_k, c->dtype, y_perm, o.inv, o.topk_w, z,
                                    c->residual ? x : nullptr, out, s),
@@ -752,6 +794,155 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
     sp.stats = o.stats;
     TRY(cuda_status(launch_stats(sp, s), "stats launch"));
     mark(7);
+    return MOE_OK;
+}
+
+// K-grouped weight-gradient GEMM: out[g] (M x N, fp32) = A[:, K_g] B[:, K_g]^T
+// with A [M, Kp], B [N, Kp] bf16 K-major and K_g = pad[g] .. pad[g+1]-1.
+moe_status_t wgrad_gemm(const bf16 *A, int M, const bf16 *B, int N, int64_t Kp, const int32_t *pad, int G,
+                        float *out, cudaStream_t s) {
+    GemmProblem g{};
+    g.A = A;
+    g.a_rows = M;
+    g.B = B;
+    g.b_rows_total = N;
+    g.b_group_rows = 0;
+    g.seg = pad;
+    g.G = G;
+    g.M = M;
+    g.N = N;
+    g.K = (int)Kp;
+    g.out = out;
+    g.ldo = N;
+    g.out_f32 = 1;
+    g.kgroup = 1;
+    g.out_group_stride = (int64_t)M * N;
+    return cuda_status(launch_grouped_gemm(g, s), "weight-gradient GEMM launch");
+}
+
+// M-grouped data-gradient GEMM: out rows of group g = A rows x B_g^T.
+moe_status_t dgrad_gemm(const bf16 *A, int64_t a_rows, const int32_t *seg, int G, int M, const bf16 *B,
+                        int b_group_rows, int N, int K, void *out, int out_f32, int64_t ldo, bf16 *pre,
+                        int64_t ld_pre, int epi_bwd, int act, cudaStream_t s) {
+    GemmProblem g{};
+    g.A = A;
+    g.a_rows = a_rows;
+    g.B = B;
+    g.b_rows_total = (int64_t)G * b_group_rows;
+    g.b_group_rows = b_group_rows;
+    g.seg = seg;
+    g.G = G;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.out = out;
+    g.ldo = ldo;
+    g.out_f32 = out_f32;
+    g.pre = pre;
+    g.ld_pre = ld_pre;
+    g.epi_bwd = epi_bwd;
+    g.act = act;
+    return cuda_status(launch_grouped_gemm(g, s), "data-gradient GEMM launch");
+}
+
+moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const void *x, const void *dout,
+                           const moe_saved_t *sv, float aux_coef, float z_coef, const moe_grads_t *gr, void *ws,
+                           cudaStream_t s) {
+    const BwdDims b = bwd_dims(c);
+    const bool gated = c->activation == MOE_ACT_SWIGLU;
+    const int act = c->activation == MOE_ACT_GELU ? 1 : (c->activation == MOE_ACT_RELU ? 2 : 0);
+    const int epi = gated ? 1 : 2;
+    const int E = (int)b.E, d = (int)b.d, F = (int)b.F, nF = (int)b.nF;
+    Carve cv{static_cast<uint8_t *>(ws)};
+    bf16 *dy = cv.take<bf16>(b.R * b.d * 2);
+    float *dgate = cv.take<float>(b.T * b.k * 4);
+    float *dl = cv.take<float>(b.T * b.E * 4);
+    int32_t *pad = cv.take<int32_t>((b.E + 1) * 4);
+    int32_t *pad1 = cv.take<int32_t>(2 * 4);
+    bf16 *w2t = cv.take<bf16>(b.E * b.F * b.d * 2);
+    bf16 *w13t = cv.take<bf16>(b.E * b.d * b.nF * 2);
+    bf16 *da = cv.take<bf16>(b.R * b.nF * 2);
+    float *dxp = cv.take<float>(b.R * b.d * 4);
+    bf16 *dyT = cv.take<bf16>(b.d * b.Rp * 2);
+    bf16 *xpT = cv.take<bf16>(b.d * b.Rp * 2);
+    bf16 *hT = cv.take<bf16>(b.F * b.Rp * 2);
+    bf16 *daT = cv.take<bf16>(b.nF * b.Rp * 2);
+    float *rwpart = cv.take<float>((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
+    const bf16 *W1 = static_cast<const bf16 *>(w->w1), *W3 = static_cast<const bf16 *>(w->w3);
+    const bf16 *W2 = static_cast<const bf16 *>(w->w2);
+    const bf16 *go = static_cast<const bf16 *>(dout);
+    cudaError_t e;
+#define CU(call, what) TRY(cuda_status((call), what))
+    // combine and router backward
+    CU(launch_combine_bwd(b.T, d, (int)b.k, go, sv->topk_w, sv->inv, sv->y_perm, dy, dgate, s), "combine backward");
+    CU(launch_router_bwd(b.T, E, (int)b.k, c->score_fn, c->renormalize, sv->logits, sv->topk_idx, dgate, sv->counts,
+                         aux_coef, z_coef, dl, s),
+       "router backward");
+    // weights to the K-major layouts of the data-gradient GEMMs
+    CU(launch_transpose_batched(W2, (int64_t)d * F, F, d, F, E, w2t, (int64_t)F * d, d, 0, s), "W2 transpose");
+    CU(launch_transpose_batched(W1, (int64_t)F * d, d, F, d, E, w13t, (int64_t)d * nF, nF, 0, s), "W1 transpose");
+    if (gated)
+        CU(launch_transpose_batched(W3, (int64_t)F * d, d, F, d, E, w13t, (int64_t)d * nF, nF, F, s), "W3 transpose");
+    // dh = dy W2 -> da (activation backward in the epilogue); dx_perm = da [W1 | W3]
+    TRY(dgrad_gemm(dy, b.R, sv->offsets, E, 0, w2t, F, F, d, da, 0, nF,
+                   const_cast<bf16 *>(static_cast<const bf16 *>(sv->pre_act)), nF, epi, act, s));
+    TRY(dgrad_gemm(da, b.R, sv->offsets, E, 0, w13t, d, d, nF, dxp, 1, d, nullptr, 0, 0, 0, s));
+    // shared expert: gate 1, A = dout
+    float *dxs = nullptr;
+    bf16 *das = nullptr;
+    if (c->num_shared) {
+        das = cv.take<bf16>(b.T * b.nF * 2);
+        dxs = cv.take<float>(b.T * b.d * 4);
+        bf16 *w2st = cv.take<bf16>(b.F * b.d * 2);
+        bf16 *w13st = cv.take<bf16>(b.d * b.nF * 2);
+        CU(launch_transpose_batched(static_cast<const bf16 *>(w->shared_w2), 0, F, d, F, 1, w2st, 0, d, 0, s),
+           "shared W2 transpose");
+        CU(launch_transpose_batched(static_cast<const bf16 *>(w->shared_w1), 0, d, F, d, 1, w13st, 0, nF, 0, s),
+           "shared W1 transpose");
+        if (gated)
+            CU(launch_transpose_batched(static_cast<const bf16 *>(w->shared_w3), 0, d, F, d, 1, w13st, 0, nF, F, s),
+               "shared W3 transpose");
+        TRY(dgrad_gemm(go, b.T, nullptr, 1, (int)b.T, w2st, F, F, d, das, 0, nF,
+                       const_cast<bf16 *>(static_cast<const bf16 *>(sv->shared_pre_act)), nF, epi, act, s));
+        TRY(dgrad_gemm(das, b.T, nullptr, 1, (int)b.T, w13st, d, d, nF, dxs, 1, d, nullptr, 0, 0, 0, s));
+    }
+    CU(launch_dx_assemble(b.T, d, (int)b.k, E, dxp, sv->inv, go, c->residual, dxs, dl,
+                          static_cast<const bf16 *>(w->w_router), gr->dx, s),
+       "dx assembly");
+    // weight gradients over the experts' rows, packed K-major and padded
+    CU(launch_pad_offsets(sv->offsets, E, 0, pad, s), "padded offsets");
+    CU(launch_transpose_pack(dy, d, d, sv->offsets, pad, E, 0, b.Rp, dyT, s), "dy pack");
+    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->x_perm), d, d, sv->offsets, pad, E, 0, b.Rp, xpT, s),
+       "x_perm pack");
+    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->hidden), F, F, sv->offsets, pad, E, 0, b.Rp, hT, s),
+       "H pack");
+    CU(launch_transpose_pack(da, nF, nF, sv->offsets, pad, E, 0, b.Rp, daT, s), "da pack");
+    if (gr->dw2) TRY(wgrad_gemm(dyT, d, hT, F, b.Rp, pad, E, gr->dw2, s));
+    if (gr->dw1) TRY(wgrad_gemm(daT, F, xpT, d, b.Rp, pad, E, gr->dw1, s));
+    if (gated && gr->dw3) TRY(wgrad_gemm(daT + b.F * b.Rp, F, xpT, d, b.Rp, pad, E, gr->dw3, s));
+    if (!gated && gr->db1) CU(launch_group_rowsum(daT, b.Rp, pad, E, F, gr->db1, s), "db1");
+    if (!gated && gr->db2) CU(launch_group_rowsum(dyT, b.Rp, pad, E, d, gr->db2, s), "db2");
+    CU(launch_router_wgrad(b.T, d, E, dl, static_cast<const bf16 *>(x), rwpart, gr->dw_router, gr->db_router, s),
+       "router weight gradient");
+    if (c->num_shared && (gr->shared_dw1 || gr->shared_dw2 || gr->shared_dw3)) {
+        bf16 *goT = cv.take<bf16>(b.d * b.Tp * 2);
+        bf16 *xT = cv.take<bf16>(b.d * b.Tp * 2);
+        bf16 *shT = cv.take<bf16>(b.F * b.Tp * 2);
+        bf16 *dasT = cv.take<bf16>(b.nF * b.Tp * 2);
+        const int Ti = (int)b.T;
+        CU(launch_pad_offsets(nullptr, 1, Ti, pad1, s), "shared padded offsets");
+        CU(launch_transpose_pack(go, d, d, nullptr, pad1, 1, Ti, b.Tp, goT, s), "dout pack");
+        CU(launch_transpose_pack(static_cast<const bf16 *>(x), d, d, nullptr, pad1, 1, Ti, b.Tp, xT, s), "x pack");
+        CU(launch_transpose_pack(static_cast<const bf16 *>(sv->shared_hidden), F, F, nullptr, pad1, 1, Ti, b.Tp, shT,
+                                 s),
+           "shared H pack");
+        CU(launch_transpose_pack(das, nF, nF, nullptr, pad1, 1, Ti, b.Tp, dasT, s), "shared da pack");
+        if (gr->shared_dw2) TRY(wgrad_gemm(goT, d, shT, F, b.Tp, pad1, 1, gr->shared_dw2, s));
+        if (gr->shared_dw1) TRY(wgrad_gemm(dasT, F, xT, d, b.Tp, pad1, 1, gr->shared_dw1, s));
+        if (gated && gr->shared_dw3) TRY(wgrad_gemm(dasT + b.F * b.Tp, F, xT, d, b.Tp, pad1, 1, gr->shared_dw3, s));
+    }
+#undef CU
+    (void)e;
     return MOE_OK;
 }
 
@@ -784,6 +975,54 @@ moe_status_t moe_route_hash(const moe_config_t *cfg, const int32_t *token_ids, i
     return cuda_status(launch_route_hash(T, cfg->num_experts, cfg->top_k, token_ids, topk_idx, topk_w,
                                          static_cast<cudaStream_t>(stream)),
                        "moe_route_hash launch");
+}
+
+moe_status_t moe_backward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x, const void *dout,
+                          const moe_saved_t *saved, float aux_coef, float z_coef, const moe_grads_t *grads,
+                          void *ws, size_t ws_bytes, moe_stream_t stream) {
+    TRY(check_cfg(cfg));
+    if (cfg->dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_UNSUPPORTED, "moe_backward needs a bf16 layer");
+    if (!isfinite(aux_coef) || !isfinite(z_coef)) return fail(MOE_ERR_INVALID_ARG, "coefficients must be finite");
+    TRY(need(weights, "weights"));
+    TRY(need(saved, "saved"));
+    TRY(need(grads, "grads"));
+    const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
+    const bool gated = cfg->activation == MOE_ACT_SWIGLU;
+    TRY(need16(x, "x", T));
+    TRY(need16(dout, "dout", T));
+    TRY(need16(weights->w_router, "w_router"));
+    TRY(check_weights_ffn(cfg, weights->w1, weights->w3, weights->w2));
+    if (cfg->num_shared) TRY(check_weights_ffn(cfg, weights->shared_w1, weights->shared_w3, weights->shared_w2));
+    TRY(need(saved->topk_idx, "saved topk_idx", S));
+    TRY(need(saved->topk_w, "saved topk_w", S));
+    TRY(need(saved->logits, "saved logits", T));
+    TRY(need(saved->inv, "saved inv", S));
+    TRY(need(saved->offsets, "saved offsets"));
+    TRY(need(saved->counts, "saved counts"));
+    TRY(need16(saved->x_perm, "saved x_perm", S));
+    TRY(need16(saved->pre_act, "saved pre_act", S));
+    TRY(need16(saved->hidden, "saved hidden", S));
+    TRY(need16(saved->y_perm, "saved y_perm", S));
+    if (cfg->num_shared) {
+        TRY(need16(saved->shared_pre_act, "saved shared_pre_act", T));
+        TRY(need16(saved->shared_hidden, "saved shared_hidden", T));
+    }
+    TRY(need16(grads->dx, "grads dx", T));
+    if (!gated && grads->dw3) return fail(MOE_ERR_INVALID_ARG, "grads dw3 given for a layer without W3");
+    TRY(need_ws(ws, ws_bytes, bwd_ws(cfg)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // no tokens: every weight gradient is zero
+        const size_t E = cfg->num_experts, d = cfg->d_model, F = cfg->d_ff;
+        struct { float *p; size_t n; } z[] = {
+            {grads->dw_router, E * d}, {grads->db_router, E}, {grads->dw1, E * F * d}, {grads->db1, E * F},
+            {grads->dw3, E * F * d}, {grads->dw2, E * d * F}, {grads->db2, E * d}, {grads->shared_dw1, F * d},
+            {grads->shared_dw3, F * d}, {grads->shared_dw2, d * F}};
+        for (auto &q : z)
+            if (q.p) TRY(cuda_status(cudaMemsetAsync(q.p, 0, q.n * sizeof(float), s), "zero gradients"));
+        return MOE_OK;
+    }
+    return backward_impl(cfg, weights, x, dout, saved, aux_coef, z_coef, grads, ws, s);
 }
 
 moe_status_t moe_ec_capacity(const moe_config_t *cfg, int64_t *capacity) {

@@ -132,6 +132,8 @@ cudaError_t launch_add_bias(float *logits, const float *b, int64_t T, int E, cud
 
 // ----------------------------------------------------------------- experts
 // Grouped GEMM with fused epilogue on the tensor cores (bf16 in, fp32 acc).
+// M-grouped (expert FFNs: rows of A in groups, B per group) or K-grouped
+// (weight gradients: the groups split K).
 //   out[r, n] = epi( sum_k A[r, k] * B[g*b_rows + n, k] )   for rows r of group g
 // gated: B2 is the second weight; epi = silu(acc1) * acc2.
 // act: 0 none, 1 GELU, 2 ReLU.  out is bf16 (out_f32 = 0) or fp32.
@@ -159,6 +161,13 @@ struct GemmProblem {
     const bf16 *bias; int64_t bias_stride;   // per group, or null
     int act; int gated;
     const RouteEpilogue *route;              // router GEMM with the routing epilogue, or null
+    // training forward: pre-activations stored (gated: [rows, 2N] a1 | a3,
+    // else [rows, N] a); activation backward (epi_bwd 1 SwiGLU, 2 GELU /
+    // ReLU by act): pre-activations read, out = da ([rows, 2N] for SwiGLU)
+    bf16 *pre; int64_t ld_pre; int epi_bwd;
+    // K-grouped (weight gradients): A [M, K], B [N, K]; group g sums over
+    // K columns seg[g] .. seg[g+1]-1 (multiples of 64) into out + g * out_group_stride
+    int kgroup; int64_t out_group_stride;
 };
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
 bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias);
@@ -188,5 +197,27 @@ struct StatsParams {
 cudaError_t launch_stats(const StatsParams &p, cudaStream_t s);
 cudaError_t launch_bias_update(int64_t T, int E, int k, const int32_t *counts, float *bias,
                                float gamma, cudaStream_t s);
+
+// ----------------------------------------------------------------- backward
+cudaError_t launch_combine_bwd(int64_t T, int d, int k, const bf16 *dout, const float *topk_w, const int32_t *inv,
+                               const float *y, bf16 *dy, float *dgate, cudaStream_t s);
+cudaError_t launch_router_bwd(int64_t T, int E, int k, int score_fn, int renormalize, const float *logits,
+                              const int32_t *topk_idx, const float *dgate, const int32_t *counts, float aux_coef,
+                              float z_coef, float *dl, cudaStream_t s);
+cudaError_t launch_dx_assemble(int64_t T, int d, int k, int E, const float *dx_perm, const int32_t *inv,
+                               const bf16 *dout, int residual, const float *dxs, const float *dl,
+                               const bf16 *w_router, float *dx, cudaStream_t s);
+int64_t router_wgrad_chunks(int64_t T);   // partial buffer: chunks * E * d floats
+cudaError_t launch_router_wgrad(int64_t T, int d, int E, const float *dl, const bf16 *x, float *part, float *dw,
+                                float *db, cudaStream_t s);
+// out[b][c][out_col0 + r] = in[b][r][c]
+cudaError_t launch_transpose_batched(const bf16 *in, int64_t in_batch, int ld_in, int rows, int cols, int batch,
+                                     bf16 *out, int64_t out_batch, int ld_out, int out_col0, cudaStream_t s);
+// out[c][pad[g] + i] = in[off[g] + i][c] (zero padding); out [cols, max_padded]
+cudaError_t launch_transpose_pack(const bf16 *in, int ld_in, int cols, const int32_t *off, const int32_t *pad, int G,
+                                  int rows, int64_t max_padded, bf16 *out, cudaStream_t s);
+cudaError_t launch_pad_offsets(const int32_t *off, int G, int rows, int32_t *pad, cudaStream_t s);
+cudaError_t launch_group_rowsum(const bf16 *in_t, int64_t ld, const int32_t *pad, int G, int C, float *out,
+                                cudaStream_t s);
 
 }  // namespace moe

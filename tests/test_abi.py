@@ -44,12 +44,28 @@ def test_library_does_not_link_the_driver():
     assert "libcuda.so" not in out
 
 
-def test_struct_layouts_match_header():
-    # moe_config_t: int64 + 12 int32 + float = 64 bytes with tail padding
-    assert C.sizeof(_lib.MoEConfig) == 64
-    assert C.sizeof(_lib.MoEStats) == 32
-    assert C.sizeof(_lib.MoEWeights) == 80
-    assert C.sizeof(_lib.MoEForwardIO) == 104
+def test_struct_layouts_match_header(tmp_path):
+    """sizeof and field offsets of every ABI struct, from the header compiled
+    by the host C compiler, equal the ctypes mirrors of the binding."""
+    structs = {"moe_config_t": _lib.MoEConfig, "moe_stats_t": _lib.MoEStats, "moe_weights_t": _lib.MoEWeights,
+               "moe_forward_io_t": _lib.MoEForwardIO, "moe_ec_io_t": _lib.MoEECIO, "moe_saved_t": _lib.MoESaved,
+               "moe_grads_t": _lib.MoEGrads}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe_b300.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname}.{fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    for cname, py in structs.items():
+        assert int(got[cname]) == C.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert int(got[f"{cname}.{fname}"]) == getattr(py, fname).offset, (cname, fname)
 
 
 def _ws_expect(w):

@@ -137,3 +137,25 @@ def test_backward_dgate_is_output_projection():
         for j in range(w.k):
             y = orc.expert_row(w, inp, int(base["idx"][t, j]), inp["x"][t].astype(np.float64))
             assert abs(gr["dgate"][t, j] - y[2]) < 1e-12
+
+
+def test_backward_units_equal_full_arrays():
+    """The per-unit weight gradients equal the rows / columns of the full
+    arrays (shared expert included)."""
+    w = wl.Workload("units", 83, T=9, d=8, E=3, k=2, F=5, activation=wl.SWIGLU, score_fn=wl.SIGMOID, dtype=wl.F32,
+                    router_bias=True, expert_bias=False, num_shared=1, residual=True)
+    inp = _inputs(w, seed=21)
+    base = orc.layer(w, inp)
+    dout = np.random.default_rng(2).standard_normal((w.T, w.d))
+    full = orc.backward(w, inp, base, dout, 0.1, 0.1)
+    units = np.array([0, 4, 7, 14, 15, 19], np.int64)       # 15.. are the shared expert's rows
+    part = orc.backward(w, inp, base, dout, 0.1, 0.1, units=units)
+    for i, u in enumerate(units):
+        e, f = divmod(int(u), w.F)
+        W1 = full["dw1"][e] if e < w.E else full["dsw1"][e - w.E]
+        W3 = full["dw3"][e] if e < w.E else full["dsw3"][e - w.E]
+        W2 = full["dw2"][e] if e < w.E else full["dsw2"][e - w.E]
+        np.testing.assert_allclose(part["dw1_rows"][i], W1[f], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(part["dw3_rows"][i], W3[f], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(part["dw2_cols"][i], W2[:, f], rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(part["dx"], full["dx"])
