@@ -21,6 +21,10 @@ routing (every expert takes C = ceil(T/E * k) tokens, the compute of top-k)
 or under hash routing of Zipf-distributed token ids; the default, top-k, is
 the headline.
 
+--train times a training step instead: the forward keeping its activations
+plus moe_backward (aux_coef 0.01, z_coef 0.001), with the backward's stage
+times and the TFLOP/s of its four GEMMs.
+
 --impl reference times the plain CPU oracle on this machine's host cores on
 a bounded sample of the same workload (full routing of every token plus the
 experts of a sample of tokens, extrapolated to the whole batch).
@@ -388,6 +392,143 @@ def run_ours(args, w, rank, world, local):
     return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms)
 
 
+# ---------------------------------------------------------------------- training step
+BWD_STAGES = ["gate_router", "weight_transpose", "dh_gemm", "dx_gemm", "shared", "dx_assemble", "pack",
+              "dw2_gemm", "dw13_gemm", "bias_router_shared"]
+
+
+def bwd_launches(w):
+    """Kernels moe_backward launches (the order of its implementation)."""
+    gated = w.activation == wl.SWIGLU
+    wide = w.E >= 64 and w.E % 8 == 0
+    n = 2 + (2 if wide else 0)                       # combine, router (+ W_r transpose, dx router GEMM)
+    n += 3 if gated else 2                           # weight transposes
+    n += 2                                           # dh, dx GEMMs
+    if w.num_shared:
+        n += (3 if gated else 2) + 2
+    n += 1 + 1 + 4 + 1 + (2 if gated else 1)         # dx assembly, offsets, packs, dW2, dW1 (+ dW3)
+    if w.expert_bias and not gated:
+        n += 2
+    if w.num_shared or wide:
+        n += 2                                       # token offsets, x pack
+    n += 7 if wide else 2                            # router weight gradient (wide: offsets, 4 packs, GEMM, db)
+    if w.num_shared:
+        n += 3 + (3 if gated else 2)
+    return n
+
+
+def run_train(args, w, rank, world, local):
+    """One step = the training forward (activations kept) + moe_backward
+    with aux_coef 0.01, z_coef 0.001."""
+    import torch
+    import sparse_mixture_experts_60_b300 as moe
+    from sparse_mixture_experts_60_b300 import build as mbuild
+
+    mbuild.build()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    inp = wl.make_inputs(w)
+    dev = upload(inp, torch)
+    cfg = moe.config_for(w)
+    wts = {k: dev[k] for k in ("w_router", "b_router", "w1", "b1", "w3", "w2", "b2", "shared_w1",
+                               "shared_w3", "shared_w2") if k in dev}
+    layer = moe.TrainingLayer(cfg, wts, dev.get("sel_bias"))
+    x = dev["x"]
+    out = torch.empty(w.T, w.d, dtype=layer.out_dtype(), device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(11)
+    dout = torch.randn(w.T, w.d, device="cuda", generator=g).to(torch.bfloat16)
+    grads = layer.new_grads()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    def events(n, m):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(m)] for _ in range(n)]
+        for row in evs:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        return evs, [[e.cuda_event for e in row] for row in evs]
+
+    for _ in range(max(3, args.warmup)):
+        layer.forward(x, out)
+        layer.backward(dout, 0.01, 0.001, grads)
+    torch.cuda.synchronize()
+    if moe.moe_check_device_error():
+        raise RuntimeError("device error flag after warm-up")
+    uuid = str(torch.cuda.get_device_properties(local).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+
+    def timed():
+        fe, fh = events(args.steps, moe.MOE_STAGE_EVENTS)
+        be, bh = events(args.steps, moe.MOE_BWD_STAGE_EVENTS)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        with ClockSampler(uuid) as cs:
+            t0.record(stream)
+            for i in range(args.steps):
+                layer.forward(x, out, stage_events=fh[i])
+                layer.backward(dout, 0.01, 0.001, grads, stage_events=bh[i])
+            t1.record(stream)
+            barrier()
+        return t0.elapsed_time(t1), fe, be, cs.summary()
+
+    total_ms, fe, be, clocks = timed()
+    if {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(clocks["reasons"]):
+        total_ms, fe, be, clocks = timed()
+        clocks["remeasured"] = True
+    fst = np.array([[fe[i][j].elapsed_time(fe[i][j + 1]) for j in range(7)] for i in range(args.steps)]).mean(0)
+    bst = np.array([[be[i][j].elapsed_time(be[i][j + 1]) for j in range(10)] for i in range(args.steps)]).mean(0)
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
+    ms = total_ms / args.steps
+    kept = int(layer.stats()["total_kept"])
+    if moe.moe_check_device_error():
+        raise RuntimeError("device error flag after the timed region")
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    nF = 2 * w.F if w.activation == wl.SWIGLU else w.F
+    R = kept
+    f1, f2 = gemm_flops(w, kept)                  # forward expert GEMMs
+    flops = {"dh_gemm": 2.0 * R * w.d * w.F, "dx_gemm": 2.0 * R * nF * w.d, "dw2_gemm": 2.0 * R * w.d * w.F,
+             "dw13_gemm": 2.0 * R * nF * w.d}
+    bms = dict(zip(BWD_STAGES, bst.tolist()))
+    gemm_tf = {k: flops[k] / (bms[k] * 1e-3) / 1e12 for k in flops}
+    top = max(flops, key=lambda k: bms[k])
+    train_flops = f1 + f2 + sum(flops.values())
+    gemm_ms = float(fst[2] + fst[3]) + sum(bms[k] for k in flops)
+    line = {
+        "metric": "MoE-layer training step (forward + backward) tokens/s on 1 B300", "value":
+        whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": dict(config_of(w), mode="train", aux_coef=0.01, z_coef=0.001),
+        "roofline": {"kernel": f"grouped_gemm ({top}, backward)", "bound": "tensor", "achieved": gemm_tf[top],
+                     "peak": peak, "unit": "TFLOP/s", "frac": gemm_tf[top] / peak,
+                     "peak_kind": f"bf16_tflops_sustained of {pk_kind}", "traffic": None,
+                     "flops_per_launch": flops[top], "ms_per_launch": bms[top]},
+        "expert_gemm": {"tflops": train_flops / (gemm_ms * 1e-3) / 1e12,
+                        "frac_of_bf16_sustained": train_flops / (gemm_ms * 1e-3) / 1e12 / peak, "ms": gemm_ms,
+                        "backward_gemm_tflops": gemm_tf},
+        "stage_ms": {"forward": dict(zip(["route", "permute", "ffn1", "ffn2", "shared", "combine", "stats"],
+                                         fst.tolist())), "backward": bms},
+        "clocks": clocks, "e2e": None,
+        "gpu_launches": (launches_per_step(w) + bwd_launches(w)) * args.steps,
+    }
+    print(json.dumps(line, default=float), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms):
     if rank != 0:
         dist.destroy_process_group()
@@ -451,6 +592,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (profiling of a smaller case; not a headline)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="time the training step (forward keeping activations + backward) instead")
     ap.add_argument("--routing", default="topk", choices=["topk", "expert_choice", "hash"],
                     help="token-choice top-k (the headline), expert-choice or hash routing")
     args = ap.parse_args()
@@ -470,6 +613,10 @@ def main():
         if args.routing != "topk":
             ap.error("--impl reference times the top-k layer only")
         return run_reference(args, w, rank, world)
+    if args.train:
+        if args.routing != "topk" or w.dtype != wl.BF16:
+            ap.error("--train times the top-k layer of a bf16 workload")
+        return run_train(args, w, rank, world, local)
     return run_ours(args, w, rank, world, local)
 
 

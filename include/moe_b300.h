@@ -417,7 +417,7 @@ moe_status_t moe_forward_expert_choice(const moe_config_t *cfg, const moe_weight
  * auxiliary load-balancing loss (Load Balancing: loss = main + coef * aux)
  * and the router z-loss,
  *   L = sum_t <dout_t, out_t> + aux_coef * L_aux + z_coef * L_z,
- * differentiated through the forward: gate-weighted combine, expert FFNs
+ * (coefficients in opts) differentiated through the forward: gate-weighted combine, expert FFNs
  * (GELU / ReLU / SwiGLU, biases), shared expert, residual, gate function
  * (softmax or sigmoid, renormalised or raw; the selection and the selection
  * bias b_i are piecewise constant and get no gradient), L_aux with the
@@ -463,8 +463,22 @@ typedef struct {
     float *shared_dw2;
 } moe_grads_t;
 
+/* Options of moe_backward (NULL: aux_coef = z_coef = 0, no events).
+ * stage_events: optional host array of MOE_BWD_STAGE_EVENTS cudaEvent_t
+ * handles recorded on the stream: [0] start, [1] gate and router gradients,
+ * [2] weights transposed, [3] dh GEMM with the activation backward, [4] dx
+ * GEMM, [5] shared expert data path, [6] dx assembled, [7] activations
+ * packed, [8] dW2 GEMM, [9] dW1 / dW3 GEMMs, [10] bias, router and shared
+ * expert weight gradients. */
+#define MOE_BWD_STAGE_EVENTS 11
+typedef struct {
+    float aux_coef;
+    float z_coef;
+    void *const *stage_events;
+} moe_backward_opts_t;
+
 moe_status_t moe_backward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x, const void *dout,
-                          const moe_saved_t *saved, float aux_coef, float z_coef, const moe_grads_t *grads,
+                          const moe_saved_t *saved, const moe_grads_t *grads, const moe_backward_opts_t *opts,
                           void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Reads and clears the device error flag (host output *code: 0 = none,

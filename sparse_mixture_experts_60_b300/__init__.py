@@ -16,7 +16,7 @@ from __future__ import annotations
 import ctypes as C
 from typing import Dict, Optional
 
-from ._lib import (MOE_STAGE_EVENTS, MOE_WS_BACKWARD, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN,  # noqa: F401
+from ._lib import (MOE_BWD_STAGE_EVENTS, MOE_STAGE_EVENTS, MOE_WS_BACKWARD, MoEBackwardOpts, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN,  # noqa: F401
                    MOE_WS_FORWARD, MOE_WS_PERMUTE, MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEECIO, MoEGrads,
                    MoESaved, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
                    last_error, lib)
@@ -223,16 +223,22 @@ def moe_forward_expert_choice(cfg, weights: Dict, x, out, io: Optional[Dict], ws
                                           C.byref(ios) if ios is not None else None, p, n, _stream(stream)))
 
 
-def moe_backward(cfg, weights: Dict, x, dout, saved: Dict, aux_coef: float, z_coef: float, grads: Dict, ws,
-                 stream=None) -> None:
+def moe_backward(cfg, weights: Dict, x, dout, saved: Dict, grads: Dict, ws, aux_coef: float = 0.0,
+                 z_coef: float = 0.0, stream=None, stage_events=None) -> None:
     """Layer backward; ``saved`` keyed like ``MoESaved``, ``grads`` (fp32
-    output tensors) keyed like ``MoEGrads`` (missing keys: not computed)."""
+    output tensors) keyed like ``MoEGrads`` (missing keys: not computed);
+    ``stage_events``: optional MOE_BWD_STAGE_EVENTS raw cudaEvent_t handles."""
     p, n = _ws(ws)
     wst = weights_struct(weights)
     sv = MoESaved(**{k: _ptr(saved.get(k)) for k, _ in MoESaved._fields_})
     gr = MoEGrads(**{k: _ptr(grads.get(k)) for k, _ in MoEGrads._fields_})
-    check(lib().moe_backward(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(dout), C.byref(sv), float(aux_coef),
-                             float(z_coef), C.byref(gr), p, n, _stream(stream)))
+    opts = MoEBackwardOpts(aux_coef=float(aux_coef), z_coef=float(z_coef))
+    if stage_events is not None:
+        arr = (C.c_void_p * MOE_BWD_STAGE_EVENTS)(*[int(e) for e in stage_events])
+        opts._events_keepalive = arr
+        opts.stage_events = C.cast(arr, C.c_void_p)
+    check(lib().moe_backward(C.byref(cfg), C.byref(wst), _ptr(x), _ptr(dout), C.byref(sv), C.byref(gr),
+                             C.byref(opts), p, n, _stream(stream)))
 
 
 def moe_check_device_error() -> int:
@@ -416,9 +422,10 @@ class TrainingLayer(MoELayer):
         return g
 
     def backward(self, dout, aux_coef: float = 0.0, z_coef: float = 0.0, grads: Optional[Dict] = None,
-                 stream=None) -> Dict:
+                 stream=None, stage_events=None) -> Dict:
         g = grads if grads is not None else self.new_grads()
-        moe_backward(self.cfg, self.weights, self._x, dout, self.saved(), aux_coef, z_coef, g, self.bws, stream)
+        moe_backward(self.cfg, self.weights, self._x, dout, self.saved(), g, self.bws, aux_coef, z_coef, stream,
+                     stage_events)
         return g
 
 

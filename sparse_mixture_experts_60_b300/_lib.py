@@ -64,6 +64,13 @@ class MoEECIO(C.Structure):
                                           "stage_events")]
 
 
+MOE_BWD_STAGE_EVENTS = 11
+
+
+class MoEBackwardOpts(C.Structure):
+    _fields_ = [("aux_coef", C.c_float), ("z_coef", C.c_float), ("stage_events", C.c_void_p)]
+
+
 class MoEError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -91,7 +98,7 @@ _SIGS = {
     "moe_forward_from_routing": ([P] * 7 + [P, C.c_size_t, P], C.c_int),
     "moe_route_hash": ([P] * 4 + [P], C.c_int),
     "moe_ec_capacity": ([P, C.POINTER(C.c_int64)], C.c_int),
-    "moe_backward": ([P] * 5 + [C.c_float, C.c_float, P, P, C.c_size_t, P], C.c_int),
+    "moe_backward": ([P] * 8 + [C.c_size_t, P], C.c_int),
     "moe_route_expert_choice": ([P] * 6 + [P], C.c_int),
     "moe_forward_expert_choice": ([P] * 5 + [P, C.c_size_t, P], C.c_int),
     "moe_check_device_error": ([C.POINTER(C.c_int32)], C.c_int),

@@ -99,13 +99,16 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t T, int d, int 
 // renormalised over the chosen experts or not), then the auxiliary loss
 // (f_e = counts_e / (T k) held fixed) and the z-loss terms are added.
 // Per-warp shared scratch: dg[E] (gate gradient per chosen expert) and
-// sel[E] (1 for a chosen expert).
+// sel[E] (1 for a chosen expert).  dl_hi / dl_lo (optional): dl split into
+// two bf16 numbers (hi = bf16(dl), lo = bf16(dl - hi)), the operands of the
+// router's tensor-core GEMMs on wide routers (hi + lo keeps ~16 bits).
 __global__ void __launch_bounds__(256) router_bwd_kernel(int64_t T, int E, int k, int score_fn, int renormalize,
                                                          const float *__restrict__ logits,
                                                          const int32_t *__restrict__ topk_idx,
                                                          const float *__restrict__ dgate,
                                                          const int32_t *__restrict__ counts, float aux_coef,
-                                                         float z_coef, float *__restrict__ dl) {
+                                                         float z_coef, float *__restrict__ dl,
+                                                         bf16 *__restrict__ dl_hi, bf16 *__restrict__ dl_lo) {
     PDL_ENTER();
     extern __shared__ float sh[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -167,19 +170,26 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(int64_t T, int E, int k
         g += aux_s * p * ((float)__ldg(counts + e) * inv_tk - fp);
         g += z_s * p;
         dl[t * E + e] = g;
+        if (dl_hi) {
+            const bf16 hi = __float2bfloat16(g);
+            dl_hi[t * E + e] = hi;
+            dl_lo[t * E + e] = __float2bfloat16(g - __bfloat162float(hi));
+        }
     }
 }
 
 // Warp per token, 8 columns per lane step:
 //   dx[t] = sum_j dx_perm[inv[t,j]] + dout_t (residual) + dxs[t] (shared)
-//           + sum_e dl[t,e] W_r[e, :]
+//           + sum_e dl[t,e] W_r[e, :]   (or dxr[t], that product from the
+//           tensor cores on wide routers)
 __global__ void __launch_bounds__(256) dx_assemble_kernel(int64_t T, int d, int k, int E,
                                                           const float *__restrict__ dx_perm,
                                                           const int32_t *__restrict__ inv,
                                                           const bf16 *__restrict__ dout, int residual,
                                                           const float *__restrict__ dxs,
                                                           const float *__restrict__ dl,
-                                                          const bf16 *__restrict__ w_router, float *__restrict__ dx) {
+                                                          const bf16 *__restrict__ w_router,
+                                                          const float *__restrict__ dxr, float *__restrict__ dx) {
     PDL_ENTER();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -209,12 +219,19 @@ __global__ void __launch_bounds__(256) dx_assemble_kernel(int64_t T, int d, int 
             acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
             acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
         }
-        for (int e = 0; e < E; ++e) {
-            const float g = __ldg(dl + t * E + e);
-            float wv[8];
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(w_router + (int64_t)e * d) + c), wv);
+        if (dxr) {
+            const float4 *p = reinterpret_cast<const float4 *>(dxr + t * d) + 2 * c;
+            const float4 a = __ldg(p), b = __ldg(p + 1);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        } else {
+            for (int e = 0; e < E; ++e) {
+                const float g = __ldg(dl + t * E + e);
+                float wv[8];
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(w_router + (int64_t)e * d) + c), wv);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, wv[i], acc[i]);
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, wv[i], acc[i]);
+            }
         }
         float4 *o = reinterpret_cast<float4 *>(dx + t * d) + 2 * c;
         o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -227,23 +244,24 @@ __global__ void __launch_bounds__(256) dx_assemble_kernel(int64_t T, int d, int 
 // part[chunk][e][col].
 constexpr int kRwCols = 128;
 constexpr int kRwChunk = 512;
+template <int EP>
 __global__ void __launch_bounds__(kRwCols) router_wgrad_partial_kernel(int64_t T, int d, int E,
                                                                       const float *__restrict__ dl,
                                                                       const bf16 *__restrict__ x,
                                                                       float *__restrict__ part) {
     PDL_ENTER();
-    __shared__ float sdl[32][33];
+    __shared__ float sdl[32][EP + 1];
     const int col = blockIdx.x * kRwCols + threadIdx.x;
     const int64_t t0 = (int64_t)blockIdx.y * kRwChunk;
     const int64_t t1 = t0 + kRwChunk < T ? t0 + kRwChunk : T;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-        float acc[32];
+    for (int e0 = 0; e0 < E; e0 += EP) {
+        float acc[EP];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < EP; ++i) acc[i] = 0.0f;
         for (int64_t tb = t0; tb < t1; tb += 32) {
             __syncthreads();
-            for (int i = threadIdx.x; i < 32 * 32; i += kRwCols) {
-                const int tt = i / 32, ee = i % 32;
+            for (int i = threadIdx.x; i < 32 * EP; i += kRwCols) {
+                const int tt = i / EP, ee = i % EP;
                 sdl[tt][ee] = (tb + tt < t1 && e0 + ee < E) ? __ldg(dl + (tb + tt) * E + e0 + ee) : 0.0f;
             }
             __syncthreads();
@@ -251,12 +269,12 @@ __global__ void __launch_bounds__(kRwCols) router_wgrad_partial_kernel(int64_t T
             for (int tt = 0; tt < nt; ++tt) {
                 const float xv = col < d ? __bfloat162float(x[(tb + tt) * d + col]) : 0.0f;
 #pragma unroll
-                for (int ee = 0; ee < 32; ++ee) acc[ee] = fmaf(sdl[tt][ee], xv, acc[ee]);
+                for (int ee = 0; ee < EP; ++ee) acc[ee] = fmaf(sdl[tt][ee], xv, acc[ee]);
             }
         }
         if (col < d) {
 #pragma unroll
-            for (int ee = 0; ee < 32; ++ee)
+            for (int ee = 0; ee < EP; ++ee)
                 if (e0 + ee < E) part[((int64_t)blockIdx.y * E + e0 + ee) * d + col] = acc[ee];
         }
     }
@@ -289,43 +307,71 @@ __global__ void __launch_bounds__(256) router_wgrad_reduce_kernel(int64_t T, int
     }
 }
 
-// Batched transpose, 64 x 64 tiles through shared memory:
-//   out[b][c][r] = in[b][r][c]   (in: rows x cols, leading dim ld_in;
-//   out: cols x rows at column offset out_col0, leading dim ld_out)
+// 64 x 64 bf16 tile transpose through shared memory with 16-byte global
+// accesses on both sides: 256 threads each load two 8-element row vectors
+// (rows past `nrows`, columns past `ncols` read as zeros), then each
+// gathers two 8-row column vectors.  Rows are 128 bytes, their eight 16-byte
+// chunks XOR-swizzled by (row / 8) mod 8: a warp's row writes cover whole
+// rows, and the eight threads of a column gather (rows 8j .. 8j+7, j = 0..7)
+// read eight different chunks, so neither side has bank conflicts.
+__device__ __forceinline__ int swz(int r, int c) { return (((c >> 3) ^ ((r >> 3) & 7)) << 3) | (c & 7); }
+template <typename SrcRow>
+__device__ __forceinline__ void tile_in(bf16 (*tile)[64], SrcRow src_row, int nrows, int ncols) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int v = threadIdx.x + h * 256;          // 512 vectors: row v / 8, columns 8 (v % 8) ..
+        const int r = v >> 3, c8 = (v & 7) * 8;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (r < nrows && c8 < ncols) u = __ldg(reinterpret_cast<const uint4 *>(src_row(r) + c8));
+        *reinterpret_cast<uint4 *>(&tile[r][swz(r, c8)]) = u;
+    }
+}
+__device__ __forceinline__ uint4 tile_col8(bf16 (*tile)[64], int c, int r8) {
+    uint32_t w[4];
+    const int pc = swz(r8, c);                         // rows r8 .. r8+7 share the swizzle
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const uint32_t lo = __bfloat16_as_ushort(tile[r8 + 2 * h][pc]);
+        const uint32_t hi = __bfloat16_as_ushort(tile[r8 + 2 * h + 1][pc]);
+        w[h] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Batched transpose: out[b][c][out_col0 + r] = in[b][r][c] (in: rows x cols
+// with leading dim ld_in; rows, cols, ld_in, ld_out, out_col0 multiples of 8).
 __global__ void __launch_bounds__(256) transpose_batched_kernel(const bf16 *__restrict__ in, int64_t in_batch,
                                                                 int ld_in, int rows, int cols,
                                                                 bf16 *__restrict__ out, int64_t out_batch,
                                                                 int ld_out, int out_col0) {
     PDL_ENTER();
-    __shared__ bf16 tile[64][66];
-    const int b = blockIdx.z;
+    __shared__ __align__(16) bf16 tile[64][64];
     const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-    const bf16 *src = in + b * in_batch;
-    for (int i = ty; i < 64; i += 4) {
-        const int r = r0 + i, c = c0 + tx;
-        tile[i][tx] = (r < rows && c < cols) ? src[(int64_t)r * ld_in + c] : __float2bfloat16(0.0f);
-    }
+    const bf16 *src = in + blockIdx.z * in_batch;
+    const int nr = rows - r0 < 64 ? rows - r0 : 64, nc = cols - c0 < 64 ? cols - c0 : 64;
+    tile_in(tile, [&](int r) { return src + (int64_t)(r0 + r) * ld_in + c0; }, nr, nc);
     __syncthreads();
-    bf16 *dst = out + b * out_batch;
-    for (int i = ty; i < 64; i += 4) {
-        const int c = c0 + i, r = r0 + tx;
-        if (c < cols && r < rows) dst[(int64_t)c * ld_out + out_col0 + r] = tile[tx][i];
+    bf16 *dst = out + blockIdx.z * out_batch;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int v = threadIdx.x + h * 256;          // output row c = v / 8, 8 input rows from 8 (v % 8)
+        const int c = v >> 3, r8 = (v & 7) * 8;
+        if (c < nc && r8 < nr)
+            *reinterpret_cast<uint4 *>(dst + (int64_t)(c0 + c) * ld_out + out_col0 + r0 + r8) = tile_col8(tile, c, r8);
     }
 }
 
 // Packed transpose of grouped rows: out[c][pad[g] + i] = in[off[g] + i][c]
 // for i < rows_g, zero for rows_g <= i < pad[g+1] - pad[g].  Every pad[g]
 // is a multiple of 64, so a 64-column output tile belongs to one group.
-// off == nullptr: a single group of `rows` rows.
+// off == nullptr: a single group of `rows` rows.  cols, ld_in multiples of 8.
 __global__ void __launch_bounds__(256) transpose_pack_kernel(const bf16 *__restrict__ in, int ld_in, int cols,
                                                              const int32_t *__restrict__ off,
                                                              const int32_t *__restrict__ pad, int G, int rows,
                                                              bf16 *__restrict__ out, int64_t ld_out) {
     PDL_ENTER();
-    __shared__ bf16 tile[64][66];
+    __shared__ __align__(16) bf16 tile[64][64];
     const int p0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
     const int total = pad[G];
     if (p0 >= total) return;
     int g = 0;
@@ -339,15 +385,16 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const bf16 *__restr
         g = lo;
     }
     const int gbeg = off ? off[g] : 0, gend = off ? off[g + 1] : rows;
-    const int pbeg = pad[g];
-    for (int i = ty; i < 64; i += 4) {
-        const int r = gbeg + (p0 + i - pbeg), c = c0 + tx;
-        tile[i][tx] = (r < gend && c < cols) ? in[(int64_t)r * ld_in + c] : __float2bfloat16(0.0f);
-    }
+    const int r0 = gbeg + (p0 - pad[g]);                  // first source row of the tile
+    const int nr = gend - r0 < 64 ? (gend - r0 > 0 ? gend - r0 : 0) : 64;
+    const int nc = cols - c0 < 64 ? cols - c0 : 64;
+    tile_in(tile, [&](int r) { return in + (int64_t)(r0 + r) * ld_in + c0; }, nr, nc);
     __syncthreads();
-    for (int i = ty; i < 64; i += 4) {
-        const int c = c0 + i;
-        if (c < cols) out[(int64_t)c * ld_out + p0 + tx] = tile[tx][i];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int v = threadIdx.x + h * 256;
+        const int c = v >> 3, r8 = (v & 7) * 8;
+        if (c < nc) *reinterpret_cast<uint4 *>(out + (int64_t)(c0 + c) * ld_out + p0 + r8) = tile_col8(tile, c, r8);
     }
 }
 
@@ -425,7 +472,7 @@ cudaError_t launch_combine_bwd(int64_t T, int d, int k, const bf16 *dout, const 
 
 cudaError_t launch_router_bwd(int64_t T, int E, int k, int score_fn, int renormalize, const float *logits,
                               const int32_t *topk_idx, const float *dgate, const int32_t *counts, float aux_coef,
-                              float z_coef, float *dl, cudaStream_t s) {
+                              float z_coef, float *dl, bf16 *dl_hi, bf16 *dl_lo, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const size_t smem = (size_t)8 * 2 * E * sizeof(float);
     if (smem > 48 * 1024) {
@@ -434,15 +481,15 @@ cudaError_t launch_router_bwd(int64_t T, int E, int k, int score_fn, int renorma
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(router_bwd_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), smem, s, T, E, k, score_fn,
-                      renormalize, logits, topk_idx, dgate, counts, aux_coef, z_coef, dl);
+                      renormalize, logits, topk_idx, dgate, counts, aux_coef, z_coef, dl, dl_hi, dl_lo);
 }
 
 cudaError_t launch_dx_assemble(int64_t T, int d, int k, int E, const float *dx_perm, const int32_t *inv,
                                const bf16 *dout, int residual, const float *dxs, const float *dl,
-                               const bf16 *w_router, float *dx, cudaStream_t s) {
+                               const bf16 *w_router, const float *dxr, float *dx, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     return launch_pdl(dx_assemble_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, T, d, k, E, dx_perm,
-                      inv, dout, residual, dxs, dl, w_router, dx);
+                      inv, dout, residual, dxs, dl, w_router, dxr, dx);
 }
 
 int64_t router_wgrad_chunks(int64_t T) { return ceil_div(T, kRwChunk); }
@@ -458,9 +505,13 @@ cudaError_t launch_router_wgrad(int64_t T, int d, int E, const float *dl, const 
     }
     const int64_t nchunk = router_wgrad_chunks(T);
     cudaError_t e = cudaSuccess;
-    if (dw)
-        e = launch_pdl(router_wgrad_partial_kernel, dim3((unsigned)ceil_div(d, kRwCols), (unsigned)nchunk),
-                       dim3(kRwCols), 0, s, T, d, E, dl, x, part);
+    if (dw) {
+        const dim3 grid((unsigned)ceil_div(d, kRwCols), (unsigned)nchunk);
+        if (E <= 8) e = launch_pdl(router_wgrad_partial_kernel<8>, grid, dim3(kRwCols), 0, s, T, d, E, dl, x, part);
+        else if (E <= 16)
+            e = launch_pdl(router_wgrad_partial_kernel<16>, grid, dim3(kRwCols), 0, s, T, d, E, dl, x, part);
+        else e = launch_pdl(router_wgrad_partial_kernel<32>, grid, dim3(kRwCols), 0, s, T, d, E, dl, x, part);
+    }
     if (e != cudaSuccess) return e;
     return launch_pdl(router_wgrad_reduce_kernel, dim3((unsigned)ceil_div(d, 256), (unsigned)E), dim3(256), 0, s,
                       T, d, E, (int)nchunk, part, dl, dw, db);
@@ -475,10 +526,10 @@ cudaError_t launch_transpose_batched(const bf16 *in, int64_t in_batch, int ld_in
 }
 
 cudaError_t launch_transpose_pack(const bf16 *in, int ld_in, int cols, const int32_t *off, const int32_t *pad, int G,
-                                  int rows, int64_t max_padded, bf16 *out, cudaStream_t s) {
+                                  int rows, int64_t max_padded, bf16 *out, int64_t ld_out, cudaStream_t s) {
     if (cols == 0 || max_padded == 0) return cudaSuccess;
     return launch_pdl(transpose_pack_kernel, dim3((unsigned)ceil_div(cols, 64), (unsigned)(max_padded / 64)),
-                      dim3(256), 0, s, in, ld_in, cols, off, pad, G, rows, out, max_padded);
+                      dim3(256), 0, s, in, ld_in, cols, off, pad, G, rows, out, ld_out);
 }
 
 cudaError_t launch_pad_offsets(const int32_t *off, int G, int rows, int32_t *pad, cudaStream_t s) {

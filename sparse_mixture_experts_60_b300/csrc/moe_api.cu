@@ -145,6 +145,10 @@ BwdDims bwd_dims(const moe_config_t *c) {
     b.Tp = (b.T + 63) / 64 * 64;
     return b;
 }
+// Wide routers (E >= 64, E % 8 == 0) take the router's two products with
+// the tensor cores (dlogits W_r for dx, dlogits^T x for dW_r).
+bool wide_router(const moe_config_t *c) { return c->num_experts >= 64 && c->num_experts % 8 == 0; }
+
 size_t bwd_ws(const moe_config_t *c) {
     const BwdDims b = bwd_dims(c);
     size_t n = align256(b.R * b.d * 2) + align256(b.T * b.k * 4) + align256(b.T * b.E * 4) +
@@ -153,9 +157,13 @@ size_t bwd_ws(const moe_config_t *c) {
     n += align256(b.R * b.nF * 2) + align256(b.R * b.d * 4);                  // da, dx_perm
     n += 2 * align256(b.d * b.Rp * 2) + align256(b.F * b.Rp * 2) + align256(b.nF * b.Rp * 2);
     n += align256((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
+    if (c->num_shared || wide_router(c)) n += align256(b.d * b.Tp * 2);          // x^T
+    if (wide_router(c))   // dlogits hi / lo, W_r^T, the router's dx term, [hi | lo]^T, [x^T | x^T]
+        n += 2 * align256(b.T * b.E * 2) + align256(b.d * b.E * 2) + align256(b.T * b.d * 4) +
+             align256(b.E * 2 * b.Tp * 2) + align256(b.d * 2 * b.Tp * 2) + align256(2 * 4);
     if (c->num_shared) {
         n += align256(b.T * b.nF * 2) + align256(b.T * b.d * 4) + align256(b.F * b.d * 2) + align256(b.d * b.nF * 2);
-        n += 2 * align256(b.d * b.Tp * 2) + align256(b.F * b.Tp * 2) + align256(b.nF * b.Tp * 2);
+        n += align256(b.d * b.Tp * 2) + align256(b.F * b.Tp * 2) + align256(b.nF * b.Tp * 2);
     }
     return n;
 }
@@ -846,8 +854,11 @@ moe_status_t dgrad_gemm(const bf16 *A, int64_t a_rows, const int32_t *seg, int G
 }
 
 moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const void *x, const void *dout,
-                           const moe_saved_t *sv, float aux_coef, float z_coef, const moe_grads_t *gr, void *ws,
-                           cudaStream_t s) {
+                           const moe_saved_t *sv, float aux_coef, float z_coef, const moe_grads_t *gr,
+                           void *const *ev, void *ws, cudaStream_t s) {
+    auto mark = [&](int i) {
+        if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+    };
     const BwdDims b = bwd_dims(c);
     const bool gated = c->activation == MOE_ACT_SWIGLU;
     const int act = c->activation == MOE_ACT_GELU ? 1 : (c->activation == MOE_ACT_RELU ? 2 : 0);
@@ -868,25 +879,44 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
     bf16 *hT = cv.take<bf16>(b.F * b.Rp * 2);
     bf16 *daT = cv.take<bf16>(b.nF * b.Rp * 2);
     float *rwpart = cv.take<float>((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
+    const bool wide = wide_router(c);
+    bf16 *xT = (c->num_shared || wide) ? cv.take<bf16>(b.d * b.Tp * 2) : nullptr;
+    bf16 *dl_hi = wide ? cv.take<bf16>(b.T * b.E * 2) : nullptr;
+    bf16 *dl_lo = wide ? cv.take<bf16>(b.T * b.E * 2) : nullptr;
+    bf16 *wrT = wide ? cv.take<bf16>(b.d * b.E * 2) : nullptr;
+    float *dxr = wide ? cv.take<float>(b.T * b.d * 4) : nullptr;
+    bf16 *dlT2 = wide ? cv.take<bf16>(b.E * 2 * b.Tp * 2) : nullptr;
+    bf16 *xT2 = wide ? cv.take<bf16>(b.d * 2 * b.Tp * 2) : nullptr;
+    int32_t *pad2 = wide ? cv.take<int32_t>(2 * 4) : nullptr;
     const bf16 *W1 = static_cast<const bf16 *>(w->w1), *W3 = static_cast<const bf16 *>(w->w3);
     const bf16 *W2 = static_cast<const bf16 *>(w->w2);
     const bf16 *go = static_cast<const bf16 *>(dout);
-    cudaError_t e;
 #define CU(call, what) TRY(cuda_status((call), what))
+    mark(0);
     // combine and router backward
     CU(launch_combine_bwd(b.T, d, (int)b.k, go, sv->topk_w, sv->inv, sv->y_perm, dy, dgate, s), "combine backward");
     CU(launch_router_bwd(b.T, E, (int)b.k, c->score_fn, c->renormalize, sv->logits, sv->topk_idx, dgate, sv->counts,
-                         aux_coef, z_coef, dl, s),
+                         aux_coef, z_coef, dl, dl_hi, dl_lo, s),
        "router backward");
+    if (wide) {
+        // dx's router term dlogits W_r on the tensor cores (K = E)
+        CU(launch_transpose_batched(static_cast<const bf16 *>(w->w_router), 0, d, E, d, 1, wrT, 0, E, 0, s),
+           "W_r transpose");
+        TRY(dgrad_gemm(dl_hi, b.T, nullptr, 1, (int)b.T, wrT, d, d, E, dxr, 1, d, nullptr, 0, 0, 0, s));
+    }
+    mark(1);
     // weights to the K-major layouts of the data-gradient GEMMs
     CU(launch_transpose_batched(W2, (int64_t)d * F, F, d, F, E, w2t, (int64_t)F * d, d, 0, s), "W2 transpose");
     CU(launch_transpose_batched(W1, (int64_t)F * d, d, F, d, E, w13t, (int64_t)d * nF, nF, 0, s), "W1 transpose");
     if (gated)
         CU(launch_transpose_batched(W3, (int64_t)F * d, d, F, d, E, w13t, (int64_t)d * nF, nF, F, s), "W3 transpose");
+    mark(2);
     // dh = dy W2 -> da (activation backward in the epilogue); dx_perm = da [W1 | W3]
     TRY(dgrad_gemm(dy, b.R, sv->offsets, E, 0, w2t, F, F, d, da, 0, nF,
                    const_cast<bf16 *>(static_cast<const bf16 *>(sv->pre_act)), nF, epi, act, s));
+    mark(3);
     TRY(dgrad_gemm(da, b.R, sv->offsets, E, 0, w13t, d, d, nF, dxp, 1, d, nullptr, 0, 0, 0, s));
+    mark(4);
     // shared expert: gate 1, A = dout
     float *dxs = nullptr;
     bf16 *das = nullptr;
@@ -906,43 +936,70 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
                        const_cast<bf16 *>(static_cast<const bf16 *>(sv->shared_pre_act)), nF, epi, act, s));
         TRY(dgrad_gemm(das, b.T, nullptr, 1, (int)b.T, w13st, d, d, nF, dxs, 1, d, nullptr, 0, 0, 0, s));
     }
+    mark(5);
     CU(launch_dx_assemble(b.T, d, (int)b.k, E, dxp, sv->inv, go, c->residual, dxs, dl,
-                          static_cast<const bf16 *>(w->w_router), gr->dx, s),
+                          static_cast<const bf16 *>(w->w_router), dxr, gr->dx, s),
        "dx assembly");
+    mark(6);
     // weight gradients over the experts' rows, packed K-major and padded
     CU(launch_pad_offsets(sv->offsets, E, 0, pad, s), "padded offsets");
-    CU(launch_transpose_pack(dy, d, d, sv->offsets, pad, E, 0, b.Rp, dyT, s), "dy pack");
-    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->x_perm), d, d, sv->offsets, pad, E, 0, b.Rp, xpT, s),
+    CU(launch_transpose_pack(dy, d, d, sv->offsets, pad, E, 0, b.Rp, dyT, b.Rp, s), "dy pack");
+    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->x_perm), d, d, sv->offsets, pad, E, 0, b.Rp, xpT, b.Rp,
+                             s),
        "x_perm pack");
-    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->hidden), F, F, sv->offsets, pad, E, 0, b.Rp, hT, s),
+    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->hidden), F, F, sv->offsets, pad, E, 0, b.Rp, hT, b.Rp,
+                             s),
        "H pack");
-    CU(launch_transpose_pack(da, nF, nF, sv->offsets, pad, E, 0, b.Rp, daT, s), "da pack");
+    CU(launch_transpose_pack(da, nF, nF, sv->offsets, pad, E, 0, b.Rp, daT, b.Rp, s), "da pack");
+    mark(7);
     if (gr->dw2) TRY(wgrad_gemm(dyT, d, hT, F, b.Rp, pad, E, gr->dw2, s));
+    mark(8);
     if (gr->dw1) TRY(wgrad_gemm(daT, F, xpT, d, b.Rp, pad, E, gr->dw1, s));
     if (gated && gr->dw3) TRY(wgrad_gemm(daT + b.F * b.Rp, F, xpT, d, b.Rp, pad, E, gr->dw3, s));
+    mark(9);
     if (!gated && gr->db1) CU(launch_group_rowsum(daT, b.Rp, pad, E, F, gr->db1, s), "db1");
     if (!gated && gr->db2) CU(launch_group_rowsum(dyT, b.Rp, pad, E, d, gr->db2, s), "db2");
-    CU(launch_router_wgrad(b.T, d, E, dl, static_cast<const bf16 *>(x), rwpart, gr->dw_router, gr->db_router, s),
-       "router weight gradient");
+    const int Ti = (int)b.T;
+    if (xT) {
+        CU(launch_pad_offsets(nullptr, 1, Ti, pad1, s), "token padded offsets");
+        CU(launch_transpose_pack(static_cast<const bf16 *>(x), d, d, nullptr, pad1, 1, Ti, b.Tp, xT, b.Tp, s),
+           "x pack");
+    }
+    if (wide) {
+        // dW_r = dlogits^T x on the tensor cores, one group over K = 2 Tp:
+        // [hi | lo]^T against [x^T | x^T], so dlogits keeps ~16 bits
+        CU(launch_pad_offsets(nullptr, 1, 2 * (int)b.Tp, pad2, s), "router K offsets");   // {0, 2 Tp}
+        CU(launch_transpose_pack(dl_hi, E, E, nullptr, pad1, 1, Ti, b.Tp, dlT2, 2 * b.Tp, s), "dlogits hi pack");
+        CU(launch_transpose_pack(dl_lo, E, E, nullptr, pad1, 1, Ti, b.Tp, dlT2 + b.Tp, 2 * b.Tp, s),
+           "dlogits lo pack");
+        CU(launch_transpose_pack(static_cast<const bf16 *>(x), d, d, nullptr, pad1, 1, Ti, b.Tp, xT2, 2 * b.Tp, s),
+           "x pack");
+        CU(launch_transpose_pack(static_cast<const bf16 *>(x), d, d, nullptr, pad1, 1, Ti, b.Tp, xT2 + b.Tp,
+                                 2 * b.Tp, s),
+           "x pack");
+        if (gr->dw_router) TRY(wgrad_gemm(dlT2, E, xT2, d, 2 * b.Tp, pad2, 1, gr->dw_router, s));
+        CU(launch_router_wgrad(b.T, d, E, dl, static_cast<const bf16 *>(x), rwpart, nullptr, gr->db_router, s),
+           "router bias gradient");
+    } else {
+        CU(launch_router_wgrad(b.T, d, E, dl, static_cast<const bf16 *>(x), rwpart, gr->dw_router, gr->db_router,
+                               s),
+           "router weight gradient");
+    }
     if (c->num_shared && (gr->shared_dw1 || gr->shared_dw2 || gr->shared_dw3)) {
         bf16 *goT = cv.take<bf16>(b.d * b.Tp * 2);
-        bf16 *xT = cv.take<bf16>(b.d * b.Tp * 2);
         bf16 *shT = cv.take<bf16>(b.F * b.Tp * 2);
         bf16 *dasT = cv.take<bf16>(b.nF * b.Tp * 2);
-        const int Ti = (int)b.T;
-        CU(launch_pad_offsets(nullptr, 1, Ti, pad1, s), "shared padded offsets");
-        CU(launch_transpose_pack(go, d, d, nullptr, pad1, 1, Ti, b.Tp, goT, s), "dout pack");
-        CU(launch_transpose_pack(static_cast<const bf16 *>(x), d, d, nullptr, pad1, 1, Ti, b.Tp, xT, s), "x pack");
+        CU(launch_transpose_pack(go, d, d, nullptr, pad1, 1, Ti, b.Tp, goT, b.Tp, s), "dout pack");
         CU(launch_transpose_pack(static_cast<const bf16 *>(sv->shared_hidden), F, F, nullptr, pad1, 1, Ti, b.Tp, shT,
-                                 s),
+                                 b.Tp, s),
            "shared H pack");
-        CU(launch_transpose_pack(das, nF, nF, nullptr, pad1, 1, Ti, b.Tp, dasT, s), "shared da pack");
+        CU(launch_transpose_pack(das, nF, nF, nullptr, pad1, 1, Ti, b.Tp, dasT, b.Tp, s), "shared da pack");
         if (gr->shared_dw2) TRY(wgrad_gemm(goT, d, shT, F, b.Tp, pad1, 1, gr->shared_dw2, s));
         if (gr->shared_dw1) TRY(wgrad_gemm(dasT, F, xT, d, b.Tp, pad1, 1, gr->shared_dw1, s));
         if (gated && gr->shared_dw3) TRY(wgrad_gemm(dasT + b.F * b.Tp, F, xT, d, b.Tp, pad1, 1, gr->shared_dw3, s));
     }
 #undef CU
-    (void)e;
+    mark(10);
     return MOE_OK;
 }
 
@@ -978,11 +1035,13 @@ moe_status_t moe_route_hash(const moe_config_t *cfg, const int32_t *token_ids, i
 }
 
 moe_status_t moe_backward(const moe_config_t *cfg, const moe_weights_t *weights, const void *x, const void *dout,
-                          const moe_saved_t *saved, float aux_coef, float z_coef, const moe_grads_t *grads,
+                          const moe_saved_t *saved, const moe_grads_t *grads, const moe_backward_opts_t *opts,
                           void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     if (cfg->dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_UNSUPPORTED, "moe_backward needs a bf16 layer");
-    if (!isfinite(aux_coef) || !isfinite(z_coef)) return fail(MOE_ERR_INVALID_ARG, "coefficients must be finite");
+    moe_backward_opts_t o{};
+    if (opts) o = *opts;
+    if (!isfinite(o.aux_coef) || !isfinite(o.z_coef)) return fail(MOE_ERR_INVALID_ARG, "coefficients must be finite");
     TRY(need(weights, "weights"));
     TRY(need(saved, "saved"));
     TRY(need(grads, "grads"));
@@ -1022,7 +1081,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const moe_weights_t *weights,
             if (q.p) TRY(cuda_status(cudaMemsetAsync(q.p, 0, q.n * sizeof(float), s), "zero gradients"));
         return MOE_OK;
     }
-    return backward_impl(cfg, weights, x, dout, saved, aux_coef, z_coef, grads, ws, s);
+    return backward_impl(cfg, weights, x, dout, saved, o.aux_coef, o.z_coef, grads, o.stage_events, ws, s);
 }
 
 moe_status_t moe_ec_capacity(const moe_config_t *cfg, int64_t *capacity) {

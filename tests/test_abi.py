@@ -49,7 +49,7 @@ def test_struct_layouts_match_header(tmp_path):
     by the host C compiler, equal the ctypes mirrors of the binding."""
     structs = {"moe_config_t": _lib.MoEConfig, "moe_stats_t": _lib.MoEStats, "moe_weights_t": _lib.MoEWeights,
                "moe_forward_io_t": _lib.MoEForwardIO, "moe_ec_io_t": _lib.MoEECIO, "moe_saved_t": _lib.MoESaved,
-               "moe_grads_t": _lib.MoEGrads}
+               "moe_grads_t": _lib.MoEGrads, "moe_backward_opts_t": _lib.MoEBackwardOpts}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe_b300.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
