@@ -138,7 +138,7 @@ def launches_per_step(w, routing="topk"):
     if routing == "hash":
         n = 1                                 # hash routing
     else:
-        n = 2 if (w.E <= 32 and w.dtype == wl.F32) else 3   # (logits GEMM +) routing + partial reduce
+        n = 1 if w.E <= 32 else 2             # fused router (GEMM epilogue / CUDA-core kernel), else logits + routing
     if S == 0:
         n += 1
     elif S <= 8192 and w.E <= 256:
