@@ -393,19 +393,18 @@ def run_ours(args, w, rank, world, local):
 
 
 # ---------------------------------------------------------------------- training step
-BWD_STAGES = ["gate_router", "weight_transpose", "dh_gemm", "dx_gemm", "shared", "dx_assemble", "pack",
-              "dw2_gemm", "dw13_gemm", "bias_router_shared"]
+BWD_STAGES = ["gate_router", "dh_gemm", "dx_gemm", "shared", "dx_assemble", "pack", "dw2_gemm", "dw13_gemm",
+              "bias_router_shared"]
 
 
 def bwd_launches(w):
     """Kernels moe_backward launches (the order of its implementation)."""
     gated = w.activation == wl.SWIGLU
-    wide = w.E >= 64 and w.E % 8 == 0
-    n = 2 + (2 if wide else 0)                       # combine, router (+ W_r transpose, dx router GEMM)
-    n += 3 if gated else 2                           # weight transposes
-    n += 2                                           # dh, dx GEMMs
+    wide = w.E >= 64 and w.E % 64 == 0
+    n = 2 + (1 if wide else 0)                       # combine, router (+ dx router GEMM)
+    n += 2                                           # dh, dx GEMMs (weights read in place)
     if w.num_shared:
-        n += (3 if gated else 2) + 2
+        n += 2
     n += 1 + 1 + 4 + 1 + (2 if gated else 1)         # dx assembly, offsets, packs, dW2, dW1 (+ dW3)
     if w.expert_bias and not gated:
         n += 2
@@ -485,7 +484,7 @@ def run_train(args, w, rank, world, local):
         total_ms, fe, be, clocks = timed()
         clocks["remeasured"] = True
     fst = np.array([[fe[i][j].elapsed_time(fe[i][j + 1]) for j in range(7)] for i in range(args.steps)]).mean(0)
-    bst = np.array([[be[i][j].elapsed_time(be[i][j + 1]) for j in range(10)] for i in range(args.steps)]).mean(0)
+    bst = np.array([[be[i][j].elapsed_time(be[i][j + 1]) for j in range(9)] for i in range(args.steps)]).mean(0)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms = total_ms / args.steps
     kept = int(layer.stats()["total_kept"])

@@ -466,11 +466,10 @@ typedef struct {
 /* Options of moe_backward (NULL: aux_coef = z_coef = 0, no events).
  * stage_events: optional host array of MOE_BWD_STAGE_EVENTS cudaEvent_t
  * handles recorded on the stream: [0] start, [1] gate and router gradients,
- * [2] weights transposed, [3] dh GEMM with the activation backward, [4] dx
- * GEMM, [5] shared expert data path, [6] dx assembled, [7] activations
- * packed, [8] dW2 GEMM, [9] dW1 / dW3 GEMMs, [10] bias, router and shared
- * expert weight gradients. */
-#define MOE_BWD_STAGE_EVENTS 11
+ * [2] dh GEMM with the activation backward, [3] dx GEMM, [4] shared expert
+ * data path, [5] dx assembled, [6] activations packed, [7] dW2 GEMM, [8]
+ * dW1 / dW3 GEMMs, [9] bias, router and shared expert weight gradients. */
+#define MOE_BWD_STAGE_EVENTS 10
 typedef struct {
     float aux_coef;
     float z_coef;

@@ -202,11 +202,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
-template <int M, int N>
+// The same for an MN-major operand tile (N contiguous in global memory):
+// TMA boxes of 64 K rows x 64 N elements (128 bytes, 128-byte swizzle), one
+// per 64-wide N block, 8 KB apart (LBO); 8-row K groups 1 KB apart (SBO).
+// One K=16 MMA step advances 16 rows = 2 KB.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(8192 >> 4) << 16;    // LBO: next 64-element N block
+    d |= (uint64_t)(1024 >> 4) << 32;    // SBO: next 8-row K group
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major; B
+// K-major, or MN-major with B_MN (the transpose-B bit).
+template <int M, int N, bool B_MN = false>
 struct IDesc {
-    static constexpr uint32_t value =
-        (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    static constexpr uint32_t value = (1u << 4) | (1u << 7) | (1u << 10) | (B_MN ? (1u << 16) : 0u) |
+                                      ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 };
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -258,6 +272,7 @@ struct Args {
     int64_t ld_pre;
     int kgroup;            // 1: groups split K (weight gradients), seg = per-group K offsets
     int64_t out_group_stride;  // K-grouped: elements between the groups' outputs
+    int k_split;           // MN-major B: K below k_split from tmB, the rest from tmB2
 };
 
 struct Tile {
@@ -532,14 +547,14 @@ __device__ __forceinline__ void route_epilogue(const Args &args, const Tile &tl,
 
 // EPI: 0 forward FFN epilogue; 8 / 16 / 32 routing epilogue (router GEMM,
 // E <= EPI); kEpiBwdGated / kEpiBwdAct activation backward.
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0>
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const Args args) {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES;
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
-    constexpr uint32_t IDESC = IDesc<BM, BN>::value;
+    constexpr uint32_t IDESC = IDesc<BM, BN, B_MN>::value;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -646,7 +661,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_expect_tx(&full[stage], C::STAGE_BYTES);
                 tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * BK, tl.row0);
-                if (GATED) {
+                if (B_MN) {
+                    // B[n][k] = W[g rows + k][n]: 64 x 64 boxes along N
+                    const bool lo = kb * BK < args.k_split;
+                    const int y = tl.g * args.b_group_rows + (lo ? kb * BK : kb * BK - args.k_split);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sB + stage * C::B_BYTES + j * 8192, lo ? &tmB : &tmB2, &full[stage],
+                                    tl.n0 + 64 * j, y);
+                } else if (GATED) {
                     tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * BK, brow);
                     tma_load_2d(sB + stage * C::B_BYTES + (BN / 2) * BK * 2, &tmB2, &full[stage], kb * BK, brow);
                 } else {
@@ -685,12 +708,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *consumed = *consumed + 1;
                 tc_fence_after();
                 const uint64_t adesc = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
-                const uint64_t bdesc = sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
+                const uint64_t bdesc = B_MN ? sdesc_sw128_mn(smem_u32(sB + stage * C::B_BYTES))
+                                            : sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                    // +32 bytes per K step inside the swizzle atom (encoded >> 4)
-                    umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
-                              (kb > kb0 || kk > 0) ? 1u : 0u);
+                    // K-major: +32 bytes per K step inside the swizzle atom;
+                    // MN-major: +16 rows of 128 bytes (encoded >> 4)
+                    umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * (B_MN ? 128 : 2)),
+                              IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty[stage]);
                 if (++stage == STAGES) {
@@ -1095,16 +1120,26 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0>
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false>
 cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     using C = Cfg<BN>;
     constexpr int BN_B = GATED ? BN / 2 : BN;   // rows per TMA box of B
     CUtensorMap ta, tb, tb2;
     if (!make_tmap(&ta, p.A, (uint64_t)p.K, (uint64_t)p.a_rows, BM)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, p.B, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) return cudaErrorInvalidValue;
+    if (B_MN) {
+        // B stored [groups * K rows][N cols] (N contiguous): 64 x 64 boxes
+        if (!make_tmap(&tb, p.B, (uint64_t)p.N, (uint64_t)p.b_rows_total, 64)) return cudaErrorInvalidValue;
+        if (p.B2) {
+            if (!make_tmap(&tb2, p.B2, (uint64_t)p.N, (uint64_t)p.b_rows_total, 64)) return cudaErrorInvalidValue;
+        } else {
+            tb2 = tb;
+        }
+    } else if (!make_tmap(&tb, p.B, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) {
+        return cudaErrorInvalidValue;
+    }
     if (GATED) {
         if (!make_tmap(&tb2, p.B2, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) return cudaErrorInvalidValue;
-    } else {
+    } else if (!B_MN) {
         tb2 = tb;
     }
     Args a{};
@@ -1127,8 +1162,13 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     a.ld_pre = p.ld_pre;
     a.kgroup = p.kgroup;
     a.out_group_stride = p.out_group_stride;
-    const size_t smem = C::smem_bytes(a.G);
-    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI>;
+    a.k_split = p.B2 ? p.k_split : p.K;
+    // MN-major B: the whole 227 KB are reserved, so that every shared-memory
+    // address the tensor cores derive from the descriptors lies inside the
+    // CTA's allocation
+    const size_t smem = B_MN ? (size_t)232448 : C::smem_bytes(a.G);
+    if (B_MN && C::smem_bytes(a.G) > smem) return cudaErrorInvalidValue;
+    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, s, ta, tb, tb2, a);
@@ -1214,8 +1254,16 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
     if (p.epi_bwd) {
         // dh = dy W2 with the activation backward in the epilogue (bf16 da out)
         if (p.out_f32 || p.gated || p.kgroup || !p.pre || p.bias) return cudaErrorInvalidValue;
+        if (p.b_mn)
+            return p.epi_bwd == 1 ? launch_t<256, false, false, kEpiBwdGated, true>(p, s)
+                                  : launch_t<256, false, false, kEpiBwdAct, true>(p, s);
         return p.epi_bwd == 1 ? launch_t<256, false, false, kEpiBwdGated>(p, s)
                               : launch_t<256, false, false, kEpiBwdAct>(p, s);
+    }
+    if (p.b_mn) {
+        // data gradient with the weights read in place (fp32 out)
+        if (p.gated || !p.out_f32 || p.kgroup || p.bias || p.K % 64 || p.N % 64) return cudaErrorInvalidValue;
+        return launch_t<256, false, true, 0, true>(p, s);
     }
     if (p.kgroup) {
         // weight gradients: fp32 out, one full M x N output per group

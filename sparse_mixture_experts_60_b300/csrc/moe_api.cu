@@ -145,24 +145,23 @@ BwdDims bwd_dims(const moe_config_t *c) {
     b.Tp = (b.T + 63) / 64 * 64;
     return b;
 }
-// Wide routers (E >= 64, E % 8 == 0) take the router's two products with
+// Wide routers (E a multiple of 64) take the router's two products with
 // the tensor cores (dlogits W_r for dx, dlogits^T x for dW_r).
-bool wide_router(const moe_config_t *c) { return c->num_experts >= 64 && c->num_experts % 8 == 0; }
+bool wide_router(const moe_config_t *c) { return c->num_experts >= 64 && c->num_experts % 64 == 0; }
 
 size_t bwd_ws(const moe_config_t *c) {
     const BwdDims b = bwd_dims(c);
     size_t n = align256(b.R * b.d * 2) + align256(b.T * b.k * 4) + align256(b.T * b.E * 4) +
                align256((b.E + 1) * 4) + align256(2 * 4);
-    n += align256(b.E * b.F * b.d * 2) + align256(b.E * b.d * b.nF * 2);      // W2^T, [W1 | W3]^T
     n += align256(b.R * b.nF * 2) + align256(b.R * b.d * 4);                  // da, dx_perm
     n += 2 * align256(b.d * b.Rp * 2) + align256(b.F * b.Rp * 2) + align256(b.nF * b.Rp * 2);
     n += align256((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
     if (c->num_shared || wide_router(c)) n += align256(b.d * b.Tp * 2);          // x^T
-    if (wide_router(c))   // dlogits hi / lo, W_r^T, the router's dx term, [hi | lo]^T, [x^T | x^T]
-        n += 2 * align256(b.T * b.E * 2) + align256(b.d * b.E * 2) + align256(b.T * b.d * 4) +
+    if (wide_router(c))   // dlogits hi / lo, the router's dx term, [hi | lo]^T, [x^T | x^T]
+        n += 2 * align256(b.T * b.E * 2) + align256(b.T * b.d * 4) +
              align256(b.E * 2 * b.Tp * 2) + align256(b.d * 2 * b.Tp * 2) + align256(2 * 4);
     if (c->num_shared) {
-        n += align256(b.T * b.nF * 2) + align256(b.T * b.d * 4) + align256(b.F * b.d * 2) + align256(b.d * b.nF * 2);
+        n += align256(b.T * b.nF * 2) + align256(b.T * b.d * 4);
         n += align256(b.d * b.Tp * 2) + align256(b.F * b.Tp * 2) + align256(b.nF * b.Tp * 2);
     }
     return n;
@@ -828,14 +827,19 @@ moe_status_t wgrad_gemm(const bf16 *A, int M, const bf16 *B, int N, int64_t Kp, 
     return cuda_status(launch_grouped_gemm(g, s), "weight-gradient GEMM launch");
 }
 
-// M-grouped data-gradient GEMM: out rows of group g = A rows x B_g^T.
+// M-grouped data-gradient GEMM with the weights read in place (MN-major B):
+// out rows of group g = A rows x W_g, W stored [G * K_g rows, N cols]; with
+// B2 the K columns from k_split on come from B2 (the [W1 | W3] stack).
 moe_status_t dgrad_gemm(const bf16 *A, int64_t a_rows, const int32_t *seg, int G, int M, const bf16 *B,
-                        int b_group_rows, int N, int K, void *out, int out_f32, int64_t ldo, bf16 *pre,
-                        int64_t ld_pre, int epi_bwd, int act, cudaStream_t s) {
+                        const bf16 *B2, int k_split, int b_group_rows, int N, int K, void *out, int out_f32,
+                        int64_t ldo, bf16 *pre, int64_t ld_pre, int epi_bwd, int act, cudaStream_t s) {
     GemmProblem g{};
     g.A = A;
     g.a_rows = a_rows;
     g.B = B;
+    g.B2 = B2;
+    g.k_split = k_split;
+    g.b_mn = 1;
     g.b_rows_total = (int64_t)G * b_group_rows;
     g.b_group_rows = b_group_rows;
     g.seg = seg;
@@ -870,8 +874,6 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
     float *dl = cv.take<float>(b.T * b.E * 4);
     int32_t *pad = cv.take<int32_t>((b.E + 1) * 4);
     int32_t *pad1 = cv.take<int32_t>(2 * 4);
-    bf16 *w2t = cv.take<bf16>(b.E * b.F * b.d * 2);
-    bf16 *w13t = cv.take<bf16>(b.E * b.d * b.nF * 2);
     bf16 *da = cv.take<bf16>(b.R * b.nF * 2);
     float *dxp = cv.take<float>(b.R * b.d * 4);
     bf16 *dyT = cv.take<bf16>(b.d * b.Rp * 2);
@@ -883,7 +885,6 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
     bf16 *xT = (c->num_shared || wide) ? cv.take<bf16>(b.d * b.Tp * 2) : nullptr;
     bf16 *dl_hi = wide ? cv.take<bf16>(b.T * b.E * 2) : nullptr;
     bf16 *dl_lo = wide ? cv.take<bf16>(b.T * b.E * 2) : nullptr;
-    bf16 *wrT = wide ? cv.take<bf16>(b.d * b.E * 2) : nullptr;
     float *dxr = wide ? cv.take<float>(b.T * b.d * 4) : nullptr;
     bf16 *dlT2 = wide ? cv.take<bf16>(b.E * 2 * b.Tp * 2) : nullptr;
     bf16 *xT2 = wide ? cv.take<bf16>(b.d * 2 * b.Tp * 2) : nullptr;
@@ -899,48 +900,36 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
                          aux_coef, z_coef, dl, dl_hi, dl_lo, s),
        "router backward");
     if (wide) {
-        // dx's router term dlogits W_r on the tensor cores (K = E)
-        CU(launch_transpose_batched(static_cast<const bf16 *>(w->w_router), 0, d, E, d, 1, wrT, 0, E, 0, s),
-           "W_r transpose");
-        TRY(dgrad_gemm(dl_hi, b.T, nullptr, 1, (int)b.T, wrT, d, d, E, dxr, 1, d, nullptr, 0, 0, 0, s));
+        // dx's router term dlogits W_r on the tensor cores (K = E, W_r read in place)
+        TRY(dgrad_gemm(dl_hi, b.T, nullptr, 1, (int)b.T, static_cast<const bf16 *>(w->w_router), nullptr, E, E, d,
+                       E, dxr, 1, d, nullptr, 0, 0, 0, s));
     }
     mark(1);
-    // weights to the K-major layouts of the data-gradient GEMMs
-    CU(launch_transpose_batched(W2, (int64_t)d * F, F, d, F, E, w2t, (int64_t)F * d, d, 0, s), "W2 transpose");
-    CU(launch_transpose_batched(W1, (int64_t)F * d, d, F, d, E, w13t, (int64_t)d * nF, nF, 0, s), "W1 transpose");
-    if (gated)
-        CU(launch_transpose_batched(W3, (int64_t)F * d, d, F, d, E, w13t, (int64_t)d * nF, nF, F, s), "W3 transpose");
-    mark(2);
     // dh = dy W2 -> da (activation backward in the epilogue); dx_perm = da [W1 | W3]
-    TRY(dgrad_gemm(dy, b.R, sv->offsets, E, 0, w2t, F, F, d, da, 0, nF,
+    TRY(dgrad_gemm(dy, b.R, sv->offsets, E, 0, W2, nullptr, d, d, F, d, da, 0, nF,
                    const_cast<bf16 *>(static_cast<const bf16 *>(sv->pre_act)), nF, epi, act, s));
+    mark(2);
+    TRY(dgrad_gemm(da, b.R, sv->offsets, E, 0, W1, gated ? W3 : nullptr, F, F, d, nF, dxp, 1, d, nullptr, 0, 0, 0,
+                   s));
     mark(3);
-    TRY(dgrad_gemm(da, b.R, sv->offsets, E, 0, w13t, d, d, nF, dxp, 1, d, nullptr, 0, 0, 0, s));
-    mark(4);
     // shared expert: gate 1, A = dout
     float *dxs = nullptr;
     bf16 *das = nullptr;
     if (c->num_shared) {
         das = cv.take<bf16>(b.T * b.nF * 2);
         dxs = cv.take<float>(b.T * b.d * 4);
-        bf16 *w2st = cv.take<bf16>(b.F * b.d * 2);
-        bf16 *w13st = cv.take<bf16>(b.d * b.nF * 2);
-        CU(launch_transpose_batched(static_cast<const bf16 *>(w->shared_w2), 0, F, d, F, 1, w2st, 0, d, 0, s),
-           "shared W2 transpose");
-        CU(launch_transpose_batched(static_cast<const bf16 *>(w->shared_w1), 0, d, F, d, 1, w13st, 0, nF, 0, s),
-           "shared W1 transpose");
-        if (gated)
-            CU(launch_transpose_batched(static_cast<const bf16 *>(w->shared_w3), 0, d, F, d, 1, w13st, 0, nF, F, s),
-               "shared W3 transpose");
-        TRY(dgrad_gemm(go, b.T, nullptr, 1, (int)b.T, w2st, F, F, d, das, 0, nF,
-                       const_cast<bf16 *>(static_cast<const bf16 *>(sv->shared_pre_act)), nF, epi, act, s));
-        TRY(dgrad_gemm(das, b.T, nullptr, 1, (int)b.T, w13st, d, d, nF, dxs, 1, d, nullptr, 0, 0, 0, s));
+        const bf16 *SW1 = static_cast<const bf16 *>(w->shared_w1), *SW3 = static_cast<const bf16 *>(w->shared_w3);
+        TRY(dgrad_gemm(go, b.T, nullptr, 1, (int)b.T, static_cast<const bf16 *>(w->shared_w2), nullptr, d, d, F, d,
+                       das, 0, nF, const_cast<bf16 *>(static_cast<const bf16 *>(sv->shared_pre_act)), nF, epi, act,
+                       s));
+        TRY(dgrad_gemm(das, b.T, nullptr, 1, (int)b.T, SW1, gated ? SW3 : nullptr, F, F, d, nF, dxs, 1, d, nullptr,
+                       0, 0, 0, s));
     }
-    mark(5);
+    mark(4);
     CU(launch_dx_assemble(b.T, d, (int)b.k, E, dxp, sv->inv, go, c->residual, dxs, dl,
                           static_cast<const bf16 *>(w->w_router), dxr, gr->dx, s),
        "dx assembly");
-    mark(6);
+    mark(5);
     // weight gradients over the experts' rows, packed K-major and padded
     CU(launch_pad_offsets(sv->offsets, E, 0, pad, s), "padded offsets");
     CU(launch_transpose_pack(dy, d, d, sv->offsets, pad, E, 0, b.Rp, dyT, b.Rp, s), "dy pack");
@@ -951,12 +940,12 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
                              s),
        "H pack");
     CU(launch_transpose_pack(da, nF, nF, sv->offsets, pad, E, 0, b.Rp, daT, b.Rp, s), "da pack");
-    mark(7);
+    mark(6);
     if (gr->dw2) TRY(wgrad_gemm(dyT, d, hT, F, b.Rp, pad, E, gr->dw2, s));
-    mark(8);
+    mark(7);
     if (gr->dw1) TRY(wgrad_gemm(daT, F, xpT, d, b.Rp, pad, E, gr->dw1, s));
     if (gated && gr->dw3) TRY(wgrad_gemm(daT + b.F * b.Rp, F, xpT, d, b.Rp, pad, E, gr->dw3, s));
-    mark(9);
+    mark(8);
     if (!gated && gr->db1) CU(launch_group_rowsum(daT, b.Rp, pad, E, F, gr->db1, s), "db1");
     if (!gated && gr->db2) CU(launch_group_rowsum(dyT, b.Rp, pad, E, d, gr->db2, s), "db2");
     const int Ti = (int)b.T;
@@ -999,7 +988,7 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
         if (gated && gr->shared_dw3) TRY(wgrad_gemm(dasT + b.F * b.Tp, F, xT, d, b.Tp, pad1, 1, gr->shared_dw3, s));
     }
 #undef CU
-    mark(10);
+    mark(9);
     return MOE_OK;
 }
 

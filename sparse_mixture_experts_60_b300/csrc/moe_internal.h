@@ -168,6 +168,10 @@ struct GemmProblem {
     // K-grouped (weight gradients): A [M, K], B [N, K]; group g sums over
     // K columns seg[g] .. seg[g+1]-1 (multiples of 64) into out + g * out_group_stride
     int kgroup; int64_t out_group_stride;
+    // MN-major B (data gradients from the stored weights): B [G * K_g rows,
+    // N cols]; group g's K rows start at g * b_group_rows; with B2 the K
+    // columns from k_split on come from B2 (the [W1 | W3] stack)
+    int b_mn; int k_split;
 };
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
 bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias);
