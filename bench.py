@@ -393,7 +393,7 @@ def run_ours(args, w, rank, world, local):
 
 
 # ---------------------------------------------------------------------- training step
-BWD_STAGES = ["gate_router", "dh_gemm", "dx_gemm", "shared", "dx_assemble", "pack", "dw2_gemm", "dw13_gemm",
+BWD_STAGES = ["gate_router", "dh_gemm", "dx_gemm", "shared", "dx_assemble", "dw2_gemm", "dw13_gemm",
               "bias_router_shared"]
 
 
@@ -405,14 +405,13 @@ def bwd_launches(w):
     n += 2                                           # dh, dx GEMMs (weights read in place)
     if w.num_shared:
         n += 2
-    n += 1 + 1 + 4 + 1 + (2 if gated else 1)         # dx assembly, offsets, packs, dW2, dW1 (+ dW3)
+    n += 1                                           # dx assembly
+    n += 2 + (1 if gated else 0)                     # dW2, dW1 (+ dW3), activations read in place
     if w.expert_bias and not gated:
-        n += 2
-    if w.num_shared or wide:
-        n += 2                                       # token offsets, x pack
-    n += 7 if wide else 2                            # router weight gradient (wide: offsets, 4 packs, GEMM, db)
+        n += 2                                       # db1, db2
+    n += 8 if wide else 2                            # router weights (wide: offsets x2, 4 packs, GEMM, db)
     if w.num_shared:
-        n += 3 + (3 if gated else 2)
+        n += 1 + 2 + (1 if gated else 0)             # token range, shared dW2, dW1 (+ dW3)
     return n
 
 
@@ -484,7 +483,7 @@ def run_train(args, w, rank, world, local):
         total_ms, fe, be, clocks = timed()
         clocks["remeasured"] = True
     fst = np.array([[fe[i][j].elapsed_time(fe[i][j + 1]) for j in range(7)] for i in range(args.steps)]).mean(0)
-    bst = np.array([[be[i][j].elapsed_time(be[i][j + 1]) for j in range(9)] for i in range(args.steps)]).mean(0)
+    bst = np.array([[be[i][j].elapsed_time(be[i][j + 1]) for j in range(8)] for i in range(args.steps)]).mean(0)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms = total_ms / args.steps
     kept = int(layer.stats()["total_kept"])

@@ -467,9 +467,9 @@ typedef struct {
  * stage_events: optional host array of MOE_BWD_STAGE_EVENTS cudaEvent_t
  * handles recorded on the stream: [0] start, [1] gate and router gradients,
  * [2] dh GEMM with the activation backward, [3] dx GEMM, [4] shared expert
- * data path, [5] dx assembled, [6] activations packed, [7] dW2 GEMM, [8]
- * dW1 / dW3 GEMMs, [9] bias, router and shared expert weight gradients. */
-#define MOE_BWD_STAGE_EVENTS 10
+ * data path, [5] dx assembled, [6] dW2 GEMM, [7] dW1 / dW3 GEMMs, [8] bias,
+ * router and shared expert weight gradients. */
+#define MOE_BWD_STAGE_EVENTS 9
 typedef struct {
     float aux_coef;
     float z_coef;

@@ -64,7 +64,7 @@ class MoEECIO(C.Structure):
                                           "stage_events")]
 
 
-MOE_BWD_STAGE_EVENTS = 10
+MOE_BWD_STAGE_EVENTS = 9
 
 
 class MoEBackwardOpts(C.Structure):

@@ -461,7 +461,47 @@ __global__ void __launch_bounds__(256) group_rowsum_kernel(const bf16 *__restric
     if (lane == 0) out[(int64_t)g * C + c] = s;
 }
 
+// Per-group column sums of a row-major bf16 matrix (bias gradients):
+// out[g][c] = sum over rows off[g] .. off[g+1]-1 of in[r][c], thread per
+// column, rows in order (deterministic).
+__global__ void __launch_bounds__(256) group_colsum_kernel(const bf16 *__restrict__ in, int64_t ld,
+                                                           const int32_t *__restrict__ off, int C,
+                                                           float *__restrict__ out) {
+    PDL_ENTER();
+    const int g = blockIdx.y;
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    if (c >= C) return;
+    const int r0 = off[g], r1 = off[g + 1];
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    int r = r0;
+    for (; r + 3 < r1; r += 4) {
+        s0 += __bfloat162float(in[(int64_t)r * ld + c]);
+        s1 += __bfloat162float(in[(int64_t)(r + 1) * ld + c]);
+        s2 += __bfloat162float(in[(int64_t)(r + 2) * ld + c]);
+        s3 += __bfloat162float(in[(int64_t)(r + 3) * ld + c]);
+    }
+    for (; r < r1; ++r) s0 += __bfloat162float(in[(int64_t)r * ld + c]);
+    out[(int64_t)g * C + c] = (s0 + s1) + (s2 + s3);
+}
+
+__global__ void fill_range_kernel(int32_t *seg, int n) {
+    PDL_ENTER();
+    seg[0] = 0;
+    seg[1] = n;
+}
+
 }  // namespace
+
+cudaError_t launch_group_colsum(const bf16 *in, int64_t ld, const int32_t *off, int G, int C, float *out,
+                                cudaStream_t s) {
+    if ((int64_t)G * C == 0) return cudaSuccess;
+    return launch_pdl(group_colsum_kernel, dim3((unsigned)ceil_div(C, 256), (unsigned)G), dim3(256), 0, s, in, ld,
+                      off, C, out);
+}
+
+cudaError_t launch_fill_range(int32_t *seg, int n, cudaStream_t s) {
+    return launch_pdl(fill_range_kernel, dim3(1), dim3(1), 0, s, seg, n);
+}
 
 cudaError_t launch_combine_bwd(int64_t T, int d, int k, const bf16 *dout, const float *topk_w, const int32_t *inv,
                                const float *y, bf16 *dy, float *dgate, cudaStream_t s) {

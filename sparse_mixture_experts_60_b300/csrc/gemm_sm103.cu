@@ -215,12 +215,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major; B
-// K-major, or MN-major with B_MN (the transpose-B bit).
-template <int M, int N, bool B_MN = false>
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, each K-major or
+// MN-major (the transpose-A / transpose-B bits).
+template <int M, int N, bool B_MN = false, bool A_MN = false>
 struct IDesc {
-    static constexpr uint32_t value = (1u << 4) | (1u << 7) | (1u << 10) | (B_MN ? (1u << 16) : 0u) |
-                                      ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    static constexpr uint32_t value = (1u << 4) | (1u << 7) | (1u << 10) | (A_MN ? (1u << 15) : 0u) |
+                                      (B_MN ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) |
+                                      ((uint32_t)(M >> 4) << 24);
 };
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -397,6 +398,20 @@ __device__ __forceinline__ Tile tile_of(const Args &args, int tile, const int *s
     return t;
 }
 
+// K blocks of a tile: M-grouped, all of K; K-grouped, the group's K range
+// (64-aligned offsets, block = column / 64); K-grouped MN-major, the
+// group's rows seg[g] .. seg[g+1]-1 in blocks of 64 from seg[g] (the last
+// block partial).
+struct KRange {
+    int kb0, kb1;
+};
+template <bool KG_MN>
+__device__ __forceinline__ KRange k_range(const Args &args, const Tile &tl, const int *seg_s, int num_kb) {
+    if (KG_MN) return {0, (seg_s[tl.g + 1] - seg_s[tl.g] + BK - 1) / BK};
+    if (args.kgroup) return {seg_s[tl.g] / BK, seg_s[tl.g + 1] / BK};
+    return {0, num_kb};
+}
+
 // Epilogue modes beyond the forward FFN: the activation backward of the
 // first expert GEMM, fused into the GEMM that produces dh = dy W2.
 constexpr int kEpiBwdGated = 100;   // SwiGLU: da1 = dh a3 silu'(a1), da3 = dh silu(a1)
@@ -547,14 +562,18 @@ __device__ __forceinline__ void route_epilogue(const Args &args, const Tile &tl,
 
 // EPI: 0 forward FFN epilogue; 8 / 16 / 32 routing epilogue (router GEMM,
 // E <= EPI); kEpiBwdGated / kEpiBwdAct activation backward.
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false>
-__global__ void __launch_bounds__(kThreads, 1)
+// KG_MN: K-grouped with both operands MN-major, read in place from the
+// row-major token tensors (A [rows, M], B [rows, N]); the group's rows are
+// its K range in blocks of 64 from seg[g], and a fixer warp zeroes the K
+// rows of a group's last block that belong to the next group.
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false>
+__global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const Args args) {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES;
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
-    constexpr uint32_t IDESC = IDesc<BM, BN, B_MN>::value;
+    constexpr uint32_t IDESC = IDesc<BM, BN, B_MN || KG_MN, KG_MN>::value;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -570,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *consumed = abort_flag + 1;
+    uint64_t *fixed = bars + 16;           // [STAGES] KG_MN: stage ready for the MMA
     int *seg_s = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES + C::BAR_BYTES);
     int *pre_s = seg_s + (args.G + 1);
 
@@ -579,7 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            // KG_MN: a stage is free once the MMAs are done and the fixer has seen it
+            mbar_init(&empty[i], KG_MN ? 2 : 1);
+            if (KG_MN) mbar_init(&fixed[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -595,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
     PDL_ENTER();   // the segment offsets and A are the previous kernel's output
-    for (int i = threadIdx.x; i <= G; i += kThreads)
+    for (int i = threadIdx.x; i <= G; i += blockDim.x)
         seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
     // tile prefix over groups: n_tiles * ceil(rows_g / BM); K-grouped: every
@@ -614,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rows = seg_s[g + 1] - seg_s[g];
                 bad |= rows < 0;
                 if (args.kgroup) {
-                    bad |= (seg_s[g] % BK) != 0 || (seg_s[g + 1] % BK) != 0;
+                    if (!KG_MN) bad |= (seg_s[g] % BK) != 0 || (seg_s[g + 1] % BK) != 0;
                     v = kg_tiles;
                 } else {
                     v = rows > 0 ? ((rows + BM - 1) / BM) * n_tiles : 0;
@@ -651,15 +673,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
             const int brow = args.kgroup ? tl.n0 : tl.g * args.b_group_rows + tl.n0;
-            const int kb0 = args.kgroup ? seg_s[tl.g] / BK : 0;
-            const int kb1 = args.kgroup ? seg_s[tl.g + 1] / BK : num_kb;
+            const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
             bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, args.err)) {
                     ok = false;
                     break;
                 }
                 mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+                if (KG_MN) {
+                    // token rows seg[g] + 64 kb .. as K: 64 x 64 boxes along M and N
+                    const int y = seg_s[tl.g] + kb * BK;
+#pragma unroll
+                    for (int j = 0; j < BM / 64; ++j)
+                        tma_load_2d(sA + stage * C::A_BYTES + j * 8192, &tmA, &full[stage], tl.row0 + 64 * j, y);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sB + stage * C::B_BYTES + j * 8192, &tmB, &full[stage], tl.n0 + 64 * j, y);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                    continue;
+                }
                 tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * BK, tl.row0);
                 if (B_MN) {
                     // B[n][k] = W[g rows + k][n]: 64 x 64 boxes along N
@@ -686,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         int stage = 0;
-        uint32_t ph = 0;
+        uint32_t ph = 0, fph = 0;
         int acc = 0;
         uint32_t aph = 0;
         bool ok = true;
@@ -694,28 +731,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            int kb0 = 0, kb1 = num_kb;
-            if (args.kgroup) {
-                const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
-                kb0 = seg_s[tl.g] / BK;
-                kb1 = seg_s[tl.g + 1] / BK;
-            }
+            const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
+            const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
+            const int kb0 = kr.kb0, kb1 = kr.kb1;
+            // KG_MN: a group's partial last block waits for the fixer, the rest for TMA
+            const int kg_rows = KG_MN ? seg_s[tl.g + 1] - seg_s[tl.g] : 0;
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait(&full[stage], ph, abort_flag, args.err)) {
+                // fixed[] completes only on tail blocks: its parity is tracked per stage
+                const bool tail = KG_MN && kg_rows - kb * BK < BK;
+                const uint32_t par = tail ? (fph >> stage) & 1u : ph;
+                if (tail) fph ^= 1u << stage;
+                if (!mbar_wait(tail ? &fixed[stage] : &full[stage], par, abort_flag, args.err)) {
                     ok = false;
                     break;
                 }
                 *consumed = *consumed + 1;
                 tc_fence_after();
-                const uint64_t adesc = sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
-                const uint64_t bdesc = B_MN ? sdesc_sw128_mn(smem_u32(sB + stage * C::B_BYTES))
-                                            : sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
+                const uint64_t adesc = KG_MN ? sdesc_sw128_mn(smem_u32(sA + stage * C::A_BYTES))
+                                             : sdesc_sw128(smem_u32(sA + stage * C::A_BYTES));
+                const uint64_t bdesc = (B_MN || KG_MN) ? sdesc_sw128_mn(smem_u32(sB + stage * C::B_BYTES))
+                                                       : sdesc_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                     // K-major: +32 bytes per K step inside the swizzle atom;
                     // MN-major: +16 rows of 128 bytes (encoded >> 4)
-                    umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * (B_MN ? 128 : 2)),
-                              IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    umma_bf16(d_tmem, adesc + (uint64_t)(kk * (KG_MN ? 128 : 2)),
+                              bdesc + (uint64_t)(kk * ((B_MN || KG_MN) ? 128 : 2)), IDESC,
+                              (kb > kb0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&empty[stage]);
                 if (++stage == STAGES) {
@@ -728,7 +770,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
-    } else if (warp >= 2) {
+    } else if (KG_MN && warp == 2 + kEpiWarps) {
+        // ------------------------------------------------ K-tail fixer
+        // A group's last K block may reach into the next group's rows: those
+        // K rows of A are zeroed (whole 128-byte lines of each 64-column box;
+        // a zero row of A zeroes the row's products), and of B too where the
+        // block runs past the last group's rows (unwritten memory), before
+        // the MMA reads the stage; the proxy fence makes the zeros visible to
+        // the tensor cores.  Full blocks go to the MMA straight from TMA; the
+        // fixer still observes every stage and frees it together with the
+        // MMA (empty counts both), so it never falls a ring cycle behind.
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
+            const int rows = seg_s[tl.g + 1] - seg_s[tl.g];
+            const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
+            for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], ph, abort_flag, args.err))) {
+                    ok = false;
+                    break;
+                }
+                const int valid = rows - kb * BK;
+                if (valid < BK) {
+                    const int bad_rows = BK - valid;
+                    const bool past_end = seg_s[tl.g] + kb * BK + BK > seg_s[G];
+                    const int boxes = BM / 64 + (past_end ? BN / 64 : 0);
+                    const int lines = bad_rows * boxes;
+                    for (int i = lane; i < lines * 8; i += 32) {
+                        const int line = i >> 3, chunk = i & 7;
+                        const int box = line / bad_rows, r = valid + line % bad_rows;
+                        uint8_t *base = box < BM / 64 ? sA + stage * C::A_BYTES + box * 8192
+                                                      : sB + stage * C::B_BYTES + (box - BM / 64) * 8192;
+                        *reinterpret_cast<uint4 *>(base + r * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&fixed[stage]);
+                }
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
         // ------------------------------------------------ epilogue
         // Thread = accumulator row.  Warps w and w+4 share a TMEM lane
         // quadrant and take alternate 32-column chunks.  Output leaves through
@@ -1107,11 +1195,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor [rows, inner] (row-major), box [box_rows, 64], 128-byte swizzle.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+               uint64_t ld = 0) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
+    cuuint64_t strides[1] = {(ld ? ld : inner) * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -1120,13 +1209,20 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false>
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false>
 cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     using C = Cfg<BN>;
     constexpr int BN_B = GATED ? BN / 2 : BN;   // rows per TMA box of B
     CUtensorMap ta, tb, tb2;
-    if (!make_tmap(&ta, p.A, (uint64_t)p.K, (uint64_t)p.a_rows, BM)) return cudaErrorInvalidValue;
-    if (B_MN) {
+    if (KG_MN) {
+        // A [K rows, M cols] and B [K rows, N cols], row strides lda / ldb
+        if (!make_tmap(&ta, p.A, (uint64_t)p.M, (uint64_t)p.K, 64, (uint64_t)p.lda)) return cudaErrorInvalidValue;
+        if (!make_tmap(&tb, p.B, (uint64_t)p.N, (uint64_t)p.K, 64, (uint64_t)p.ldb)) return cudaErrorInvalidValue;
+        tb2 = tb;
+    } else if (!make_tmap(&ta, p.A, (uint64_t)p.K, (uint64_t)p.a_rows, BM)) {
+        return cudaErrorInvalidValue;
+    }
+    if (B_MN && !KG_MN) {
         // B stored [groups * K rows][N cols] (N contiguous): 64 x 64 boxes
         if (!make_tmap(&tb, p.B, (uint64_t)p.N, (uint64_t)p.b_rows_total, 64)) return cudaErrorInvalidValue;
         if (p.B2) {
@@ -1134,12 +1230,12 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
         } else {
             tb2 = tb;
         }
-    } else if (!make_tmap(&tb, p.B, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) {
+    } else if (!KG_MN && !make_tmap(&tb, p.B, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) {
         return cudaErrorInvalidValue;
     }
     if (GATED) {
         if (!make_tmap(&tb2, p.B2, (uint64_t)p.K, (uint64_t)p.b_rows_total, BN_B)) return cudaErrorInvalidValue;
-    } else if (!B_MN) {
+    } else if (!B_MN && !KG_MN) {
         tb2 = tb;
     }
     Args a{};
@@ -1166,12 +1262,12 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     // MN-major B: the whole 227 KB are reserved, so that every shared-memory
     // address the tensor cores derive from the descriptors lies inside the
     // CTA's allocation
-    const size_t smem = B_MN ? (size_t)232448 : C::smem_bytes(a.G);
-    if (B_MN && C::smem_bytes(a.G) > smem) return cudaErrorInvalidValue;
-    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI, B_MN>;
+    const size_t smem = (B_MN || KG_MN) ? (size_t)232448 : C::smem_bytes(a.G);
+    if ((B_MN || KG_MN) && C::smem_bytes(a.G) > smem) return cudaErrorInvalidValue;
+    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI, B_MN, KG_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, s, ta, tb, tb2, a);
+    return launch_pdl(kern, dim3(num_sms()), dim3(KG_MN ? kThreads + 32 : kThreads), smem, s, ta, tb, tb2, a);
 }
 
 template <int BN, bool GATED, bool OUT_F32>
@@ -1250,7 +1346,10 @@ bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias) 
 }
 
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
-    if (!grouped_gemm_supported(p.N, p.K, p.gated, p.out_f32, p.bias != nullptr)) return cudaErrorInvalidValue;
+    // K-grouped MN-major: K is the rows (the outer TMA dimension), any count
+    const bool ok = p.kgroup && p.kg_mn ? (p.out_f32 && p.N % 4 == 0 && p.K >= 0)
+                                        : grouped_gemm_supported(p.N, p.K, p.gated, p.out_f32, p.bias != nullptr);
+    if (!ok) return cudaErrorInvalidValue;
     if (p.epi_bwd) {
         // dh = dy W2 with the activation backward in the epilogue (bf16 da out)
         if (p.out_f32 || p.gated || p.kgroup || !p.pre || p.bias) return cudaErrorInvalidValue;
@@ -1268,6 +1367,10 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
     if (p.kgroup) {
         // weight gradients: fp32 out, one full M x N output per group
         if (p.gated || !p.out_f32 || p.bias || !p.seg) return cudaErrorInvalidValue;
+        if (p.kg_mn) {
+            if (p.M % 64 || p.N % 64 || p.lda % 8 || p.ldb % 8) return cudaErrorInvalidValue;
+            return launch_t<256, false, true, 0, false, true>(p, s);
+        }
         return launch_t<256, false, true>(p, s);
     }
     if (p.route) {

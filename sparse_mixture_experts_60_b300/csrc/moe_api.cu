@@ -126,9 +126,8 @@ size_t ec_ws(const moe_config_t *c) {
     return n;
 }
 
-// Backward workspace: R = T k expert rows; every expert's rows padded to a
-// multiple of 64 in the packed transposes (Rp columns), the shared expert's
-// T tokens to Tp.
+// Backward workspace: R = T k expert rows; the wide router's dlogits and x
+// are packed K-major with the T tokens padded to Tp.
 struct BwdDims {
     int64_t T, d, E, k, F, nF, R, Rp, Tp;
 };
@@ -154,16 +153,11 @@ size_t bwd_ws(const moe_config_t *c) {
     size_t n = align256(b.R * b.d * 2) + align256(b.T * b.k * 4) + align256(b.T * b.E * 4) +
                align256((b.E + 1) * 4) + align256(2 * 4);
     n += align256(b.R * b.nF * 2) + align256(b.R * b.d * 4);                  // da, dx_perm
-    n += 2 * align256(b.d * b.Rp * 2) + align256(b.F * b.Rp * 2) + align256(b.nF * b.Rp * 2);
     n += align256((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
-    if (c->num_shared || wide_router(c)) n += align256(b.d * b.Tp * 2);          // x^T
     if (wide_router(c))   // dlogits hi / lo, the router's dx term, [hi | lo]^T, [x^T | x^T]
         n += 2 * align256(b.T * b.E * 2) + align256(b.T * b.d * 4) +
              align256(b.E * 2 * b.Tp * 2) + align256(b.d * 2 * b.Tp * 2) + align256(2 * 4);
-    if (c->num_shared) {
-        n += align256(b.T * b.nF * 2) + align256(b.T * b.d * 4);
-        n += align256(b.d * b.Tp * 2) + align256(b.F * b.Tp * 2) + align256(b.nF * b.Tp * 2);
-    }
+    if (c->num_shared) n += align256(b.T * b.nF * 2) + align256(b.T * b.d * 4);
     return n;
 }
 
@@ -827,6 +821,32 @@ moe_status_t wgrad_gemm(const bf16 *A, int M, const bf16 *B, int N, int64_t Kp, 
     return cuda_status(launch_grouped_gemm(g, s), "weight-gradient GEMM launch");
 }
 
+// K-grouped weight-gradient GEMM with both operands read in place (MN-major):
+// out[g] (M x N, fp32) = A[rows_g, :M]^T B[rows_g, :N], rows_g = seg[g] ..
+// seg[g+1]-1 of the row-major A (row stride lda) and B (ldb); K = rows.
+moe_status_t wgrad_gemm_rows(const bf16 *A, int64_t lda, int M, const bf16 *B, int64_t ldb, int N, int64_t rows,
+                             const int32_t *seg, int G, float *out, cudaStream_t s) {
+    GemmProblem g{};
+    g.A = A;
+    g.a_rows = rows;
+    g.B = B;
+    g.b_rows_total = rows;
+    g.seg = seg;
+    g.G = G;
+    g.M = M;
+    g.N = N;
+    g.K = (int)rows;
+    g.out = out;
+    g.ldo = N;
+    g.out_f32 = 1;
+    g.kgroup = 1;
+    g.kg_mn = 1;
+    g.lda = lda;
+    g.ldb = ldb;
+    g.out_group_stride = (int64_t)M * N;
+    return cuda_status(launch_grouped_gemm(g, s), "weight-gradient GEMM launch");
+}
+
 // M-grouped data-gradient GEMM with the weights read in place (MN-major B):
 // out rows of group g = A rows x W_g, W stored [G * K_g rows, N cols]; with
 // B2 the K columns from k_split on come from B2 (the [W1 | W3] stack).
@@ -876,13 +896,8 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
     int32_t *pad1 = cv.take<int32_t>(2 * 4);
     bf16 *da = cv.take<bf16>(b.R * b.nF * 2);
     float *dxp = cv.take<float>(b.R * b.d * 4);
-    bf16 *dyT = cv.take<bf16>(b.d * b.Rp * 2);
-    bf16 *xpT = cv.take<bf16>(b.d * b.Rp * 2);
-    bf16 *hT = cv.take<bf16>(b.F * b.Rp * 2);
-    bf16 *daT = cv.take<bf16>(b.nF * b.Rp * 2);
     float *rwpart = cv.take<float>((size_t)router_wgrad_chunks(b.T) * b.E * b.d * 4);
     const bool wide = wide_router(c);
-    bf16 *xT = (c->num_shared || wide) ? cv.take<bf16>(b.d * b.Tp * 2) : nullptr;
     bf16 *dl_hi = wide ? cv.take<bf16>(b.T * b.E * 2) : nullptr;
     bf16 *dl_lo = wide ? cv.take<bf16>(b.T * b.E * 2) : nullptr;
     float *dxr = wide ? cv.take<float>(b.T * b.d * 4) : nullptr;
@@ -930,31 +945,18 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
                           static_cast<const bf16 *>(w->w_router), dxr, gr->dx, s),
        "dx assembly");
     mark(5);
-    // weight gradients over the experts' rows, packed K-major and padded
-    CU(launch_pad_offsets(sv->offsets, E, 0, pad, s), "padded offsets");
-    CU(launch_transpose_pack(dy, d, d, sv->offsets, pad, E, 0, b.Rp, dyT, b.Rp, s), "dy pack");
-    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->x_perm), d, d, sv->offsets, pad, E, 0, b.Rp, xpT, b.Rp,
-                             s),
-       "x_perm pack");
-    CU(launch_transpose_pack(static_cast<const bf16 *>(sv->hidden), F, F, sv->offsets, pad, E, 0, b.Rp, hT, b.Rp,
-                             s),
-       "H pack");
-    CU(launch_transpose_pack(da, nF, nF, sv->offsets, pad, E, 0, b.Rp, daT, b.Rp, s), "da pack");
+    // weight gradients over the experts' rows, read in place (K = the rows)
+    const bf16 *XP = static_cast<const bf16 *>(sv->x_perm), *H = static_cast<const bf16 *>(sv->hidden);
+    if (gr->dw2) TRY(wgrad_gemm_rows(dy, d, d, H, F, F, b.R, sv->offsets, E, gr->dw2, s));
     mark(6);
-    if (gr->dw2) TRY(wgrad_gemm(dyT, d, hT, F, b.Rp, pad, E, gr->dw2, s));
+    if (gr->dw1) TRY(wgrad_gemm_rows(da, nF, F, XP, d, d, b.R, sv->offsets, E, gr->dw1, s));
+    if (gated && gr->dw3) TRY(wgrad_gemm_rows(da + F, nF, F, XP, d, d, b.R, sv->offsets, E, gr->dw3, s));
     mark(7);
-    if (gr->dw1) TRY(wgrad_gemm(daT, F, xpT, d, b.Rp, pad, E, gr->dw1, s));
-    if (gated && gr->dw3) TRY(wgrad_gemm(daT + b.F * b.Rp, F, xpT, d, b.Rp, pad, E, gr->dw3, s));
-    mark(8);
-    if (!gated && gr->db1) CU(launch_group_rowsum(daT, b.Rp, pad, E, F, gr->db1, s), "db1");
-    if (!gated && gr->db2) CU(launch_group_rowsum(dyT, b.Rp, pad, E, d, gr->db2, s), "db2");
+    if (!gated && gr->db1) CU(launch_group_colsum(da, nF, sv->offsets, E, F, gr->db1, s), "db1");
+    if (!gated && gr->db2) CU(launch_group_colsum(dy, d, sv->offsets, E, d, gr->db2, s), "db2");
     const int Ti = (int)b.T;
-    if (xT) {
-        CU(launch_pad_offsets(nullptr, 1, Ti, pad1, s), "token padded offsets");
-        CU(launch_transpose_pack(static_cast<const bf16 *>(x), d, d, nullptr, pad1, 1, Ti, b.Tp, xT, b.Tp, s),
-           "x pack");
-    }
     if (wide) {
+        CU(launch_pad_offsets(nullptr, 1, Ti, pad1, s), "token padded offsets");
         // dW_r = dlogits^T x on the tensor cores, one group over K = 2 Tp:
         // [hi | lo]^T against [x^T | x^T], so dlogits keeps ~16 bits
         CU(launch_pad_offsets(nullptr, 1, 2 * (int)b.Tp, pad2, s), "router K offsets");   // {0, 2 Tp}
@@ -975,20 +977,15 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
            "router weight gradient");
     }
     if (c->num_shared && (gr->shared_dw1 || gr->shared_dw2 || gr->shared_dw3)) {
-        bf16 *goT = cv.take<bf16>(b.d * b.Tp * 2);
-        bf16 *shT = cv.take<bf16>(b.F * b.Tp * 2);
-        bf16 *dasT = cv.take<bf16>(b.nF * b.Tp * 2);
-        CU(launch_transpose_pack(go, d, d, nullptr, pad1, 1, Ti, b.Tp, goT, b.Tp, s), "dout pack");
-        CU(launch_transpose_pack(static_cast<const bf16 *>(sv->shared_hidden), F, F, nullptr, pad1, 1, Ti, b.Tp, shT,
-                                 b.Tp, s),
-           "shared H pack");
-        CU(launch_transpose_pack(das, nF, nF, nullptr, pad1, 1, Ti, b.Tp, dasT, b.Tp, s), "shared da pack");
-        if (gr->shared_dw2) TRY(wgrad_gemm(goT, d, shT, F, b.Tp, pad1, 1, gr->shared_dw2, s));
-        if (gr->shared_dw1) TRY(wgrad_gemm(dasT, F, xT, d, b.Tp, pad1, 1, gr->shared_dw1, s));
-        if (gated && gr->shared_dw3) TRY(wgrad_gemm(dasT + b.F * b.Tp, F, xT, d, b.Tp, pad1, 1, gr->shared_dw3, s));
+        // one group: all T tokens
+        CU(launch_fill_range(pad, Ti, s), "token range");
+        const bf16 *SH = static_cast<const bf16 *>(sv->shared_hidden), *X = static_cast<const bf16 *>(x);
+        if (gr->shared_dw2) TRY(wgrad_gemm_rows(go, d, d, SH, F, F, b.T, pad, 1, gr->shared_dw2, s));
+        if (gr->shared_dw1) TRY(wgrad_gemm_rows(das, nF, F, X, d, d, b.T, pad, 1, gr->shared_dw1, s));
+        if (gated && gr->shared_dw3) TRY(wgrad_gemm_rows(das + F, nF, F, X, d, d, b.T, pad, 1, gr->shared_dw3, s));
     }
 #undef CU
-    mark(9);
+    mark(8);
     return MOE_OK;
 }
 

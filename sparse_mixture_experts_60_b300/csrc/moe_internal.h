@@ -172,6 +172,10 @@ struct GemmProblem {
     // N cols]; group g's K rows start at g * b_group_rows; with B2 the K
     // columns from k_split on come from B2 (the [W1 | W3] stack)
     int b_mn; int k_split;
+    // K-grouped with both operands read in place (kg_mn): A [K rows, M
+    // cols] (row stride lda), B [K rows, N cols] (ldb); seg[g] .. seg[g+1]-1
+    // are group g's rows (any offsets), K the total rows
+    int kg_mn; int64_t lda, ldb;
 };
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
 bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias);
@@ -223,5 +227,9 @@ cudaError_t launch_transpose_pack(const bf16 *in, int ld_in, int cols, const int
 cudaError_t launch_pad_offsets(const int32_t *off, int G, int rows, int32_t *pad, cudaStream_t s);
 cudaError_t launch_group_rowsum(const bf16 *in_t, int64_t ld, const int32_t *pad, int G, int C, float *out,
                                 cudaStream_t s);
+// out[g][c] = sum of in[r][c] over the rows off[g] .. off[g+1]-1 (fp32)
+cudaError_t launch_group_colsum(const bf16 *in, int64_t ld, const int32_t *off, int G, int C, float *out,
+                                cudaStream_t s);
+cudaError_t launch_fill_range(int32_t *seg, int n, cudaStream_t s);   // seg = {0, n}
 
 }  // namespace moe
