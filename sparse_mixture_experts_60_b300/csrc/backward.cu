@@ -4,10 +4,9 @@
 //   dx assembly       sum of the expert rows' dx, residual, shared expert,
 //                     and the router term dlogits W_r
 //   router weights    dW_r = dlogits^T x, db_r (two-pass, fixed order)
-//   transposes        weights to the K-major layouts of the data-gradient
-//                     GEMMs; activations packed per expert with every
-//                     expert's rows padded to a multiple of 64 (zeros), the
-//                     K-major operands of the weight-gradient GEMMs
+//   packed transpose  dlogits and x, K-major with the tokens padded to a
+//                     multiple of 64 (zeros): the operands of a wide
+//                     router's dW_r GEMM
 //   bias gradients    per-expert sums of da and dy over their rows
 //
 // No page prints a backward; the objective is the one the "MoE Training:
@@ -338,29 +337,6 @@ __device__ __forceinline__ uint4 tile_col8(bf16 (*tile)[64], int c, int r8) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Batched transpose: out[b][c][out_col0 + r] = in[b][r][c] (in: rows x cols
-// with leading dim ld_in; rows, cols, ld_in, ld_out, out_col0 multiples of 8).
-__global__ void __launch_bounds__(256) transpose_batched_kernel(const bf16 *__restrict__ in, int64_t in_batch,
-                                                                int ld_in, int rows, int cols,
-                                                                bf16 *__restrict__ out, int64_t out_batch,
-                                                                int ld_out, int out_col0) {
-    PDL_ENTER();
-    __shared__ __align__(16) bf16 tile[64][64];
-    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    const bf16 *src = in + blockIdx.z * in_batch;
-    const int nr = rows - r0 < 64 ? rows - r0 : 64, nc = cols - c0 < 64 ? cols - c0 : 64;
-    tile_in(tile, [&](int r) { return src + (int64_t)(r0 + r) * ld_in + c0; }, nr, nc);
-    __syncthreads();
-    bf16 *dst = out + blockIdx.z * out_batch;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int v = threadIdx.x + h * 256;          // output row c = v / 8, 8 input rows from 8 (v % 8)
-        const int c = v >> 3, r8 = (v & 7) * 8;
-        if (c < nc && r8 < nr)
-            *reinterpret_cast<uint4 *>(dst + (int64_t)(c0 + c) * ld_out + out_col0 + r0 + r8) = tile_col8(tile, c, r8);
-    }
-}
-
 // Packed transpose of grouped rows: out[c][pad[g] + i] = in[off[g] + i][c]
 // for i < rows_g, zero for rows_g <= i < pad[g+1] - pad[g].  Every pad[g]
 // is a multiple of 64, so a 64-column output tile belongs to one group.
@@ -442,23 +418,6 @@ __global__ void __launch_bounds__(1024) pad_offsets_kernel(const int32_t *__rest
         if (threadIdx.x == blockDim.x - 1) carry = incl;
         __syncthreads();
     }
-}
-
-// Bias gradient from a packed transpose: out[g][c] = sum over the group's
-// padded columns of in_t[c][.] (padding is zero).  Warp per (c, g).
-__global__ void __launch_bounds__(256) group_rowsum_kernel(const bf16 *__restrict__ in_t, int64_t ld,
-                                                           const int32_t *__restrict__ pad, int G, int C,
-                                                           float *__restrict__ out) {
-    PDL_ENTER();
-    const int lane = threadIdx.x & 31;
-    const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (wid >= (int64_t)C * G) return;
-    const int g = (int)(wid / C), c = (int)(wid % C);
-    const bf16 *row = in_t + (int64_t)c * ld;
-    float s = 0.0f;
-    for (int i = pad[g] + lane; i < pad[g + 1]; i += 32) s += __bfloat162float(row[i]);
-    s = warp_sum(s);
-    if (lane == 0) out[(int64_t)g * C + c] = s;
 }
 
 // Per-group column sums of a row-major bf16 matrix (bias gradients):
@@ -557,14 +516,6 @@ cudaError_t launch_router_wgrad(int64_t T, int d, int E, const float *dl, const 
                       T, d, E, (int)nchunk, part, dl, dw, db);
 }
 
-cudaError_t launch_transpose_batched(const bf16 *in, int64_t in_batch, int ld_in, int rows, int cols, int batch,
-                                     bf16 *out, int64_t out_batch, int ld_out, int out_col0, cudaStream_t s) {
-    if (rows == 0 || cols == 0 || batch == 0) return cudaSuccess;
-    return launch_pdl(transpose_batched_kernel, dim3((unsigned)ceil_div(cols, 64), (unsigned)ceil_div(rows, 64),
-                                                     (unsigned)batch),
-                      dim3(256), 0, s, in, in_batch, ld_in, rows, cols, out, out_batch, ld_out, out_col0);
-}
-
 cudaError_t launch_transpose_pack(const bf16 *in, int ld_in, int cols, const int32_t *off, const int32_t *pad, int G,
                                   int rows, int64_t max_padded, bf16 *out, int64_t ld_out, cudaStream_t s) {
     if (cols == 0 || max_padded == 0) return cudaSuccess;
@@ -574,13 +525,6 @@ cudaError_t launch_transpose_pack(const bf16 *in, int ld_in, int cols, const int
 
 cudaError_t launch_pad_offsets(const int32_t *off, int G, int rows, int32_t *pad, cudaStream_t s) {
     return launch_pdl(pad_offsets_kernel, dim3(1), dim3(1024), 0, s, off, G, rows, pad);
-}
-
-cudaError_t launch_group_rowsum(const bf16 *in_t, int64_t ld, const int32_t *pad, int G, int C, float *out,
-                                cudaStream_t s) {
-    if ((int64_t)C * G == 0) return cudaSuccess;
-    return launch_pdl(group_rowsum_kernel, dim3((unsigned)ceil_div((int64_t)C * G, 8)), dim3(256), 0, s, in_t, ld,
-                      pad, G, C, out);
 }
 
 }  // namespace moe

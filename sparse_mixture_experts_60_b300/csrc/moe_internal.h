@@ -218,15 +218,10 @@ cudaError_t launch_dx_assemble(int64_t T, int d, int k, int E, const float *dx_p
 int64_t router_wgrad_chunks(int64_t T);   // partial buffer: chunks * E * d floats
 cudaError_t launch_router_wgrad(int64_t T, int d, int E, const float *dl, const bf16 *x, float *part, float *dw,
                                 float *db, cudaStream_t s);
-// out[b][c][out_col0 + r] = in[b][r][c]
-cudaError_t launch_transpose_batched(const bf16 *in, int64_t in_batch, int ld_in, int rows, int cols, int batch,
-                                     bf16 *out, int64_t out_batch, int ld_out, int out_col0, cudaStream_t s);
 // out[c * ld_out + pad[g] + i] = in[off[g] + i][c] (zero padding), pad[G] <= max_padded
 cudaError_t launch_transpose_pack(const bf16 *in, int ld_in, int cols, const int32_t *off, const int32_t *pad, int G,
                                   int rows, int64_t max_padded, bf16 *out, int64_t ld_out, cudaStream_t s);
 cudaError_t launch_pad_offsets(const int32_t *off, int G, int rows, int32_t *pad, cudaStream_t s);
-cudaError_t launch_group_rowsum(const bf16 *in_t, int64_t ld, const int32_t *pad, int G, int C, float *out,
-                                cudaStream_t s);
 // out[g][c] = sum of in[r][c] over the rows off[g] .. off[g+1]-1 (fp32)
 cudaError_t launch_group_colsum(const bf16 *in, int64_t ld, const int32_t *off, int G, int C, float *out,
                                 cudaStream_t s);

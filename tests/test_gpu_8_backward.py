@@ -64,6 +64,7 @@ def run_backward(w, inp, aux, z, seed=5, units=None):
     fwd = dict(logits=lg, idx=r["idx"], gate=r["gate"], inv=dsp["inv"], counts=dsp["counts"])
     ref = orc.backward(w, inp, fwd, wl.bf16_to_f32(dout_h).astype(np.float64), aux, z, units=units)
     ref["inv"] = dsp["inv"]
+    ref["idx"] = r["idx"]
     return got, ref
 
 
@@ -93,6 +94,10 @@ CASES = {
                            min_capacity=4), 0.05, 0.01),
     "switch_relu_raw": (dict(T=333, d=128, E=4, k=1, F=256, activation=wl.RELU, score_fn=wl.SOFTMAX,
                              router_bias=True, expert_bias=True, renormalize=False), 0.1, 0.01),
+    # skewed router: empty experts, experts with a few rows and with more than
+    # 64 (partial K blocks everywhere in the weight-gradient GEMMs)
+    "skewed_segments": (dict(T=210, d=128, E=16, k=2, F=128, activation=wl.SWIGLU, score_fn=wl.SOFTMAX,
+                             router_bias=True, expert_bias=False, residual=True), 0.02, 0.01),
 }
 
 
@@ -101,9 +106,16 @@ def test_backward_parity(case):
     kw, aux, z = CASES[case]
     w = wl.Workload(f"bwd_{case}", 90 + len(case), dtype=wl.BF16, **kw)
     inp = wl.make_inputs(w)
+    if case == "skewed_segments":
+        # two popular experts, a middle group, rare ones and four never chosen
+        inp["b_router"] = np.array([0.5, 0.4, 0, 0, 0, 0, -0.15, -0.25, -0.35, -0.45, -0.55, -0.65, -40, -40, -40, -40],
+                                   np.float32)
     got, ref = run_backward(w, inp, aux, z)
     if w.drop_tokens:
         assert (ref["inv"] < 0).any()               # slots were dropped
+    if case == "skewed_segments":
+        counts = np.bincount(ref["idx"].reshape(-1), minlength=w.E)
+        assert (counts == 0).any() and ((counts > 0) & (counts < 8)).any() and (counts > 64).any(), counts
     check_grads(w, got, ref, case)
 
 
