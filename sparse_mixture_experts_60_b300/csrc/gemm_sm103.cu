@@ -1321,16 +1321,18 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
 }
 
 // CTA pairs pay off when groups are tall (a pair tile covers 256 rows, so
-// short expert segments would waste most of it); measured on B300 they win
-// for the second expert GEMM (fp32 output) and lose for the gated first one,
-// so only the former uses them by default.  MOE_B300_GEMM_PAIR=0 or 1 forces
-// the choice (the tests run both kernels on the same shapes).
+// short expert segments would waste most of it).  Measured on B300: they
+// lose for the gated first expert GEMM; for the second (fp32 output) they
+// win with K = 4096 (Quick Start shape: 0.112 vs 0.125 ms) and lose with
+// K = 14336 (Mixtral shape: 3.12 vs 3.07 ms), so they run only the second
+// GEMM of tall groups with K <= 8192 by default.  MOE_B300_GEMM_PAIR=0 or 1
+// forces the choice (the tests run both kernels on the same shapes).
 bool use_pair(const GemmProblem &p) {
     const char *e = getenv("MOE_B300_GEMM_PAIR");
     if (e && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
     const int groups = p.seg ? p.G : 1;
     const int64_t rows_per_group = p.a_rows / (groups > 0 ? groups : 1);
-    return rows_per_group >= 1024 && p.out_f32 && !p.gated;
+    return rows_per_group >= 1024 && p.out_f32 && !p.gated && p.K <= 8192;
 }
 
 }  // namespace
