@@ -27,12 +27,13 @@ def golden():
 
 
 def pytest_sessionfinish(session, exitstatus):
-    """Write the float-parity margins of the GPU tests (if any ran)."""
+    """Write the float-parity margins of the GPU tests (if any ran) to the
+    directory named by PARITY_REPORT_DIR (no report without it)."""
     mod = sys.modules.get("tests.gpu_util")
     rep = getattr(mod, "REPORT", None) if mod else None
-    if not rep:
+    out = os.environ.get("PARITY_REPORT_DIR")
+    if not rep or not out:
         return
-    out = os.path.join(ROOT, "gpurun_out")
     os.makedirs(out, exist_ok=True)
     name = os.environ.get("PARITY_REPORT", "parity_report.txt")
     with open(os.path.join(out, name), "a") as f:
