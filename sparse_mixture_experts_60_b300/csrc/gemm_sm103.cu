@@ -306,51 +306,58 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const in
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 
-// One 32-column chunk of a warp's 32 rows (thread = row) to global memory:
-// staged through the warp's 32-row x 64-byte shared buffer (16-byte units
-// XOR-swizzled by row, conflict-free both ways) and stored as row-contiguous
-// 64-byte segments: whole 32-byte sectors, 8 rows per warp store.  Rows
-// from row_end and columns from ncols (in 16-byte units) are not written.
+// One 32-column chunk of a warp's 32 rows (thread = row) to global memory,
+// staged through the warp's 2 KB shared buffer (16-byte units XOR-swizzled
+// by row, conflict-free both ways).  bf16: 32 rows x 64 B in one pass, 8
+// rows per warp store.  fp32: the chunk is 128 B per row, so it goes in two
+// passes of 16 rows (lanes 0-15, then 16-31) and every warp store writes 4
+// whole 128-byte lines.  Rows from row_end and columns from ncols (in
+// 16-byte units) are not written.
 template <bool OUT_F32>
 __device__ __forceinline__ void store_chunk(const float (&v)[32], void *out, int64_t ldo, int col, int ncols,
                                             int row_base, int row_end, uint8_t *stg, int lane) {
-    // one or two passes of 64 B per row: 32 bf16, or 16 fp32 at a time
-    constexpr int PASSES = OUT_F32 ? 2 : 1;
-    constexpr int COLS = 32 / PASSES;                    // output columns per pass
-    uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
+    if constexpr (OUT_F32) {
+        uint4 *sbuf = reinterpret_cast<uint4 *>(stg);      // [16 rows][8 units]
 #pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) {
+        for (int ps = 0; ps < 2; ++ps) {
+            if ((lane >> 4) == ps) {
+                const int r = lane & 15;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    sbuf[r * 8 + (j ^ (r & 7))] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                                             __float_as_uint(v[4 * j + 2]),
+                                                             __float_as_uint(v[4 * j + 3]));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int idx = it * 32 + lane, r = idx >> 3, cc = idx & 7;
+                const uint4 val = sbuf[r * 8 + (cc ^ (r & 7))];
+                const int grow = row_base + 16 * ps + r;
+                if (grow < row_end && col + 4 * cc < ncols)
+                    reinterpret_cast<uint4 *>(static_cast<float *>(out) + (int64_t)grow * ldo + col)[cc] = val;
+            }
+            __syncwarp();
+        }
+    } else {
+        uint4 *srow = reinterpret_cast<uint4 *>(stg + lane * 64);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            uint4 unit;
-            if (OUT_F32) {
-                const float *f = v + ps * 16 + 4 * j;
-                unit = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                                  __float_as_uint(f[3]));
-            } else {
-                uint32_t w[4];
+            uint32_t w[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
-                    w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-                }
-                unit = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
+                w[h] = *reinterpret_cast<const uint32_t *>(&b2);
             }
-            srow[j ^ ((lane >> 1) & 3)] = unit;
+            srow[j ^ ((lane >> 1) & 3)] = make_uint4(w[0], w[1], w[2], w[3]);
         }
         __syncwarp();
-        const int pcol = col + ps * COLS;
-        constexpr int UNIT_COLS = OUT_F32 ? 4 : 8;
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
             const int cidx = it * 32 + lane, r = cidx >> 2, cc = cidx & 3;
             const uint4 val = reinterpret_cast<const uint4 *>(stg + r * 64)[cc ^ ((r >> 1) & 3)];
-            if (row_base + r < row_end && pcol + UNIT_COLS * cc < ncols) {
-                if (OUT_F32)
-                    reinterpret_cast<uint4 *>(static_cast<float *>(out) + (int64_t)(row_base + r) * ldo + pcol)[cc] = val;
-                else
-                    reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + (int64_t)(row_base + r) * ldo + pcol)[cc] = val;
-            }
+            if (row_base + r < row_end && col + 8 * cc < ncols)
+                reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + (int64_t)(row_base + r) * ldo + col)[cc] = val;
         }
         __syncwarp();
     }
@@ -589,7 +596,9 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *consumed = abort_flag + 1;
-    uint64_t *fixed = bars + 16;           // [STAGES] KG_MN: stage ready for the MMA
+    // KG_MN: [STAGES] stage ready for the MMA, after drain and the flags
+    uint64_t *fixed = bars + 2 * STAGES + 8;
+    static_assert(!KG_MN || (3 * STAGES + 8) * 8 <= C::BAR_BYTES, "barrier area too small");
     int *seg_s = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES + C::BAR_BYTES);
     int *pre_s = seg_s + (args.G + 1);
 
@@ -820,9 +829,8 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
         // ------------------------------------------------ epilogue
         // Thread = accumulator row.  Warps w and w+4 share a TMEM lane
         // quadrant and take alternate 32-column chunks.  Output leaves through
-        // a per-warp shared-memory buffer of 32 rows x 64 B (16-byte units
-        // XOR-swizzled by row, conflict-free both ways) as row-contiguous
-        // 64-byte segments: whole 32-byte sectors, 8 rows per warp store.
+        // a per-warp 2 KB shared-memory buffer (store_chunk): row-contiguous
+        // 64-byte segments of bf16, whole 128-byte lines of fp32.
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int half = (warp - 2) >> 2;       // which alternate chunks
         uint8_t *stg = sEpi + (warp - 2) * (32 * 64);
