@@ -37,6 +37,8 @@
 // released before the CTA exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -274,6 +276,7 @@ struct Args {
     int kgroup;            // 1: groups split K (weight gradients), seg = per-group K offsets
     int64_t out_group_stride;  // K-grouped: elements between the groups' outputs
     int k_split;           // MN-major B: K below k_split from tmB, the rest from tmB2
+    int n_inner;           // K-grouped: consecutive tiles walk N (else M) inside a group
 };
 
 struct Tile {
@@ -398,7 +401,15 @@ __device__ __forceinline__ Tile tile_of(const Args &args, int tile, const int *s
     Tile t;
     t.g = tile / kg_tiles;
     const int local = tile - t.g * kg_tiles;
-    const int nb = local / mt, mb = local - nb * mt;
+    int mb, nb;
+    if (args.n_inner) {
+        const int nt = kg_tiles / mt;
+        mb = local / nt;
+        nb = local - mb * nt;
+    } else {
+        nb = local / mt;
+        mb = local - nb * mt;
+    }
     t.row0 = mb * BM;
     t.seg_end = args.M;
     t.n0 = nb * bn_out;
@@ -1267,6 +1278,17 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     a.kgroup = p.kgroup;
     a.out_group_stride = p.out_group_stride;
     a.k_split = p.B2 ? p.k_split : p.K;
+    // K-grouped: of the two tile orders inside a group, the one whose wave of
+    // concurrent tiles (one per SM) touches fewer operand rows (A tiles x BM
+    // + B tiles x BN), so that a wave's operands stay in L2
+    a.n_inner = 0;
+    if (p.kgroup) {
+        const int64_t W = num_sms();
+        const int64_t mt = ((int64_t)p.M + BM - 1) / BM, nt = ((int64_t)p.N + BN_B - 1) / BN_B;
+        const int64_t fm = std::min(mt, W) * BM + std::min(nt, (W + mt - 1) / mt) * BN;
+        const int64_t fn = std::min(nt, W) * BN + std::min(mt, (W + nt - 1) / nt) * BM;
+        a.n_inner = fn < fm ? 1 : 0;
+    }
     // MN-major B: the whole 227 KB are reserved, so that every shared-memory
     // address the tensor cores derive from the descriptors lies inside the
     // CTA's allocation
