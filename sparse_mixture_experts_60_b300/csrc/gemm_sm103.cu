@@ -306,7 +306,28 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const in
     return decode_tile_m(tile, seg_s, pre_s, G, bn_out, BM);
 }
 
-__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+// Gaussian CDF for the GELU epilogues, from the rational approximation of
+// erfc in Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.26
+// (after Hastings): for x >= 0, erfc(x) = t (a1 + t (a2 + t (a3 + t (a4 +
+// t a5)))) exp(-x^2) + eps, t = 1 / (1 + p x), |eps| <= 1.5e-7.  With
+// x = |a| / sqrt(2), Phi(a) = erfc(x) / 2 for a < 0 (no cancellation) and
+// 1 - erfc(x) / 2 otherwise; exp(-x^2) = exp(-a^2 / 2) is returned in `e`
+// for the density term of GELU'.  One exponential and one reciprocal per
+// element, where erff and expf cost the backward epilogue twice as much.
+__device__ __forceinline__ float gauss_cdf(float a, float &e) {
+    constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
+                    a4 = -1.453152027f, a5 = 1.061405429f;
+    const float x = fabsf(a) * 0.70710678118654752f;
+    const float t = __fdividef(1.0f, fmaf(p, x, 1.0f));
+    e = __expf(-x * x);
+    const float half_erfc = 0.5f * t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1) * e;
+    return a >= 0.0f ? 1.0f - half_erfc : half_erfc;
+}
+// GELU(a) = a Phi(a)
+__device__ __forceinline__ float gelu_erf(float v) {
+    float e;
+    return v * gauss_cdf(v, e);
+}
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 
 // One 32-column chunk of a warp's 32 rows (thread = row) to global memory,
@@ -387,8 +408,11 @@ __device__ __forceinline__ void load_row32_bf16(const bf16 *base, int64_t ld, in
     }
 }
 
+// GELU'(a) = Phi(a) + a phi(a), phi(a) = exp(-a^2 / 2) / sqrt(2 pi)
 __device__ __forceinline__ float gelu_erf_grad(float a) {
-    return 0.5f * (1.0f + erff(a * 0.70710678118654752f)) + a * 0.39894228040143268f * expf(-0.5f * a * a);
+    float e;
+    const float c = gauss_cdf(a, e);
+    return fmaf(a * 0.39894228040143268f, e, c);
 }
 
 // Tile of either kind of problem: M-grouped (rows of A split into groups,
