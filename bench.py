@@ -150,13 +150,17 @@ def launches_per_step(w, routing="topk"):
     return n
 
 
-def traffic_for_gemm():
+def traffic_for_gemm(w, routing):
     """dram bytes per launch of the first expert GEMM from the committed ncu
-    summary, valid only while the kernel source is unchanged."""
+    summary: only for the workload it was captured on, and only while the
+    kernel source is unchanged."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         t = json.load(f)
+    key = t.get("key", {})
+    if key.get("workload") != w.name or key.get("tokens") != w.T or key.get("routing") != routing:
+        return None
     sha = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
     if t.get("source_sha256") != sha:
         return None
@@ -557,22 +561,37 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
     pk, pk_kind = peaks()
     f1, f2 = gemm_flops(w, kept)
     ffn1_ms, ffn2_ms = float(stage_ms[2]), float(stage_ms[3])
-    achieved = f1 / (ffn1_ms * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     rb, pb, cb = hbm_bytes(w, kept, args.routing)
     hbm_ms = float(stage_ms[0] + stage_ms[1] + stage_ms[5])
     hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gemm_ms = ffn1_ms + ffn2_ms + float(stage_ms[4])
+    # the first routed expert GEMM (the shared expert is its own stage): its
+    # FLOPs, and its algorithmic bytes (W1 (+W3) of every expert, x_perm
+    # read, H written); bound by whichever takes longer at the peaks
+    n1 = (2 if w.gated else 1) * w.F
+    f1r = 2.0 * kept * w.d * n1
+    b1r = float(w.E * n1 * w.d * w.elem_bytes + kept * w.d * w.elem_bytes + kept * w.F * w.elem_bytes)
+    kname = ("grouped_gemm_kernel (expert W1/W3 + SwiGLU)" if w.gated
+             else "grouped_gemm_kernel (expert W1 + activation)")
+    if b1r / (hbm_peak * 1e9) > f1r / (peak * 1e12):
+        gbs = b1r / (ffn1_ms * 1e-3) / 1e9
+        roofline = {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": gbs / hbm_peak, "peak_kind": f"hbm_gbs of {pk_kind}",
+                    "traffic": traffic_for_gemm(w, args.routing), "bytes_per_launch": b1r,
+                    "ms_per_launch": ffn1_ms}
+    else:
+        achieved = f1r / (ffn1_ms * 1e-3) / 1e12
+        roofline = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "peak_kind": f"bf16_tflops_sustained of {pk_kind}",
+                    "traffic": traffic_for_gemm(w, args.routing), "flops_per_launch": f1r,
+                    "ms_per_launch": ffn1_ms}
     line = {
         "metric": METRIC, "value": whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
         "data": "synthetic", "config": config_of(w, args.routing),
-        "roofline": {"kernel": "grouped_gemm_kernel (expert W1/W3 + SwiGLU)" if w.gated
-                     else "grouped_gemm_kernel (expert W1 + activation)",
-                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_kind": f"bf16_tflops_sustained of {pk_kind}",
-                     "traffic": traffic_for_gemm(), "flops_per_launch": f1, "ms_per_launch": ffn1_ms},
+        "roofline": roofline,
         "expert_gemm": {"tflops": (f1 + f2) / (gemm_ms * 1e-3) / 1e12,
                         "frac_of_bf16_sustained": (f1 + f2) / (gemm_ms * 1e-3) / 1e12 / peak,
                         "ms": gemm_ms, "kept_rows": kept},
