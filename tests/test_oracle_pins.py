@@ -467,6 +467,60 @@ def test_fmix32_closed_forms():
     assert 14 < float(np.mean(flips)) < 18
 
 
+def test_fmix32_murmur3_test_vectors():
+    """MurmurHash3_x86_32 of the empty input with seed s is fmix32(s) (no
+    blocks, no tail, length 0), so the finalizer's published test vectors
+    for the empty input pin it: seed 0 -> 0, seed 1 -> 0x514E28B7, seed
+    0xFFFFFFFF -> 0x81F16F39 (MurmurHash3, A. Appleby, SMHasher
+    verification values)."""
+    assert orc.fmix32(0) == 0
+    assert orc.fmix32(1) == 0x514E28B7
+    assert orc.fmix32(0xFFFFFFFF) == 0x81F16F39
+
+
+def _golden_stride():
+    # floor(2^32 / phi) = floor(2^31 (sqrt(5) - 1)), in integers
+    return ((1 << 31) * (math.isqrt(5 << 128) - (1 << 64))) >> 64
+
+
+def test_hash_choices_use_the_golden_ratio_stride():
+    """Choice j hashes token_id + j * floor(2^32 / phi) (mod 2^32); where the
+    keys of a token do not collide, every choice is that hash mod E."""
+    stride = _golden_stride()
+    assert stride == 0x9E3779B9
+    E, k = 64, 3
+    tok = np.arange(5000, dtype=np.int32) * 7 + 3
+    r = orc.route_hash(len(tok), E, k, tok)
+    checked = 0
+    for t, tid in enumerate(tok):
+        raw = [orc.fmix32((int(tid) + j * stride) & 0xFFFFFFFF) % E for j in range(k)]
+        if len(set(raw)) == k:
+            assert list(r["idx"][t]) == raw
+            checked += 1
+    assert checked > 4000
+
+
+def test_hash_collision_moves_up_cyclically():
+    """A choice that an earlier choice of the same token took moves to the
+    next expert up, wrapping at E."""
+    stride = _golden_stride()
+    E = 5
+    tok = np.arange(4000, dtype=np.int32)
+    r = orc.route_hash(len(tok), E, 2, tok)
+    hits = wraps = 0
+    for t, tid in enumerate(tok):
+        a = orc.fmix32(int(tid)) % E
+        b = orc.fmix32((int(tid) + stride) & 0xFFFFFFFF) % E
+        assert r["idx"][t, 0] == a
+        if a == b:
+            assert r["idx"][t, 1] == (a + 1) % E
+            hits += 1
+            wraps += a == E - 1
+        else:
+            assert r["idx"][t, 1] == b
+    assert hits > 400 and wraps > 50
+
+
 def test_hash_collision_moves_to_next_free_expert():
     """With E = 2, k = 2 the second choice must be the expert the first did
     not take, whatever the hash of the second key is."""
@@ -498,6 +552,31 @@ def test_expert_choice_selection_against_sort():
     mask = ec["tok_row"] >= 0
     np.testing.assert_allclose(ec["tok_gate"][mask], probs[mask], rtol=1e-12)
     assert np.all(ec["tok_gate"][~mask] == 0)
+
+
+def test_expert_choice_ties_at_the_capacity_boundary():
+    """Logits in {0, 1}: about half the tokens tie at the C-th largest
+    value; the expert takes the ties with the lowest token indices (a
+    stable sort of the negated logits, first C, back in token order)."""
+    w = _cfg(T=301, E=6, k=1, capacity_factor=1.7, min_capacity=0)
+    g = np.random.default_rng(5)
+    lg = g.integers(0, 2, (w.T, w.E)).astype(np.float32)
+    ec = orc.route_expert_choice(w, lg)
+    C = ec["C"]
+    for e in range(w.E):
+        order = np.argsort(-lg[:, e], kind="stable")
+        assert lg[order[C - 1], e] == lg[order[C], e]          # the boundary really is a tie
+        np.testing.assert_array_equal(ec["row_token"][e * C:(e + 1) * C], np.sort(order[:C]))
+
+
+def test_expert_choice_capacity_closed_forms():
+    """C = min(T, max(min_capacity, ceil(T / E * capacity_factor))), on
+    values where T / E * capacity_factor is not within rounding of an
+    integer."""
+    for T, E, cf, mc, want in [(301, 6, 1.7, 0, 86), (10, 3, 1.0, 0, 4), (10, 4, 1.5, 0, 4), (10, 4, 1.5, 5, 5),
+                               (3, 1, 2.0, 0, 3), (7, 7, 1.0, 0, 1), (1000, 8, 0.01, 2, 2)]:
+        w = _cfg(T=T, E=E, k=1, capacity_factor=cf, min_capacity=mc)
+        assert orc.ec_capacity(w) == want, (T, E, cf, mc)
 
 
 def test_expert_choice_full_capacity_is_the_dense_soft_mixture():
