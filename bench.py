@@ -419,6 +419,63 @@ def bwd_launches(w):
     return n
 
 
+def train_line(args, w, world, ms, fst, bst, kept, clocks):
+    """The training step's JSON line from its timings: ms per step, the
+    forward's 7 and the backward's 8 mean stage times (ms), the kept rows."""
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    nF = 2 * w.F if w.activation == wl.SWIGLU else w.F
+    R = kept
+    f1, f2 = gemm_flops(w, kept)                  # forward expert GEMMs
+    flops = {"dh_gemm": 2.0 * R * w.d * w.F, "dx_gemm": 2.0 * R * nF * w.d, "dw2_gemm": 2.0 * R * w.d * w.F,
+             "dw13_gemm": 2.0 * R * nF * w.d}
+    bms = dict(zip(BWD_STAGES, bst.tolist()))
+    gemm_tf = {k: flops[k] / (bms[k] * 1e-3) / 1e12 for k in flops}
+    top = max(flops, key=lambda k: bms[k])
+    # algorithmic HBM bytes of the weight-gradient GEMMs: the fp32 gradient
+    # written once, each bf16 operand read once per launch (dW1 and dW3 are
+    # two launches over x_perm); at large E and few rows per expert these
+    # GEMMs are bound by the gradient writes, not by the tensor cores
+    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    n13 = 2 if w.activation == wl.SWIGLU else 1
+    wbytes = {"dw2_gemm": 4.0 * w.E * w.d * w.F + 2.0 * R * (w.d + w.F),
+              "dw13_gemm": 4.0 * w.E * nF * w.d + 2.0 * R * (nF + n13 * w.d)}
+    gemm_roof = {}
+    for k in flops:
+        t_tc = flops[k] / (peak * 1e12)
+        t_hbm = wbytes.get(k, 0.0) / (hbm_peak * 1e9)
+        ms_k = bms[k] * 1e-3
+        gemm_roof[k] = ({"bound": "hbm", "frac": t_hbm / ms_k, "gbs": wbytes[k] / ms_k / 1e9} if t_hbm > t_tc
+                        else {"bound": "tensor", "frac": t_tc / ms_k, "tflops": gemm_tf[k]})
+    if gemm_roof[top]["bound"] == "hbm":
+        roofline = {"kernel": f"grouped_gemm ({top}, backward)", "bound": "hbm", "achieved": gemm_roof[top]["gbs"],
+                    "peak": hbm_peak, "unit": "GB/s", "frac": gemm_roof[top]["frac"],
+                    "peak_kind": f"hbm_gbs of {pk_kind}", "traffic": None, "bytes_per_step": wbytes[top],
+                    "ms_per_step": bms[top]}
+    else:
+        roofline = {"kernel": f"grouped_gemm ({top}, backward)", "bound": "tensor", "achieved": gemm_tf[top],
+                    "peak": peak, "unit": "TFLOP/s", "frac": gemm_tf[top] / peak,
+                    "peak_kind": f"bf16_tflops_sustained of {pk_kind}", "traffic": None,
+                    "flops_per_step": flops[top], "ms_per_step": bms[top]}
+    train_flops = f1 + f2 + sum(flops.values())
+    gemm_ms = float(fst[2] + fst[3]) + sum(bms[k] for k in flops)
+    line = {
+        "metric": "MoE-layer training step (forward + backward) tokens/s on 1 B300", "value":
+        whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": dict(config_of(w), mode="train", aux_coef=0.01, z_coef=0.001),
+        "roofline": roofline,
+        "expert_gemm": {"tflops": train_flops / (gemm_ms * 1e-3) / 1e12,
+                        "frac_of_bf16_sustained": train_flops / (gemm_ms * 1e-3) / 1e12 / peak, "ms": gemm_ms,
+                        "backward_gemm_tflops": gemm_tf, "backward_gemm_roofline": gemm_roof},
+        "stage_ms": {"forward": dict(zip(["route", "permute", "ffn1", "ffn2", "shared", "combine", "stats"],
+                                         fst.tolist())), "backward": bms},
+        "clocks": clocks, "e2e": None,
+        "gpu_launches": (launches_per_step(w) + bwd_launches(w)) * args.steps,
+    }
+    return line
+
+
 def run_train(args, w, rank, world, local):
     """One step = the training forward (activations kept) + moe_backward
     with aux_coef 0.01, z_coef 0.001."""
@@ -496,57 +553,7 @@ def run_train(args, w, rank, world, local):
     if rank != 0:
         dist.destroy_process_group()
         return 0
-    pk, pk_kind = peaks()
-    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    nF = 2 * w.F if w.activation == wl.SWIGLU else w.F
-    R = kept
-    f1, f2 = gemm_flops(w, kept)                  # forward expert GEMMs
-    flops = {"dh_gemm": 2.0 * R * w.d * w.F, "dx_gemm": 2.0 * R * nF * w.d, "dw2_gemm": 2.0 * R * w.d * w.F,
-             "dw13_gemm": 2.0 * R * nF * w.d}
-    bms = dict(zip(BWD_STAGES, bst.tolist()))
-    gemm_tf = {k: flops[k] / (bms[k] * 1e-3) / 1e12 for k in flops}
-    top = max(flops, key=lambda k: bms[k])
-    # algorithmic HBM bytes of the weight-gradient GEMMs: the fp32 gradient
-    # written once, each bf16 operand read once per launch (dW1 and dW3 are
-    # two launches over x_perm); at large E and few rows per expert these
-    # GEMMs are bound by the gradient writes, not by the tensor cores
-    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    n13 = 2 if w.activation == wl.SWIGLU else 1
-    wbytes = {"dw2_gemm": 4.0 * w.E * w.d * w.F + 2.0 * R * (w.d + w.F),
-              "dw13_gemm": 4.0 * w.E * nF * w.d + 2.0 * R * (nF + n13 * w.d)}
-    gemm_roof = {}
-    for k in flops:
-        t_tc = flops[k] / (peak * 1e12)
-        t_hbm = wbytes.get(k, 0.0) / (hbm_peak * 1e9)
-        ms_k = bms[k] * 1e-3
-        gemm_roof[k] = ({"bound": "hbm", "frac": t_hbm / ms_k, "gbs": wbytes[k] / ms_k / 1e9} if t_hbm > t_tc
-                        else {"bound": "tensor", "frac": t_tc / ms_k, "tflops": gemm_tf[k]})
-    if gemm_roof[top]["bound"] == "hbm":
-        roofline = {"kernel": f"grouped_gemm ({top}, backward)", "bound": "hbm", "achieved": gemm_roof[top]["gbs"],
-                    "peak": hbm_peak, "unit": "GB/s", "frac": gemm_roof[top]["frac"],
-                    "peak_kind": f"hbm_gbs of {pk_kind}", "traffic": None, "bytes_per_step": wbytes[top],
-                    "ms_per_step": bms[top]}
-    else:
-        roofline = {"kernel": f"grouped_gemm ({top}, backward)", "bound": "tensor", "achieved": gemm_tf[top],
-                    "peak": peak, "unit": "TFLOP/s", "frac": gemm_tf[top] / peak,
-                    "peak_kind": f"bf16_tflops_sustained of {pk_kind}", "traffic": None,
-                    "flops_per_step": flops[top], "ms_per_step": bms[top]}
-    train_flops = f1 + f2 + sum(flops.values())
-    gemm_ms = float(fst[2] + fst[3]) + sum(bms[k] for k in flops)
-    line = {
-        "metric": "MoE-layer training step (forward + backward) tokens/s on 1 B300", "value":
-        whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": dict(config_of(w), mode="train", aux_coef=0.01, z_coef=0.001),
-        "roofline": roofline,
-        "expert_gemm": {"tflops": train_flops / (gemm_ms * 1e-3) / 1e12,
-                        "frac_of_bf16_sustained": train_flops / (gemm_ms * 1e-3) / 1e12 / peak, "ms": gemm_ms,
-                        "backward_gemm_tflops": gemm_tf, "backward_gemm_roofline": gemm_roof},
-        "stage_ms": {"forward": dict(zip(["route", "permute", "ffn1", "ffn2", "shared", "combine", "stats"],
-                                         fst.tolist())), "backward": bms},
-        "clocks": clocks, "e2e": None,
-        "gpu_launches": (launches_per_step(w) + bwd_launches(w)) * args.steps,
-    }
+    line = train_line(args, w, world, ms, fst, bst, kept, clocks)
     print(json.dumps(line, default=float), flush=True)
     if dist is not None:
         dist.destroy_process_group()
