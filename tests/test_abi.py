@@ -167,3 +167,48 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_c_program_links_and_calls_the_host_entry_points(L, tmp_path):
+    """A plain C program compiled against the header and linked with the
+    library (no Python, no GPU) sizes workspaces, gets the expert-choice
+    capacity, and reads back the host-side error of a bad call."""
+    src = tmp_path / "user.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "moe_b300.h"
+int main(void) {
+    moe_config_t c;
+    memset(&c, 0, sizeof c);
+    c.num_tokens = 16384; c.d_model = 4096; c.num_experts = 8; c.top_k = 2; c.d_ff = 14336;
+    c.score_fn = MOE_SCORE_SOFTMAX; c.activation = MOE_ACT_SWIGLU; c.dtype = MOE_DTYPE_BF16;
+    c.renormalize = 1; c.residual = 1; c.capacity_factor = 2.0f;
+    size_t fwd = 0, bwd = 0;
+    if (moe_workspace_size(&c, MOE_WS_FORWARD, &fwd) != MOE_OK) return 1;
+    if (moe_workspace_size(&c, MOE_WS_BACKWARD, &bwd) != MOE_OK) return 2;
+    int64_t cap = 0;
+    if (moe_ec_capacity(&c, &cap) != MOE_OK) return 3;
+    c.top_k = 0;
+    size_t n = 0;
+    moe_status_t st = moe_workspace_size(&c, MOE_WS_FORWARD, &n);
+    char msg[256];
+    moe_last_error(msg, sizeof msg);
+    printf("%d %zu %zu %lld %d %s\n", moe_version(), fwd, bwd, (long long)cap, (int)st, msg);
+    return 0;
+}
+''')
+    exe = tmp_path / "user"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lmoe_b300", "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    ver, fwd, bwd, cap, st, *msg = r.stdout.split()
+    w = wl.WORKLOADS["mixtral"]
+    assert int(ver) == L.moe_version()
+    assert int(fwd) == _ws_expect(w)["fwd"]
+    assert int(fwd) == moe.moe_workspace_size(moe.config_for(w), moe.MOE_WS_FORWARD)
+    assert int(bwd) > 0
+    assert int(cap) == 4096                        # ceil(16384 / 8 * 2.0)
+    assert int(st) == 1 and msg                    # MOE_ERR_INVALID_ARG with a message
