@@ -52,6 +52,13 @@ from sparse_mixture_experts_60_b300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; expert GEMM TFLOP/s and % of bf16 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# nominal B300 figures (dense bf16 tensor rate, HBM3e bandwidth), reported
+# next to the fractions of the measured peaks
+SPEC_PEAKS = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
+# a timed region shorter than this runs at the burst clocks: the tensor-core
+# kernels inside it are compared with the burst bf16 figure, longer regions
+# with the sustained one (measured under the power cap)
+BURST_REGION_S = 1.0
 GEMM_SRC = os.path.join(ROOT, "sparse_mixture_experts_60_b300", "csrc", "gemm_sm103.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 ACT_NAME = {wl.GELU: "gelu", wl.RELU: "relu", wl.SWIGLU: "swiglu"}
@@ -95,7 +102,9 @@ def gemm_flops(w, kept_rows):
 
 
 def hbm_bytes(w, kept_rows, routing="topk"):
-    """Algorithmic bytes of the HBM-bound stages (route, dispatch, combine)."""
+    """Algorithmic bytes of the HBM-bound stages (route, dispatch, combine):
+    every tensor the stage must read or write, once, at its storage type
+    (expert outputs y and the shared expert's z in the layer dtype)."""
     eb = w.elem_bytes
     T, d, E, S = w.T, w.d, w.E, w.T * w.k
     if routing == "expert_choice":
@@ -104,13 +113,82 @@ def hbm_bytes(w, kept_rows, routing="topk"):
         # row_token out), gates (logits, tok_row in; tok_gate out)
         route = T * d * eb + E * d * eb + T * E * 4 + T * E * 4 + T * E * 4 + R * 4 + 3 * T * E * 4
         permute = 2 * R * d * eb + R * 4                       # row gather: read and write each chosen row
-        combine = R * d * 4 + T * d * eb + (T * d * eb if w.residual else 0) + \
-            (T * d * 4 if w.num_shared else 0) + T * E * 8
+        combine = R * d * eb + T * d * eb + (T * d * eb if w.residual else 0) + \
+            (T * d * eb if w.num_shared else 0) + T * E * 8
         return route, permute, combine
     route = T * d * eb + E * d * eb + T * E * 4 + S * 8 + T * 4
     permute = T * d * eb + kept_rows * d * eb + S * 4 * 3 + T * w.k * 4
-    combine = kept_rows * d * 4 + T * d * eb + (T * d * eb if w.residual else 0) + (T * d * 4 if w.num_shared else 0) + S * 8
+    combine = kept_rows * d * eb + T * d * eb + (T * d * eb if w.residual else 0) + \
+        (T * d * eb if w.num_shared else 0) + S * 8
     return route, permute, combine
+
+
+def tensor_peak(pk, region_s):
+    """The bf16 tensor peak a kernel inside a timed region of region_s
+    seconds is compared with: burst below BURST_REGION_S, else sustained."""
+    if region_s < BURST_REGION_S:
+        return float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), "bf16_tflops (burst)"
+    return float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])), \
+        "bf16_tflops_sustained"
+
+
+def forward_roofline(w, kept_rows, active_experts, stage_ms, clocks, region_s, routing="topk"):
+    """Roofline of the first routed expert GEMM, the expert GEMMs together,
+    and the HBM-bound stages, from the mean stage times (ms: route, permute,
+    ffn1, ffn2, shared, combine, stats).
+
+    The first GEMM's algorithmic FLOPs are 2 kept_rows d nF; its algorithmic
+    bytes are W1 (+ W3) of the experts that hold at least one kept row (an
+    expert with no rows loads no weight tile), x_perm read once and H
+    written once.  It is classed by whichever of the two takes longer at
+    the measured peaks."""
+    pk, pk_kind = peaks()
+    peak, peak_name = tensor_peak(pk, region_s)
+    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    f1, f2 = gemm_flops(w, kept_rows)
+    ffn1_ms, ffn2_ms = float(stage_ms[2]), float(stage_ms[3])
+    n1 = (2 if w.gated else 1) * w.F
+    f1r = 2.0 * kept_rows * w.d * n1
+    b1r = float(active_experts * n1 * w.d * w.elem_bytes + kept_rows * w.d * w.elem_bytes +
+                kept_rows * w.F * w.elem_bytes)
+    kname = ("grouped_gemm_kernel (expert W1/W3 + SwiGLU)" if w.gated
+             else "grouped_gemm_kernel (expert W1 + activation)")
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    clock_ratio = (smax / sm) if sm and smax else None
+    if b1r / (hbm_peak * 1e9) > f1r / (peak * 1e12):
+        gbs = b1r / (ffn1_ms * 1e-3) / 1e9
+        roof = {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "peak_kind": f"hbm_gbs of {pk_kind}",
+                "frac_of_spec": gbs / SPEC_PEAKS["hbm_gbs"], "spec_peak": SPEC_PEAKS["hbm_gbs"],
+                "traffic": traffic_for_gemm(w, routing), "bytes_per_launch": b1r, "ms_per_launch": ffn1_ms,
+                "active_experts": int(active_experts)}
+    else:
+        achieved = f1r / (ffn1_ms * 1e-3) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": f"{peak_name} of {pk_kind}",
+                "frac_of_sustained": achieved / float(pk.get("bf16_tflops_sustained",
+                                                            FALLBACK_PEAKS["bf16_tflops_sustained"])),
+                "frac_of_spec": achieved / SPEC_PEAKS["bf16_tflops"], "spec_peak": SPEC_PEAKS["bf16_tflops"],
+                "frac_at_sm_max_clock": (achieved / peak / clock_ratio) if clock_ratio else None,
+                "traffic": traffic_for_gemm(w, routing), "flops_per_launch": f1r, "ms_per_launch": ffn1_ms}
+    gemm_ms = ffn1_ms + ffn2_ms + float(stage_ms[4])
+    gemm_tf = (f1 + f2) / (gemm_ms * 1e-3) / 1e12
+    expert_gemm = {"tflops": gemm_tf, "frac_of_peak": gemm_tf / peak, "peak_kind": peak_name,
+                   "ffn1_tflops": f1r / (ffn1_ms * 1e-3) / 1e12,
+                   "ffn2_tflops": 2.0 * kept_rows * w.F * w.d / (ffn2_ms * 1e-3) / 1e12,
+                   "ms": gemm_ms, "kept_rows": int(kept_rows), "active_experts": int(active_experts)}
+    expert_gemm["ffn1_frac"] = expert_gemm["ffn1_tflops"] / peak
+    expert_gemm["ffn2_frac"] = expert_gemm["ffn2_tflops"] / peak
+    rb, pb, cb = hbm_bytes(w, kept_rows, routing)
+    hbm_ms = float(stage_ms[0] + stage_ms[1] + stage_ms[5])
+    gbs = (rb + pb + cb) / (hbm_ms * 1e-3) / 1e9
+    hbm = {"gbs": gbs, "peak_gbs": hbm_peak, "frac": gbs / hbm_peak, "frac_of_spec": gbs / SPEC_PEAKS["hbm_gbs"],
+           "ms": hbm_ms, "bytes": rb + pb + cb}
+    for name, b, i in (("route", rb, 0), ("permute", pb, 1), ("combine", cb, 5)):
+        g = b / (float(stage_ms[i]) * 1e-3) / 1e9
+        hbm[f"{name}_gbs"] = g
+        hbm[f"{name}_frac"] = g / hbm_peak
+    return roof, expert_gemm, hbm
 
 
 def max_over_ranks(ms: float, dist, device) -> float:
@@ -366,16 +444,18 @@ def run_ours(args, w, rank, world, local):
     if args.routing == "expert_choice":
         stats = None
         kept = w.E * layer.capacity
+        active = w.E if layer.capacity > 0 else 0
     else:
         stats = layer.stats()
         kept = int(stats["total_kept"])
+        active = int((layer.io["kept"] > 0).sum().item())
     code = moe.moe_check_device_error()
     if code:
         raise RuntimeError(f"device error flag {code} after the timed region")
 
     # ----------------------------------------------------------- end to end from host buffers
     if args.no_e2e or args.routing == "hash":
-        return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, None)
+        return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, None, active)
     # two pinned input and output batches, used round-robin; every step
     # uploads its whole x and downloads its whole output, overlapped with
     # the neighbouring steps' compute (MoELayer.run_host_batches)
@@ -393,7 +473,7 @@ def run_ours(args, w, rank, world, local):
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, "cuda")
-    return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms)
+    return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms, active)
 
 
 # ---------------------------------------------------------------------- training step
@@ -423,7 +503,7 @@ def train_line(args, w, world, ms, fst, bst, kept, clocks):
     """The training step's JSON line from its timings: ms per step, the
     forward's 7 and the backward's 8 mean stage times (ms), the kept rows."""
     pk, pk_kind = peaks()
-    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak, peak_name = tensor_peak(pk, ms * args.steps * 1e-3)
     nF = 2 * w.F if w.activation == wl.SWIGLU else w.F
     R = kept
     f1, f2 = gemm_flops(w, kept)                  # forward expert GEMMs
@@ -455,7 +535,8 @@ def train_line(args, w, world, ms, fst, bst, kept, clocks):
     else:
         roofline = {"kernel": f"grouped_gemm ({top}, backward)", "bound": "tensor", "achieved": gemm_tf[top],
                     "peak": peak, "unit": "TFLOP/s", "frac": gemm_tf[top] / peak,
-                    "peak_kind": f"bf16_tflops_sustained of {pk_kind}", "traffic": None,
+                    "peak_kind": f"{peak_name} of {pk_kind}", "traffic": None,
+                    "frac_of_spec": gemm_tf[top] / SPEC_PEAKS["bf16_tflops"],
                     "flops_per_step": flops[top], "ms_per_step": bms[top]}
     train_flops = f1 + f2 + sum(flops.values())
     gemm_ms = float(fst[2] + fst[3]) + sum(bms[k] for k in flops)
@@ -466,7 +547,8 @@ def train_line(args, w, world, ms, fst, bst, kept, clocks):
         "dtype": "bf16", "data": "synthetic", "config": dict(config_of(w), mode="train", aux_coef=0.01, z_coef=0.001),
         "roofline": roofline,
         "expert_gemm": {"tflops": train_flops / (gemm_ms * 1e-3) / 1e12,
-                        "frac_of_bf16_sustained": train_flops / (gemm_ms * 1e-3) / 1e12 / peak, "ms": gemm_ms,
+                        "frac_of_peak": train_flops / (gemm_ms * 1e-3) / 1e12 / peak, "peak_kind": peak_name,
+                        "ms": gemm_ms,
                         "backward_gemm_tflops": gemm_tf, "backward_gemm_roofline": gemm_roof},
         "stage_ms": {"forward": dict(zip(["route", "permute", "ffn1", "ffn2", "shared", "combine", "stats"],
                                          fst.tolist())), "backward": bms},
@@ -560,54 +642,23 @@ def run_train(args, w, rank, world, local):
     return 0
 
 
-def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms):
+def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms, active=None,
+           extra=None):
     if rank != 0:
         dist.destroy_process_group()
         return 0
-
-    pk, pk_kind = peaks()
-    f1, f2 = gemm_flops(w, kept)
-    ffn1_ms, ffn2_ms = float(stage_ms[2]), float(stage_ms[3])
-    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    rb, pb, cb = hbm_bytes(w, kept, args.routing)
-    hbm_ms = float(stage_ms[0] + stage_ms[1] + stage_ms[5])
-    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    gemm_ms = ffn1_ms + ffn2_ms + float(stage_ms[4])
-    # the first routed expert GEMM (the shared expert is its own stage): its
-    # FLOPs, and its algorithmic bytes (W1 (+W3) of every expert, x_perm
-    # read, H written); bound by whichever takes longer at the peaks
-    n1 = (2 if w.gated else 1) * w.F
-    f1r = 2.0 * kept * w.d * n1
-    b1r = float(w.E * n1 * w.d * w.elem_bytes + kept * w.d * w.elem_bytes + kept * w.F * w.elem_bytes)
-    kname = ("grouped_gemm_kernel (expert W1/W3 + SwiGLU)" if w.gated
-             else "grouped_gemm_kernel (expert W1 + activation)")
-    if b1r / (hbm_peak * 1e9) > f1r / (peak * 1e12):
-        gbs = b1r / (ffn1_ms * 1e-3) / 1e9
-        roofline = {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": gbs / hbm_peak, "peak_kind": f"hbm_gbs of {pk_kind}",
-                    "traffic": traffic_for_gemm(w, args.routing), "bytes_per_launch": b1r,
-                    "ms_per_launch": ffn1_ms}
-    else:
-        achieved = f1r / (ffn1_ms * 1e-3) / 1e12
-        roofline = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_kind": f"bf16_tflops_sustained of {pk_kind}",
-                    "traffic": traffic_for_gemm(w, args.routing), "flops_per_launch": f1r,
-                    "ms_per_launch": ffn1_ms}
+    active = w.E if active is None else active
+    roofline, expert_gemm, hbm = forward_roofline(w, kept, active, stage_ms, clocks, ms * args.steps * 1e-3,
+                                                  args.routing)
     line = {
         "metric": METRIC, "value": whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
         "data": "synthetic", "config": config_of(w, args.routing),
         "roofline": roofline,
-        "expert_gemm": {"tflops": (f1 + f2) / (gemm_ms * 1e-3) / 1e12,
-                        "frac_of_bf16_sustained": (f1 + f2) / (gemm_ms * 1e-3) / 1e12 / peak,
-                        "ms": gemm_ms, "kept_rows": kept},
-        "hbm_stages": {"gbs": (rb + pb + cb) / (hbm_ms * 1e-3) / 1e9, "peak_gbs": hbm_peak,
-                       "frac": (rb + pb + cb) / (hbm_ms * 1e-3) / 1e9 / hbm_peak, "ms": hbm_ms,
-                       "route_gbs": rb / (stage_ms[0] * 1e-3) / 1e9,
-                       "permute_gbs": pb / (stage_ms[1] * 1e-3) / 1e9,
-                       "combine_gbs": cb / (stage_ms[5] * 1e-3) / 1e9},
-        "stage_ms": {"route": stage_ms[0], "permute": stage_ms[1], "ffn1": ffn1_ms, "ffn2": ffn2_ms,
+        "expert_gemm": expert_gemm,
+        "hbm_stages": hbm,
+        "stage_ms": {"route": stage_ms[0], "permute": stage_ms[1], "ffn1": stage_ms[2], "ffn2": stage_ms[3],
                      "shared": stage_ms[4], "combine": stage_ms[5], "stats": stage_ms[6]},
         "clocks": clocks,
         "e2e": None if e2e_ms is None else {
@@ -616,6 +667,8 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
             "d2h_bytes_per_step": int(out.numel() * out.element_size()), "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step(w, args.routing) * args.steps,
     }
+    if extra:
+        line["workloads"] = extra
     if world == 1 and not args.no_cpu_baseline and args.routing == "topk":
         t, desc, cores = oracle_sample(w, inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": w.T / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -637,6 +690,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count (profiling of a smaller case; not a headline)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the routed expert count (profiling of another shape; not a headline)")
+    ap.add_argument("--top-k", type=int, default=None,
+                    help="override top_k (profiling of another shape; not a headline)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time the training step (forward keeping activations + backward) instead")
@@ -653,6 +710,9 @@ def main():
     w = wl.WORKLOADS[args.workload]
     if args.tokens is not None:
         w = w.scaled(args.tokens)
+    if args.experts is not None or args.top_k is not None:
+        w = w.with_(E=args.experts or w.E, k=args.top_k or w.k, name=f"{w.name}_E{args.experts or w.E}"
+                    f"_k{args.top_k or w.k}")
     if args.routing == "expert_choice":
         w = dataclasses.replace(w, capacity_factor=float(w.k))
     if args.impl == "reference":

@@ -484,6 +484,35 @@ moe_status_t moe_backward(const moe_config_t *cfg, const moe_weights_t *weights,
  * else a moe_status_t).  Synchronises the device first. */
 moe_status_t moe_check_device_error(int32_t *code);
 
+/*
+ * Process-wide switches (all devices, every host thread; they take effect
+ * at the next launch).  None is needed in normal use; they exist so that
+ * tests can run every kernel variant and exercise the device-side error
+ * path without a device fault.
+ *   MOE_OPT_PDL            1 (default): the library's kernels are launched
+ *                          with programmatic dependent launch; 0: plain
+ *                          stream order.
+ *   MOE_OPT_GEMM_PAIR      -1 (default): the expert GEMM kernel is chosen by
+ *                          shape; 0: always the one-CTA tcgen05 kernel;
+ *                          1: the CTA-pair (cta_group::2) kernel wherever
+ *                          it takes the problem.
+ *   MOE_OPT_WAIT_LIMIT_NS  bound, in ns, of every wait of the GEMM kernels
+ *                          on a tensor-core or copy barrier (default 2e9).
+ *                          A wait that runs out makes the kernel leave its
+ *                          loops, let the copies and MMAs it issued land,
+ *                          release its tensor memory and return, and raises
+ *                          MOE_ERR_DEVICE_TIMEOUT for moe_check_device_error;
+ *                          the outputs of that call are then undefined.
+ *                          A limit far below a kernel's run time (a few
+ *                          microseconds) forces this path on purpose.
+ * moe_set_option returns MOE_ERR_INVALID_ARG for an unknown option or a
+ * value out of range (PDL 0/1, GEMM_PAIR -1/0/1, WAIT_LIMIT_NS >= 0).
+ */
+enum { MOE_OPT_PDL = 0, MOE_OPT_GEMM_PAIR = 1, MOE_OPT_WAIT_LIMIT_NS = 2 };
+moe_status_t moe_set_option(int32_t option, int64_t value);
+/* Current value of an option (host output). */
+moe_status_t moe_get_option(int32_t option, int64_t *value);
+
 /* Message of the last failing call on this host thread (host buffer). */
 void moe_last_error(char *buf, size_t len);
 

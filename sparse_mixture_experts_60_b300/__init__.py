@@ -16,7 +16,8 @@ from __future__ import annotations
 import ctypes as C
 from typing import Dict, Optional
 
-from ._lib import (MOE_BWD_STAGE_EVENTS, MOE_STAGE_EVENTS, MOE_WS_BACKWARD, MoEBackwardOpts, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN,  # noqa: F401
+from ._lib import (MOE_OPT_GEMM_PAIR, MOE_OPT_PDL, MOE_OPT_WAIT_LIMIT_NS,  # noqa: F401
+                   MOE_BWD_STAGE_EVENTS, MOE_STAGE_EVENTS, MOE_WS_BACKWARD, MoEBackwardOpts, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN,  # noqa: F401
                    MOE_WS_FORWARD, MOE_WS_PERMUTE, MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEECIO, MoEGrads,
                    MoESaved, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
                    last_error, lib)
@@ -245,6 +246,17 @@ def moe_check_device_error() -> int:
     code = C.c_int32(0)
     check(lib().moe_check_device_error(C.byref(code)))
     return code.value
+
+
+def moe_set_option(option: int, value: int) -> None:
+    """Process-wide switch (MOE_OPT_PDL, MOE_OPT_GEMM_PAIR, MOE_OPT_WAIT_LIMIT_NS)."""
+    check(lib().moe_set_option(int(option), int(value)))
+
+
+def moe_get_option(option: int) -> int:
+    v = C.c_int64(0)
+    check(lib().moe_get_option(int(option), C.byref(v)))
+    return v.value
 
 
 def stats_from_buffer(buf) -> Dict:

@@ -16,6 +16,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_BAD_ALIGNMENT", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_DEVICE_TIMEOUT"}
+MOE_OPT_PDL, MOE_OPT_GEMM_PAIR, MOE_OPT_WAIT_LIMIT_NS = 0, 1, 2
 (MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_SHARED_FFN, MOE_WS_EXPERT_CHOICE,
  MOE_WS_BACKWARD) = range(7)
 
@@ -102,6 +103,8 @@ _SIGS = {
     "moe_route_expert_choice": ([P] * 6 + [P], C.c_int),
     "moe_forward_expert_choice": ([P] * 5 + [P, C.c_size_t, P], C.c_int),
     "moe_check_device_error": ([C.POINTER(C.c_int32)], C.c_int),
+    "moe_set_option": ([C.c_int32, C.c_int64], C.c_int),
+    "moe_get_option": ([C.c_int32, C.POINTER(C.c_int64)], C.c_int),
 }
 
 

@@ -39,6 +39,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -51,21 +53,81 @@ namespace moe {
 // ------------------------------------------------------------------ device flag
 __device__ int32_t g_moe_device_error = 0;
 
-int32_t *device_error_flag() {
-    static int32_t *ptr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!ptr[dev]) {
+// The context current on this thread (the driver's cuCtxGetCurrent, looked
+// up through the runtime so that the library does not link the driver).
+static void *current_context() {
+    using Fn = CUresult (*)(CUcontext *);
+    static Fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_moe_device_error) != cudaSuccess) return nullptr;
-        ptr[dev] = static_cast<int32_t *>(p);
-    }
-    return ptr[dev];
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<Fn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
 }
 
-bool pdl_enabled() {
-    const char *e = getenv("MOE_B300_PDL");
-    return !(e && e[0] == '0');
+void *symbol_address(SymbolCache &cache, const void *symbol) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SymbolCache::kDevices) return nullptr;
+    void *ctx = current_context();
+    std::lock_guard<std::mutex> lock(cache.mu);
+    if (!cache.ptr[dev] || !ctx || cache.ctx[dev] != ctx) {
+        void *p = nullptr;
+        // (makes the device's primary context current if no context was)
+        if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+        cache.ptr[dev] = p;
+        cache.ctx[dev] = current_context();
+    }
+    return cache.ptr[dev];
+}
+
+int32_t *device_error_flag() {
+    static SymbolCache cache;
+    return static_cast<int32_t *>(symbol_address(cache, (const void *)&g_moe_device_error));
+}
+
+// Process-wide switches set through moe_set_option (defaults: programmatic
+// dependent launch on, GEMM kernel chosen by shape, 2 s device waits).
+namespace {
+std::atomic<int64_t> g_opt_pdl{1};
+std::atomic<int64_t> g_opt_gemm_pair{-1};
+std::atomic<int64_t> g_opt_wait_ns{2000000000ll};
+}  // namespace
+
+bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
+int gemm_pair_option() { return (int)g_opt_gemm_pair.load(std::memory_order_relaxed); }
+uint64_t wait_limit_ns() { return (uint64_t)g_opt_wait_ns.load(std::memory_order_relaxed); }
+
+bool set_option(int option, int64_t value) {
+    switch (option) {
+        case 0:   // MOE_OPT_PDL
+            if (value != 0 && value != 1) return false;
+            g_opt_pdl.store(value);
+            return true;
+        case 1:   // MOE_OPT_GEMM_PAIR
+            if (value < -1 || value > 1) return false;
+            g_opt_gemm_pair.store(value);
+            return true;
+        case 2:   // MOE_OPT_WAIT_LIMIT_NS
+            if (value < 0) return false;
+            g_opt_wait_ns.store(value);
+            return true;
+        default:
+            return false;
+    }
+}
+bool get_option(int option, int64_t *value) {
+    switch (option) {
+        case 0: *value = g_opt_pdl.load(); return true;
+        case 1: *value = g_opt_gemm_pair.load(); return true;
+        case 2: *value = g_opt_wait_ns.load(); return true;
+        default: return false;
+    }
 }
 
 int num_sms() {
@@ -87,7 +149,7 @@ constexpr int BK = 64;                 // one 128-byte swizzle atom of bf16
 constexpr int UMMA_K = 16;
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;       // producer, MMA, epilogue
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDrainLimitNs = 2000000000ull;  // teardown waits: 2 s, whatever the wait limit
 
 template <int BN>
 struct Cfg {
@@ -135,16 +197,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait on a phase parity.  Returns false when the CTA is aborting
-// (flag already set) or the limit ran out (then sets both flags).
+// (flag already set) or the limit (ns of %globaltimer) ran out (then sets
+// both flags).
 __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                            int32_t *err) {
+                                            int32_t *err, uint64_t limit_ns) {
     const uint64_t t0 = global_timer();
     uint32_t n = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 15u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer() - t0 > kWaitLimitNs) {
+            if (global_timer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicExch(err, 6);  // MOE_ERR_DEVICE_TIMEOUT
                 return false;
@@ -153,15 +216,16 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, vola
     }
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *err) {
+                                          int32_t *err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort_flag, err);
+    return mbar_wait_slow(bar, parity, abort_flag, err, limit_ns);
 }
-// Wait bounded by time only (teardown: in-flight work must land first).
+// Wait bounded by time only (teardown: in-flight work must land first, so
+// this bound does not follow the configurable wait limit).
 __device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = global_timer();
     while (!mbar_try_wait(bar, parity))
-        if (global_timer() - t0 > kWaitLimitNs) return false;
+        if (global_timer() - t0 > kDrainLimitNs) return false;
     return true;
 }
 
@@ -277,6 +341,7 @@ struct Args {
     int64_t out_group_stride;  // K-grouped: elements between the groups' outputs
     int k_split;           // MN-major B: K below k_split from tmB, the rest from tmB2
     int n_inner;           // K-grouped: consecutive tiles walk N (else M) inside a group
+    uint64_t wait_ns;      // bound of every mbarrier wait (ns); a wait that runs out aborts the kernel
 };
 
 struct Tile {
@@ -720,7 +785,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
             const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
             bool ok = true;
             for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
-                if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, args.err)) {
+                if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, args.err, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -772,7 +837,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
         uint32_t aph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, args.err)) break;
+            if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, args.err, args.wait_ns)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
@@ -785,7 +850,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
                 const bool tail = KG_MN && kg_rows - kb * BK < BK;
                 const uint32_t par = tail ? (fph >> stage) & 1u : ph;
                 if (tail) fph ^= 1u << stage;
-                if (!mbar_wait(tail ? &fixed[stage] : &full[stage], par, abort_flag, args.err)) {
+                if (!mbar_wait(tail ? &fixed[stage] : &full[stage], par, abort_flag, args.err, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -832,7 +897,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
             const int rows = seg_s[tl.g + 1] - seg_s[tl.g];
             const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
             for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], ph, abort_flag, args.err))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], ph, abort_flag, args.err, args.wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -874,7 +939,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
             // tcgen05.ld below is warp-collective: leave only as a whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag, args.err))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag, args.err, args.wait_ns))) break;
             tc_fence_after();
             const int row_base = tl.row0 + q * 32;          // first row of this warp's 32
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -999,7 +1064,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
 }
 // bounded wait with cluster-scope acquire (arrivals may come from the peer CTA)
 __device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                               int32_t *err) {
+                                               int32_t *err, uint64_t limit_ns) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer();
     uint32_t n = 0;
@@ -1007,7 +1072,7 @@ __device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, v
         if (mbar_try_wait_cluster(bar, parity)) return true;
         if ((++n & 15u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer() - t0 > kWaitLimitNs) {
+            if (global_timer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicExch(err, 6);  // MOE_ERR_DEVICE_TIMEOUT
                 return false;
@@ -1129,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap *bmap = (GATED && rank == 1) ? &tmB2 : &tmB;
             bool ok = true;
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait_cluster(&empty[stage], ph ^ 1u, abort_flag, args.err)) {
+                if (!mbar_wait_cluster(&empty[stage], ph ^ 1u, abort_flag, args.err, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -1152,11 +1217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t aph = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += ncl) {
-            if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag, args.err)) break;
+            if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag, args.err, args.wait_ns)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait_cluster(&full[stage], ph, abort_flag, args.err)) {
+                if (!mbar_wait_cluster(&full[stage], ph, abort_flag, args.err, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -1187,7 +1252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t aph = 0;
         for (int tile = cid; tile < total; tile += ncl) {
             const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M);
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tfull[acc], aph, abort_flag, args.err))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tfull[acc], aph, abort_flag, args.err, args.wait_ns))) break;
             tc_fence_after();
             const int row_base = tl.row0 + BM * (int)rank + q * 32;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -1296,6 +1361,7 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     a.act = p.act;
     a.err = device_error_flag();
     if (!a.err) return cudaErrorUnknown;
+    a.wait_ns = wait_limit_ns();
     a.route = p.route ? *p.route : RouteEpilogue{};
     a.pre = p.pre;
     a.ld_pre = p.ld_pre;
@@ -1351,6 +1417,7 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     a.act = p.act;
     a.err = device_error_flag();
     if (!a.err) return cudaErrorUnknown;
+    a.wait_ns = wait_limit_ns();
     const size_t smem = C::smem_bytes(a.G);
     auto kern = grouped_gemm_pair_kernel<BN, GATED, OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1379,11 +1446,11 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
 // lose for the gated first expert GEMM; for the second (fp32 output) they
 // win with K = 4096 (Quick Start shape: 0.112 vs 0.125 ms) and lose with
 // K = 14336 (Mixtral shape: 3.12 vs 3.07 ms), so they run only the second
-// GEMM of tall groups with K <= 8192 by default.  MOE_B300_GEMM_PAIR=0 or 1
-// forces the choice (the tests run both kernels on the same shapes).
+// GEMM of tall groups with K <= 8192 by default.  The MOE_OPT_GEMM_PAIR
+// option forces the choice (the tests run both kernels on the same shapes).
 bool use_pair(const GemmProblem &p) {
-    const char *e = getenv("MOE_B300_GEMM_PAIR");
-    if (e && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+    const int opt = gemm_pair_option();
+    if (opt == 0 || opt == 1) return opt == 1;
     const int groups = p.seg ? p.G : 1;
     const int64_t rows_per_group = p.a_rows / (groups > 0 ? groups : 1);
     return rows_per_group >= 1024 && p.out_f32 && !p.gated && p.K <= 8192;

@@ -1153,6 +1153,19 @@ moe_status_t moe_forward_expert_choice(const moe_config_t *cfg, const moe_weight
     return MOE_OK;
 }
 
+moe_status_t moe_set_option(int32_t option, int64_t value) {
+    if (!set_option(option, value))
+        return fail(MOE_ERR_INVALID_ARG, "moe_set_option: unknown option %d or value %lld out of range", option,
+                    (long long)value);
+    return MOE_OK;
+}
+
+moe_status_t moe_get_option(int32_t option, int64_t *value) {
+    TRY(need(value, "value"));
+    if (!get_option(option, value)) return fail(MOE_ERR_INVALID_ARG, "moe_get_option: unknown option %d", option);
+    return MOE_OK;
+}
+
 moe_status_t moe_check_device_error(int32_t *code) {
     TRY(need(code, "code"));
     cudaError_t e = cudaDeviceSynchronize();

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 namespace moe {
@@ -19,6 +20,19 @@ constexpr int kMaxExperts = 1024;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Device address of one of the library's __device__ variables on the
+// current device, looked up once per (device, context) with that device
+// current: a cudaDeviceReset, or a primary context released and created
+// again, loads the module again at another address, so the cached address
+// is used only while the context it was looked up in is the current one.
+struct SymbolCache {
+    static constexpr int kDevices = 64;
+    std::mutex mu;
+    void *ctx[kDevices] = {};
+    void *ptr[kDevices] = {};
+};
+void *symbol_address(SymbolCache &cache, const void *symbol);
+
 // Device error flag shared by every kernel of the library (defined in
 // gemm_sm103.cu).  Returns its device address on the current device.
 int32_t *device_error_flag();
@@ -31,7 +45,7 @@ int num_sms();
 // launched as soon as every CTA of this one has started, so its launch and
 // prologue overlap this kernel's tail, and griddepcontrol.wait still holds it
 // until this grid has completed and its writes are visible.  Without the
-// launch attribute (MOE_B300_PDL=0, or launches from other code) both
+// launch attribute (MOE_OPT_PDL set to 0, or launches from other code) both
 // instructions are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -42,6 +56,9 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
     } while (0)
 
 bool pdl_enabled();
+// Process-wide options of moe_set_option (defined in gemm_sm103.cu).
+bool set_option(int option, int64_t value);
+bool get_option(int option, int64_t *value);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,

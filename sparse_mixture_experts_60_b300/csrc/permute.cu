@@ -335,18 +335,10 @@ __global__ void __launch_bounds__(256) perm_copy_kernel(const uint4 *x, int64_t 
 static __device__ __align__(256) int32_t g_perm_static_scratch[kPermStaticScratchInts];
 
 int32_t *permute_static_scratch() {
-    // one cudaGetSymbolAddress per device, made with that device current
-    static std::mutex mu;
-    static int32_t *ptr[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_perm_static_scratch) != cudaSuccess) return nullptr;
-        ptr[dev] = static_cast<int32_t *>(p);
-    }
-    return ptr[dev];
+    // one cudaGetSymbolAddress per device (and per context of that device),
+    // made with that device current
+    static SymbolCache cache;
+    return static_cast<int32_t *>(symbol_address(cache, (const void *)g_perm_static_scratch));
 }
 
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {

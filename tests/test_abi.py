@@ -212,3 +212,29 @@ int main(void) {
     assert int(bwd) > 0
     assert int(cap) == 4096                        # ceil(16384 / 8 * 2.0)
     assert int(st) == 1 and msg                    # MOE_ERR_INVALID_ARG with a message
+
+
+def test_options_are_checked_on_host(L):
+    """moe_set_option / moe_get_option: defaults, range checks, round trip
+    (host state only, nothing is launched)."""
+    assert moe.moe_get_option(moe.MOE_OPT_PDL) == 1
+    assert moe.moe_get_option(moe.MOE_OPT_GEMM_PAIR) == -1
+    assert moe.moe_get_option(moe.MOE_OPT_WAIT_LIMIT_NS) == 2_000_000_000
+    with pytest.raises(moe.MoEError, match="out of range"):
+        moe.moe_set_option(moe.MOE_OPT_WAIT_LIMIT_NS, -1)
+    with pytest.raises(moe.MoEError, match="out of range"):
+        moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, 2)
+    with pytest.raises(moe.MoEError, match="out of range"):
+        moe.moe_set_option(moe.MOE_OPT_PDL, 5)
+    with pytest.raises(moe.MoEError, match="unknown option"):
+        moe.moe_set_option(99, 0)
+    with pytest.raises(moe.MoEError, match="unknown option"):
+        moe.moe_get_option(99)
+    try:
+        moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, 0)
+        assert moe.moe_get_option(moe.MOE_OPT_GEMM_PAIR) == 0
+        moe.moe_set_option(moe.MOE_OPT_WAIT_LIMIT_NS, 12345)
+        assert moe.moe_get_option(moe.MOE_OPT_WAIT_LIMIT_NS) == 12345
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, -1)
+        moe.moe_set_option(moe.MOE_OPT_WAIT_LIMIT_NS, 2_000_000_000)

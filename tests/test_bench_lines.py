@@ -19,22 +19,44 @@ import bench  # noqa: E402
 from sparse_mixture_experts_60_b300 import workloads as wl  # noqa: E402
 
 CLOCKS = {"sm_mhz": 1275.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"], "samples": 10}
+PEAKS = {"hbm_gbs": 6486.5, "bf16_tflops": 1805.2, "bf16_tflops_sustained": 1405.8}
+
+
+@pytest.fixture(autouse=True)
+def fixed_peaks(monkeypatch):
+    """The lines are checked against fixed peaks, not this machine's file."""
+    monkeypatch.setattr(bench, "peaks", lambda: (dict(PEAKS), "measured"))
 KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
         "vs_baseline", "dtype", "data", "config", "roofline", "clocks", "e2e", "gpu_launches"}
 
-# measured on one B300 (ms): route, permute, ffn1, ffn2, shared, combine, stats; kept rows
+# measured on one B300 (ms): route, permute, ffn1, ffn2, shared, combine, stats; kept rows; experts
+# holding kept rows; bound of the first expert GEMM
 FORWARD = {
-    "mixtral": (9.3748, [0.04629, 0.09512, 5.88898, 3.16829, 0.00143, 0.15551, 0.01289], 32768, "tensor", 0.9338),
-    "deepseek_v3": (4.8929, [0.15674, 0.14200, 2.53212, 1.45942, 0.36588, 0.20369, 0.02652], 32768, "hbm", 0.9512),
-    "capacity_e128": (0.38982, [0.03563, 0.01909, 0.14534, 0.14765, 0.00156, 0.02042, 0.01446], 2879, "hbm",
-                      1.1692),
+    "mixtral": (9.3748, [0.04629, 0.09512, 5.88898, 3.16829, 0.00143, 0.15551, 0.01289], 32768, 8, "tensor"),
+    "deepseek_v3": (4.8929, [0.15674, 0.14200, 2.53212, 1.45942, 0.36588, 0.20369, 0.02652], 32768, 256, "hbm"),
+    "capacity_e128": (0.38982, [0.03563, 0.01909, 0.14534, 0.14765, 0.00156, 0.02042, 0.01446], 2879, 61, "hbm"),
 }
+
+
+def expected_frac(w, ms_ffn1, kept, active, steps, ms_step):
+    """First routed expert GEMM: FLOPs 2 kept d nF against the burst (timed
+    region under 1 s) or sustained bf16 peak, or bytes (W1 (+ W3) of the
+    experts with kept rows, x_perm read, H written) against the copy peak."""
+    nF = 2 * w.F if w.gated else w.F
+    flops = 2.0 * kept * w.d * nF
+    nbytes = (active * nF * w.d + kept * w.d + kept * w.F) * w.elem_bytes
+    tpk = PEAKS["bf16_tflops"] if steps * ms_step < 1000.0 else PEAKS["bf16_tflops_sustained"]
+    t_tc, t_hbm = flops / (tpk * 1e12), nbytes / (PEAKS["hbm_gbs"] * 1e9)
+    return max(t_tc, t_hbm) / (ms_ffn1 * 1e-3), "tensor" if t_tc >= t_hbm else "hbm"
 # forward stages as above; backward: gate_router, dh, dx, shared, dx_assemble, dW2, dW1|dW3, bias/router/shared
 TRAIN = {
     "mixtral": (29.966, [0.04647, 0.09398, 6.02053, 3.14277, 0.00140, 0.15314, 0.01104],
-                [0.18328, 3.36744, 5.82591, 0.00199, 0.33901, 3.53388, 7.02107, 0.19902], "tensor", 0.7832),
+                [0.18328, 3.36744, 5.82591, 0.00199, 0.33901, 3.53388, 7.02107, 0.19902], "tensor",
+                2.0 * 32768 * 28672 * 4096 / 7.02107e-3 / 1e12 / PEAKS["bf16_tflops"]),
     "deepseek_v3": (20.036, [0.12149, 0.12313, 2.30103, 1.28188, 0.31187, 0.19892, 0.02132],
-                    [0.34430, 1.18386, 2.33069, 0.31982, 0.22989, 3.57827, 7.15927, 0.50534], "hbm", 0.6729),
+                    [0.34430, 1.18386, 2.33069, 0.31982, 0.22989, 3.57827, 7.15927, 0.50534], "hbm",
+                    (4.0 * 256 * 4096 * 7168 + 2.0 * 32768 * (4096 + 2 * 7168)) / 7.15927e-3 / 1e9
+                    / PEAKS["hbm_gbs"]),
 }
 
 
@@ -42,12 +64,15 @@ def _args(steps=150, warmup=5, routing="topk"):
     return argparse.Namespace(steps=steps, warmup=warmup, routing=routing, no_cpu_baseline=True, cpu_seconds=1.0)
 
 
+@pytest.mark.parametrize("steps", [20, 150])
 @pytest.mark.parametrize("name", list(FORWARD))
-def test_forward_line(name, capsys):
-    ms, stages, kept, bound, frac = FORWARD[name]
+def test_forward_line(name, steps, capsys):
+    ms, stages, kept, active, bound = FORWARD[name]
     w = wl.WORKLOADS[name]
+    frac, bound2 = expected_frac(w, stages[2], kept, active, steps, ms)
+    assert bound2 == bound
     x = torch.empty(w.T, w.d, dtype=torch.bfloat16)
-    bench.finish(_args(), w, 0, 1, None, None, x, x, ms, stages, None, kept, CLOCKS, ms * 1.01)
+    bench.finish(_args(steps=steps), w, 0, 1, None, None, x, x, ms, stages, None, kept, CLOCKS, ms * 1.01, active)
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert KEYS <= set(line)
     assert line["n_gpus"] == 1 and line["scaling"] == "weak" and line["higher_is_better"] is True
@@ -60,7 +85,18 @@ def test_forward_line(name, capsys):
     assert r["unit"] == ("TFLOP/s" if bound == "tensor" else "GB/s")
     e2e = line["e2e"]
     assert e2e["h2d_bytes_per_step"] == e2e["d2h_bytes_per_step"] == w.T * w.d * 2
-    assert line["gpu_launches"] == bench.launches_per_step(w) * 150
+    assert line["gpu_launches"] == bench.launches_per_step(w) * steps
+    if bound == "tensor":
+        assert r["peak"] == (PEAKS["bf16_tflops"] if steps * ms < 1000.0 else PEAKS["bf16_tflops_sustained"])
+        assert r["frac_of_spec"] == pytest.approx(r["achieved"] / 2250.0)
+    else:
+        assert r["active_experts"] == active
+    # HBM stages: y and the output at the layer dtype (2 bytes)
+    h = line["hbm_stages"]
+    assert h["frac"] == pytest.approx(h["gbs"] / PEAKS["hbm_gbs"])
+    assert h["combine_gbs"] == pytest.approx(
+        (kept * w.d * 2 + w.T * w.d * 2 * (1 + int(w.residual) + int(w.num_shared > 0)) + w.T * w.k * 8)
+        / (stages[5] * 1e-3) / 1e9)
     if name != "mixtral":
         assert r["traffic"] is None                          # captured on the Mixtral forward only
     else:

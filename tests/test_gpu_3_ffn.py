@@ -13,12 +13,13 @@ from tests.gpu_util import as_f32, dev, float_check, host, weights
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["0", "1"], ids=["single_cta", "cta_pair"])
-def gemm_kernel(request, monkeypatch):
+@pytest.fixture(params=[0, 1], ids=["single_cta", "cta_pair"])
+def gemm_kernel(request):
     """Run the test with the single-CTA tcgen05 kernel, then with the CTA-pair
-    (cta_group::2) kernel (the library reads MOE_B300_GEMM_PAIR per launch)."""
-    monkeypatch.setenv("MOE_B300_GEMM_PAIR", request.param)
-    return request.param
+    (cta_group::2) kernel (the MOE_OPT_GEMM_PAIR option, read per launch)."""
+    moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, request.param)
+    yield request.param
+    moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, -1)
 
 
 def oracle_dispatch(w, inp):
@@ -27,7 +28,9 @@ def oracle_dispatch(w, inp):
     return r, orc.dispatch(w, r["idx"])
 
 
-def run_expert_ffn(w, inp, d_ref):
+def run_expert_ffn(w, inp, d_ref, expect_flag=0):
+    """y_perm rows 0 .. offsets[E]-1 of moe_expert_ffn on the oracle's
+    dispatch; the device error flag must read expect_flag afterwards."""
     cfg = moe.config_for(w)
     S, d = w.T * w.k, w.d
     X = inp["x"]
@@ -40,7 +43,7 @@ def run_expert_ffn(w, inp, d_ref):
     moe.moe_expert_ffn(cfg, dev(xp), dev(d_ref["offsets"]), W["w1"], W.get("b1"), W.get("w3"), W["w2"],
                        W.get("b2"), y, ws)
     torch.cuda.synchronize()
-    assert moe.moe_check_device_error() == 0
+    assert moe.moe_check_device_error() == expect_flag
     return host(y)[:nk]
 
 

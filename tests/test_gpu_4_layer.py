@@ -94,13 +94,17 @@ def test_tiny_layer_against_bruteforce():
     float_check(got["out"], dense, w, "tiny vs brute force")
 
 
-def test_layer_deterministic():
-    w = wl.WORKLOADS["deepseek_v3"].scaled(300)
+@pytest.mark.parametrize("name,T,ntok", LAYER_CASES)
+def test_layer_deterministic(name, T, ntok):
+    """Two forwards of the same layer on the same inputs, each with its own
+    buffers and workspace: every output and intermediate bit-identical."""
+    w = wl.WORKLOADS[name].scaled(T)
     inp = wl.make_inputs(w)
     _, a = run_layer(w, inp)
     _, b = run_layer(w, inp)
-    for key in ("out", "logits", "topk_idx", "topk_w", "lse", "prob_mean", "perm", "inv", "f"):
-        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    for key in ("out", "logits", "topk_idx", "topk_w", "lse", "prob_mean", "counts", "kept", "offsets", "perm",
+                "inv", "f"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=f"{name} {key}")
     assert a["stats"] == b["stats"]
 
 
