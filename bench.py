@@ -363,6 +363,94 @@ def run_reference(args, w, rank, world):
     return 0
 
 
+# ---------------------------------------------------------------------- the other workloads
+EXTRA = ("quickstart_bf16", "capacity_e128", "deepseek_v3", "tiny_fp32")
+
+
+def device_expert_weights(w, torch, seed):
+    """Expert weights of a workload drawn on the device (N(0, 0.02), the
+    workload's distribution; biases N(0, 0.02)), one matrix at a time: the
+    timing of the other workloads does not depend on the exact values, and
+    the 22.6 GB of the DeepSeek-V3 experts would take a minute on the host."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    dt = torch.bfloat16 if w.dtype == wl.BF16 else torch.float32
+
+    def stack(n, rows, cols):
+        out = torch.empty(n, rows, cols, dtype=dt, device="cuda")
+        for e in range(n):
+            out[e].copy_(torch.randn(rows, cols, generator=g, device="cuda") * 0.02)
+        return out
+
+    wts = {"w1": stack(w.E, w.F, w.d), "w2": stack(w.E, w.d, w.F)}
+    if w.gated:
+        wts["w3"] = stack(w.E, w.F, w.d)
+    if w.expert_bias:
+        wts["b1"] = (torch.randn(w.E, w.F, generator=g, device="cuda") * 0.02).to(dt)
+        wts["b2"] = (torch.randn(w.E, w.d, generator=g, device="cuda") * 0.02).to(dt)
+    if w.num_shared:
+        wts["shared_w1"] = stack(1, w.F, w.d)[0]
+        wts["shared_w2"] = stack(1, w.d, w.F)[0]
+        if w.gated:
+            wts["shared_w3"] = stack(1, w.F, w.d)[0]
+    return wts
+
+
+def time_extra(name, steps, warmup, torch, moe):
+    """Device-timed forward of another workload at its full size (the
+    router inputs and x from the seeded generators, so its routing is the
+    workload's; expert weights drawn on the device).  Returns the summary
+    kept in the headline line's "workloads" key."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, with_weights=False) if w.name != "tiny_fp32" else wl.make_inputs(w)
+    dev = upload(inp, torch)
+    wts = {k: dev[k] for k in ("w_router", "b_router", "w1", "b1", "w3", "w2", "b2", "shared_w1", "shared_w3",
+                               "shared_w2") if k in dev}
+    if "w1" not in wts:
+        wts.update(device_expert_weights(w, torch, 1000 + w.index))
+    layer = moe.MoELayer(moe.config_for(w), wts, dev.get("sel_bias"))
+    x = dev["x"]
+    out = torch.empty(w.T, w.d, dtype=layer.out_dtype(), device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        layer.forward(x, out)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_STAGE_EVENTS)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        layer.forward(x, out, stage_events=[e.cuda_event for e in evs[i]])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if moe.moe_check_device_error():
+        raise RuntimeError(f"device error flag after timing {name}")
+    ms = t0.elapsed_time(t1) / steps
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(7)] for i in range(steps)]).mean(0)
+    res = {"tokens_per_s": w.T / (ms * 1e-3), "ms_per_step": ms, "steps": steps, "tokens": w.T,
+           "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
+           "stage_ms": dict(zip(["route", "permute", "ffn1", "ffn2", "shared", "combine", "stats"],
+                                stage_ms.tolist())),
+           "weights": "router and x seeded as the workload; expert weights N(0, 0.02) drawn on the device"
+                      if w.name != "tiny_fp32" else "all seeded as the workload"}
+    if w.name == "tiny_fp32":
+        res["latency_us"] = ms * 1e3
+        res["note"] = "latency only: the layer (70 KB) stays in L2"
+    else:
+        kept = int(layer.stats()["total_kept"])
+        active = int((layer.io["kept"] > 0).sum().item())
+        roof, eg, hbm = forward_roofline(w, kept, active, stage_ms, {}, ms * steps * 1e-3)
+        res["roofline"] = {k: roof[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                "frac_of_spec", "peak_kind")}
+        res["expert_gemm"] = {k: eg[k] for k in ("tflops", "frac_of_peak", "ffn1_tflops", "ffn2_tflops",
+                                                 "kept_rows", "active_experts")}
+        res["hbm_stages"] = {k: hbm[k] for k in ("gbs", "frac", "route_frac", "permute_frac", "combine_frac")}
+    del layer, wts, dev
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------------- GPU path
 def run_ours(args, w, rank, world, local):
     import torch
@@ -453,9 +541,18 @@ def run_ours(args, w, rank, world, local):
     if code:
         raise RuntimeError(f"device error flag {code} after the timed region")
 
+    # ----------------------------------------------------------- the other workloads (headline run only)
+    extra = None
+    if rank == 0 and args.extra_steps > 0 and w.name == "mixtral" and args.routing == "topk" and not args.train:
+        extra = {}
+        with ClockSampler(uuid) as cs:
+            for name in EXTRA:
+                extra[name] = time_extra(name, args.extra_steps, 3, torch, moe)
+        extra["clocks"] = cs.summary()
     # ----------------------------------------------------------- end to end from host buffers
     if args.no_e2e or args.routing == "hash":
-        return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, None, active)
+        return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, None, active,
+                      extra)
     # two pinned input and output batches, used round-robin; every step
     # uploads its whole x and downloads its whole output, overlapped with
     # the neighbouring steps' compute (MoELayer.run_host_batches)
@@ -473,7 +570,8 @@ def run_ours(args, w, rank, world, local):
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, "cuda")
-    return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms, active)
+    return finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, clocks, e2e_ms, active,
+                  extra)
 
 
 # ---------------------------------------------------------------------- training step
@@ -695,6 +793,8 @@ def main():
     ap.add_argument("--top-k", type=int, default=None,
                     help="override top_k (profiling of another shape; not a headline)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--extra-steps", type=int, default=20,
+                    help="timed steps of each of the other workloads added to the headline (Mixtral) line; 0: none")
     ap.add_argument("--train", action="store_true",
                     help="time the training step (forward keeping activations + backward) instead")
     ap.add_argument("--routing", default="topk", choices=["topk", "expert_choice", "hash"],

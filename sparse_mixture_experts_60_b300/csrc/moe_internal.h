@@ -127,6 +127,12 @@ struct PermuteParams {
 // kernels, which spread the integer work over many SMs.
 constexpr int64_t kSmallSlots = 8192;
 constexpr int kSmallExperts = 256;
+// Up to this many chunks (kPermChunk slots each) the dispatch runs as one
+// kernel in which every CTA recounts the expert ids before its chunk
+// (no scratch, one launch for the whole integer dispatch); above it the
+// chunked kernels with the workspace tables (the recount would grow with
+// the square of the chunk count).
+constexpr int64_t kFusedChunks = 64;
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
 // Device address of the file-scope scratch of the allocation-free dispatch
 // (looked up once per device, on first use, with that device current).
@@ -166,7 +172,17 @@ struct RouteEpilogue {
     int32_t *part_cnt;     // [E, nblk]
     float *part_z;         // [nblk]
     int64_t nblk;          // ceil(T / kRouteTokPerCta)
+    // K split: every 128-token tile's K range is cut into ksplit units that
+    // run on different CTAs; kpart [tiles, ksplit, 128, E] holds their
+    // partial logits and kcount [tiles] (zeroed before the launch) counts
+    // the units that finished a tile
+    int ksplit;
+    float *kpart;
+    int32_t *kcount;
 };
+constexpr int kRouteMaxSplit = 8;
+// K splits of the router GEMM for T tokens and d_model d on sms SMs
+int route_ksplit(int64_t T, int d, int sms);
 
 struct GemmProblem {
     const bf16 *A; int64_t a_rows;           // A [a_rows, K]
@@ -207,8 +223,9 @@ struct SimtProblem {
 cudaError_t launch_ffn_simt(const SimtProblem &p, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine / stats
-cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_perm,
-                           const int32_t *inv, const float *topk_w, const float *shared_out,
+// y_perm and shared_out in the layer dtype (bf16 when dtype == 1, else fp32)
+cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const void *y_perm,
+                           const int32_t *inv, const float *topk_w, const void *shared_out,
                            const void *x_res, void *out, cudaStream_t s);
 struct StatsParams {
     int64_t T; int E, k; int64_t cap; int drop;
@@ -225,7 +242,7 @@ cudaError_t launch_bias_update(int64_t T, int E, int k, const int32_t *counts, f
 
 // ----------------------------------------------------------------- backward
 cudaError_t launch_combine_bwd(int64_t T, int d, int k, const bf16 *dout, const float *topk_w, const int32_t *inv,
-                               const float *y, bf16 *dy, float *dgate, cudaStream_t s);
+                               const bf16 *y, bf16 *dy, float *dgate, cudaStream_t s);
 cudaError_t launch_router_bwd(int64_t T, int E, int k, int score_fn, int renormalize, const float *logits,
                               const int32_t *topk_idx, const float *dgate, const int32_t *counts, float aux_coef,
                               float z_coef, float *dl, bf16 *dl_hi, bf16 *dl_lo, cudaStream_t s);

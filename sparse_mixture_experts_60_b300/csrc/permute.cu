@@ -166,6 +166,137 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *
     }
 }
 
+// Whole integer dispatch in one launch of nchunk CTAs and no scratch, for
+// layers of at most kFusedChunks chunks.  CTA c owns priorities
+// [c*kPermChunk, (c+1)*kPermChunk).  Every CTA first reads all S expert ids
+// (slot order, 16-byte loads) and counts, per expert, all slots (-> counts,
+// kept, offsets, the same in every CTA) and the slots of priority below its
+// chunk (-> its chunk's base per expert): the prefix over the chunks is
+// recomputed by each CTA instead of being exchanged, so no CTA waits for
+// another and nothing is written between launches.  Then the chunk's ranks
+// as in perm_rank_kernel.  CTA 0 writes counts, kept and offsets.
+__device__ __forceinline__ void count_slot(int e, int *h) {
+    // e >= 0: one more slot for expert e, summed over the warp's equal ids
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (e >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[e], __popc(peers));
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_fused_kernel(const int32_t *idx, int64_t T, int k, int E,
+                                                                  int64_t cap, int32_t *counts, int32_t *kept,
+                                                                  int32_t *offsets, int32_t *perm, int32_t *inv,
+                                                                  int32_t *err) {
+    PDL_ENTER();
+    extern __shared__ int sm[];
+    int *tot = sm;                       // [E] all slots per expert
+    int *bef = tot + E;                  // [E] slots of priority below this chunk
+    int *off_s = bef + E;                // [E + 1] offsets
+    int *wh = off_s + E + 1;             // [8][E] warp histograms, then warp running bases
+    __shared__ int scan_s[kPermThreads];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int nw = kPermThreads / 32;
+    for (int i = threadIdx.x; i < 2 * E + (E + 1) + nw * E; i += blockDim.x) sm[i] = 0;
+    __syncthreads();
+    const int64_t S = T * k;
+    const int64_t p0 = (int64_t)blockIdx.x * kPermChunk;
+    // A: histograms over every slot
+    auto classify = [&](int64_t s, int e) {
+        const bool ok = e >= 0 && e < E;
+        if (!ok && s < S) atomicExch(err, 1);  // MOE_ERR_INVALID_ARG
+        const int64_t t = s / k, j = s - t * k;
+        const bool before = ok && s < S && j * T + t < p0;
+        count_slot(ok && s < S ? e : -1, tot);
+        count_slot(before ? e : -1, bef);
+    };
+    const bool vec = (S & 3) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15) == 0;
+    if (vec) {
+        const int64_t nvec = S / 4;
+        for (int64_t b0 = 0; b0 < nvec; b0 += blockDim.x) {
+            const int64_t v = b0 + threadIdx.x;
+            int4 q = make_int4(-1, -1, -1, -1);
+            if (v < nvec) q = __ldg(reinterpret_cast<const int4 *>(idx) + v);
+            const int a4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) classify(v < nvec ? 4 * v + h : S, a4[h]);
+        }
+    } else {
+        for (int64_t b0 = 0; b0 < S; b0 += blockDim.x) {
+            const int64_t sl = b0 + threadIdx.x;
+            classify(sl < S ? sl : S, sl < S ? __ldg(idx + sl) : -1);
+        }
+    }
+    __syncthreads();
+    // B: kept and offsets (exclusive scan of kept over the experts), each
+    // thread a contiguous run of experts
+    const int per = (E + kPermThreads - 1) / kPermThreads;
+    const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+    int run = 0;
+    for (int e = e0; e < e1; ++e) run += (int)min((int64_t)tot[e], cap);
+    scan_s[threadIdx.x] = run;
+    __syncthreads();
+    for (int o = 1; o < kPermThreads; o <<= 1) {
+        const int add = threadIdx.x >= o ? scan_s[threadIdx.x - o] : 0;
+        __syncthreads();
+        scan_s[threadIdx.x] += add;
+        __syncthreads();
+    }
+    int before_run = scan_s[threadIdx.x] - run;
+    for (int e = e0; e < e1; ++e) {
+        const int kp = (int)min((int64_t)tot[e], cap);
+        off_s[e] = before_run;
+        if (blockIdx.x == 0) {
+            counts[e] = tot[e];
+            kept[e] = kp;
+            offsets[e] = before_run;
+        }
+        before_run += kp;
+    }
+    if (threadIdx.x == kPermThreads - 1) {
+        off_s[E] = scan_s[kPermThreads - 1];
+        if (blockIdx.x == 0) offsets[E] = scan_s[kPermThreads - 1];
+    }
+    __syncthreads();
+    // C: this chunk's ranks (warp w: priorities p0 + 256 w ..), as perm_rank_kernel
+    const int64_t pw = p0 + (int64_t)warp * kWarpSpan;
+    int *my = wh + warp * E;
+    for (int g = 0; g < kWarpSpan; g += 32) {
+        int64_t sl;
+        const int e = slot_expert(idx, pw + g + lane, T, k, E, S, &sl, err);
+        if (e >= 0) atomicAdd(&my[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int r = bef[e];
+        for (int w = 0; w < nw; ++w) {
+            const int c = wh[w * E + e];
+            wh[w * E + e] = r;
+            r += c;
+        }
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int g = 0; g < kWarpSpan; g += 32) {
+        int64_t sl = -1;
+        const int e = slot_expert(idx, pw + g + lane, T, k, E, S, &sl, err);
+        const unsigned peers = __match_any_sync(kFull, e);
+        int rank = 0;
+        if (e >= 0) rank = my[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && (peers & lt) == 0) my[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            if ((int64_t)rank < cap) {
+                const int row = off_s[e] + rank;
+                perm[row] = (int32_t)sl;
+                inv[sl] = row;
+            } else {
+                inv[sl] = -1;
+            }
+        } else if (e == -2) {
+            inv[sl] = -1;
+        }
+    }
+}
+
 // Whole integer dispatch in one CTA of 1024 threads, for layers of at most
 // kSmallSlots slots and kSmallExperts experts.  The top-k indices are first
 // copied into shared memory (16-bit, one vectorised pass), then warp w owns
@@ -358,6 +489,18 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
         }
         e = launch_pdl(perm_small_kernel, dim3(1), dim3(kSmallThreads), smem, s, p.topk_idx, (int)p.T, p.k, p.E,
                        p.cap, p.counts, p.kept, p.offsets, p.perm, p.inv, err);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k,
+                          nvec, p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
+    }
+    if (!p.chunked && nchunk > 0 && nchunk <= kFusedChunks) {
+        const size_t smem = (size_t)(2 * p.E + p.E + 1 + (kPermThreads / 32) * p.E) * sizeof(int);
+        if (smem > 48 * 1024) {
+            e = cudaFuncSetAttribute(perm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        e = launch_pdl(perm_fused_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), smem, s, p.topk_idx, p.T, p.k,
+                       p.E, p.cap, p.counts, p.kept, p.offsets, p.perm, p.inv, err);
         if (e != cudaSuccess) return e;
         return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k,
                           nvec, p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));

@@ -62,7 +62,8 @@ def test_permute_bit_exact_full_size(name):
 
 
 @pytest.mark.parametrize("case", ["one_expert_capacity", "k_equals_E", "single_token", "ragged_many_chunks",
-                                  "empty_experts", "e1024_drop", "fp32_k3_drop", "chunked_80k_slots"])
+                                  "empty_experts", "e1024_drop", "fp32_k3_drop", "fused_80k_slots",
+                                  "chunked_160k_slots"])
 def test_permute_edge_cases(case):
     g = np.random.default_rng(len(case))
     if case == "one_expert_capacity":
@@ -95,13 +96,20 @@ def test_permute_edge_cases(case):
                         capacity_factor=2.0, min_capacity=4)
         pop = np.exp(g.standard_normal(w.E) * 1.5)
         idx = np.stack([g.choice(w.E, 4, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
-    elif case == "chunked_80k_slots":
-        # far above the one-CTA dispatch limit: the chunked kernels
+    elif case == "fused_80k_slots":
+        # far above the one-CTA dispatch limit: 40 chunks, the one-launch dispatch
         w = wl.Workload(case, 48, T=40000, d=64, E=64, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                         dtype=wl.BF16, router_bias=False, expert_bias=False, drop_tokens=True,
                         capacity_factor=1.1, min_capacity=4)
         pop = np.exp(g.standard_normal(w.E))
         idx = np.stack([g.choice(w.E, 2, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
+    elif case == "chunked_160k_slots":
+        # above the one-launch limit (64 chunks): the chunked kernels with the workspace tables
+        w = wl.Workload(case, 51, T=40000, d=64, E=64, k=4, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
+                        dtype=wl.BF16, router_bias=False, expert_bias=False, drop_tokens=True,
+                        capacity_factor=1.1, min_capacity=4)
+        pop = np.exp(g.standard_normal(w.E))
+        idx = np.stack([g.choice(w.E, 4, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
     else:
         w = wl.Workload(case, 46, T=2049, d=36, E=6, k=3, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                         dtype=wl.F32, router_bias=False, expert_bias=False, drop_tokens=True,
@@ -117,10 +125,11 @@ def test_permute_empty_batch():
     assert got["counts"].tolist() == [0] * w.E and got["offsets"].tolist() == [0] * (w.E + 1)
 
 
-def test_permute_flags_out_of_range_expert():
+@pytest.mark.parametrize("T", [100, 6000], ids=["one_cta", "one_launch"])
+def test_permute_flags_out_of_range_expert(T):
     """An index outside [0, E) is skipped (slot dropped) and raises the
     library's device error flag, read back as MOE_ERR_INVALID_ARG."""
-    w = wl.Workload("bad_idx", 47, T=100, d=64, E=8, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
+    w = wl.Workload("bad_idx", 47, T=T, d=64, E=8, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                     dtype=wl.BF16, router_bias=False, expert_bias=False)
     g = np.random.default_rng(1)
     idx = np.stack([g.choice(8, 2, replace=False) for _ in range(w.T)]).astype(np.int32)
@@ -133,10 +142,11 @@ def test_permute_flags_out_of_range_expert():
     assert moe.moe_check_device_error() == 0   # read clears the flag
 
 
-def test_permute_unaligned_topk_idx():
+@pytest.mark.parametrize("T", [3001, 5001], ids=["one_cta", "one_launch"])
+def test_permute_unaligned_topk_idx(T):
     """topk_idx need not be 16-byte aligned: a view starting 4 bytes into a
     buffer gives the same dispatch."""
-    w = wl.Workload("unaligned", 49, T=3001, d=64, E=16, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
+    w = wl.Workload("unaligned", 49, T=T, d=64, E=16, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                     dtype=wl.BF16, router_bias=False, expert_bias=False)
     g = np.random.default_rng(3)
     idx = np.stack([g.choice(w.E, 2, replace=False) for _ in range(w.T)]).astype(np.int32)
