@@ -1,6 +1,8 @@
 """Pins of the oracle's backward: central finite differences of the
 oracle's own forward loss (an independent route to every gradient), and the
 E = 1 dense special case against torch autograd in fp64."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -159,3 +161,133 @@ def test_backward_units_equal_full_arrays():
         np.testing.assert_allclose(part["dw3_rows"][i], W3[f], rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(part["dw2_cols"][i], W2[:, f], rtol=1e-12, atol=1e-14)
     np.testing.assert_array_equal(part["dx"], full["dx"])
+
+
+# ------------------------------------------------------------ bf16 rounding points, worked by hand
+def _bf16(v: float) -> float:
+    """Nearest bf16 value of an fp64 number (ties to even), by rounding the
+    fp64 bit pattern to 7 fraction bits (finite normal values)."""
+    import struct
+    b = struct.unpack("<Q", struct.pack("<d", float(v)))[0]
+    drop = 52 - 7
+    rem = b & ((1 << drop) - 1)
+    b >>= drop
+    half = 1 << (drop - 1)
+    if rem > half or (rem == half and (b & 1)):
+        b += 1
+    return struct.unpack("<d", struct.pack("<Q", b << drop))[0]
+
+
+def _bf16_array(shape, g, scale):
+    return np.vectorize(_bf16)(g.standard_normal(shape) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("act", [wl.SWIGLU, wl.GELU])
+def test_backward_bf16_rounding_points_worked_by_hand(act):
+    """Three tokens, two experts, top-1 with the raw softmax gate, eight
+    hidden units, residual, bf16 storage.  Every gradient is worked out here
+    from the chain rule of the "MoE Training: Mixture of Experts" objective
+    (loss = <dout, out>; L = main + coef * aux with coef 0), with the bf16
+    rounding at each point where a bf16 layer stores a value: the forward's
+    H and expert output y, the stored pre-activations the activation
+    derivative reads, dy = gate * dout, and da.  Each rounding changes some
+    of its values here (checked), and with 24 rounded pre-activations per
+    point a change that large moves some rounded da, so moving or dropping
+    any one rounding in the oracle changes a gradient far beyond the 1e-12
+    tolerance."""
+    T, d, F, E = 3, 8, 8, 2
+    w = wl.Workload("bf16_pin", 84, T=T, d=d, E=E, k=1, F=F, activation=act, score_fn=wl.SOFTMAX, dtype=wl.BF16,
+                    router_bias=False, expert_bias=act != wl.SWIGLU, renormalize=False, residual=True)
+    g = np.random.default_rng(40 + act)
+    x = _bf16_array((T, d), g, 1.0)
+    wr = _bf16_array((E, d), g, 0.7)
+    w1 = _bf16_array((E, F, d), g, 0.6)
+    w2 = _bf16_array((E, d, F), g, 0.6)
+    dout = _bf16_array((T, d), g, 1.0)
+    inp = {"x": wl.bf16_round(x), "w_router": wl.bf16_round(wr), "w1": wl.bf16_round(w1), "w2": wl.bf16_round(w2)}
+    if act == wl.SWIGLU:
+        w3 = _bf16_array((E, F, d), g, 0.6)
+        inp["w3"] = wl.bf16_round(w3)
+    else:
+        b1 = _bf16_array((E, F), g, 0.3)
+        b2 = _bf16_array((E, d), g, 0.3)
+        inp["b1"], inp["b2"] = wl.bf16_round(b1), wl.bf16_round(b2)
+    base = orc.layer(w, inp)
+    gr = orc.backward(w, inp, base, dout.astype(np.float64), 0.0, 0.0)
+
+    bfv = np.vectorize(_bf16)
+    f64 = lambda a: np.asarray(a, np.float64)
+    silu = lambda v: v / (1.0 + np.exp(-v))
+    erf = np.vectorize(math.erf)
+    gelu = lambda v: 0.5 * v * (1.0 + erf(v / math.sqrt(2.0)))
+    dgelu = lambda v: 0.5 * (1.0 + erf(v / math.sqrt(2.0))) + v * np.exp(-0.5 * v * v) / math.sqrt(2 * math.pi)
+    Wr = f64(wr)
+    dx = np.zeros((T, d))
+    dW1, dW3, dW2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
+    db1, db2, dWr = np.zeros((E, F)), np.zeros((E, d)), np.zeros((E, d))
+    points = {k: [] for k in ("h", "y", "dy", "a1", "a3", "da1", "da3")}
+    for t in range(T):
+        X, D = f64(x[t]), f64(dout[t])
+        lg = f64(base["logits"][t])                      # fp32 router logits of the forward
+        e = int(base["idx"][t, 0])
+        assert e == int(np.argmax(lg))
+        p = np.exp(lg - lg.max())
+        p /= p.sum()
+        gate = p[e]                                      # raw softmax gate (top-1, no renormalisation)
+        W1, W2 = f64(w1[e]), f64(w2[e])
+        a1 = W1 @ X
+        if act == wl.SWIGLU:
+            a3 = f64(w3[e]) @ X
+            hv = silu(a1) * a3
+        else:
+            a1 = a1 + f64(b1[e])
+            hv = gelu(a1)
+        h = bfv(hv)
+        yv = W2 @ h + (f64(b2[e]) if act != wl.SWIGLU else 0.0)
+        y = bfv(yv)
+        dyv = gate * D
+        dy = bfv(dyv)
+        dh = W2.T @ dy
+        a1s = bfv(a1)                                    # the stored pre-activations the derivative reads
+        if act == wl.SWIGLU:
+            a3s = bfv(a3)
+            sg = 1.0 / (1.0 + np.exp(-a1s))
+            da1v = dh * a3s * sg * (1.0 + a1s * (1.0 - sg))
+            da3v = dh * a1s * sg
+            da3 = bfv(da3v)
+            points["a3"].append(a3)
+            points["da3"].append(da3v)
+        else:
+            da1v = dh * dgelu(a1s)
+        da1 = bfv(da1v)
+        for k_, v in (("h", hv), ("y", yv), ("dy", dyv), ("a1", a1), ("da1", da1v)):
+            points[k_].append(v)
+        dgate = float(D @ y)                             # the gate reads the stored y
+        assert gr["dgate"][t, 0] == pytest.approx(dgate, rel=1e-12, abs=1e-15)
+        dl = -p * p[e] * dgate                           # raw softmax: dl_c = p_c (dg [c = e] - p_e dg)
+        dl[e] += p[e] * dgate
+        np.testing.assert_allclose(gr["dlogits"][t], dl, rtol=1e-12, atol=1e-15)
+        dx[t] = W1.T @ da1 + D + dl @ Wr
+        if act == wl.SWIGLU:
+            dx[t] += f64(w3[e]).T @ da3
+            dW3[e] += np.outer(da3, X)
+        dW1[e] += np.outer(da1, X)
+        dW2[e] += np.outer(dy, h)
+        db1[e] += da1
+        db2[e] += dy
+        dWr += np.outer(dl, X)
+        np.testing.assert_allclose(base["out"][t], gate * y + X, rtol=1e-12, atol=1e-15)
+    for name, vals in points.items():                    # every rounding point is live
+        if vals:
+            v = np.concatenate([np.atleast_1d(u) for u in vals])
+            assert np.any(bfv(v) != v), name
+    tol = dict(rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(gr["dx"], dx, **tol)
+    np.testing.assert_allclose(gr["dw_router"], dWr, **tol)
+    np.testing.assert_allclose(gr["dw1"], dW1, **tol)
+    np.testing.assert_allclose(gr["dw2"], dW2, **tol)
+    if act == wl.SWIGLU:
+        np.testing.assert_allclose(gr["dw3"], dW3, **tol)
+    else:
+        np.testing.assert_allclose(gr["db1"], db1, **tol)
+        np.testing.assert_allclose(gr["db2"], db2, **tol)
