@@ -73,8 +73,9 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def config_of(w, routing="topk"):
-    return {"workload": w.name, "routing": routing, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d_model": w.d,
+def config_of(w, routing="topk", gemm_pair="auto"):
+    extra = {} if gemm_pair == "auto" else {"gemm_kernel": "cta_pair" if gemm_pair == "1" else "one_cta"}
+    return {**extra, "workload": w.name, "routing": routing, "tokens": w.T, "batch": w.batch, "seq": w.seq, "d_model": w.d,
             "experts": w.E, "top_k": w.k, "d_ff": w.F, "activation": ACT_NAME[w.activation],
             "score": "sigmoid" if w.score_fn == wl.SIGMOID else "softmax",
             "shared_experts": w.num_shared, "residual": bool(w.residual),
@@ -459,6 +460,8 @@ def run_ours(args, w, rank, world, local):
 
     mbuild.build()
     torch.cuda.set_device(local)
+    if args.gemm_pair != "auto":
+        moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, int(args.gemm_pair))
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -752,7 +755,7 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
         "metric": METRIC, "value": whole_job_value(w.T, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == wl.BF16 else "f32",
-        "data": "synthetic", "config": config_of(w, args.routing),
+        "data": "synthetic", "config": config_of(w, args.routing, getattr(args, "gemm_pair", "auto")),
         "roofline": roofline,
         "expert_gemm": expert_gemm,
         "hbm_stages": hbm,
@@ -793,6 +796,8 @@ def main():
     ap.add_argument("--top-k", type=int, default=None,
                     help="override top_k (profiling of another shape; not a headline)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gemm-pair", default="auto", choices=["auto", "0", "1"],
+                    help="expert GEMM kernel: chosen by shape (auto), one-CTA (0) or CTA-pair (1) tiles")
     ap.add_argument("--extra-steps", type=int, default=20,
                     help="timed steps of each of the other workloads added to the headline (Mixtral) line; 0: none")
     ap.add_argument("--train", action="store_true",

@@ -28,10 +28,10 @@
  *   - Dense tensors are row-major and contiguous.  Weight matrices use the
  *     nn.Linear layout [out_features, in_features]; expert weights are
  *     stacked over experts: w1, w3 [E, d_ff, d_model], w2 [E, d_model, d_ff].
- *   - "dtype" tensors (x, weights, expert biases, out, x_perm, the expert
- *     outputs y_perm and the shared expert's output) are fp32 or bf16 as
- *     moe_config_t.dtype says.  Router bias, selection bias, logits, gates,
- *     lse and probabilities are always fp32.  Index tensors are int32.
+ *   - "dtype" tensors (x, weights, expert biases, out, x_perm) are fp32 or
+ *     bf16 as moe_config_t.dtype says.  Router bias, selection bias, logits,
+ *     gates, lse, probabilities and y_perm are always fp32.  Index tensors
+ *     are int32.
  *   - x, out, x_perm, y_perm and every weight must be 16-byte aligned.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and never synchronises the device.
@@ -138,8 +138,8 @@ typedef struct {
  * routing members above): x_perm [T*k, d] and hidden [T*k, F] (H, the
  * input of the second expert GEMM) in the layer dtype; pre_act, the first
  * GEMM's pre-activations in bf16: [T*k, 2F] holding W1 x | W3 x for SwiGLU,
- * [T*k, F] holding W1 x + b1 for GELU / ReLU; y_perm [T*k, d] expert
- * outputs in the layer dtype; shared_pre_act [T, 2F or F] and shared_hidden [T, F] for the
+ * [T*k, F] holding W1 x + b1 for GELU / ReLU; y_perm [T*k, d] fp32 expert
+ * outputs; shared_pre_act [T, 2F or F] and shared_hidden [T, F] for the
  * shared expert.  Rows past offsets[E] are not written. */
 #define MOE_STAGE_EVENTS 8
 typedef struct {
@@ -159,7 +159,7 @@ typedef struct {
     void *x_perm;
     void *pre_act;
     void *hidden;
-    void *y_perm;
+    float *y_perm;
     void *shared_pre_act;
     void *shared_hidden;
 } moe_forward_io_t;
@@ -266,26 +266,23 @@ moe_status_t moe_permute_noalloc(const moe_config_t *cfg, const void *x, const i
  * moe_code.py Expert (ReLU; dropout is the identity in a forward pass);
  * SwiGLU is the three-matrix expert of the Mixtral parameter arithmetic.
  *   x_perm [T*k, d] dtype; offsets [E+1] device; weights as moe_weights_t.
- * Output: y_perm [T*k, d] dtype, rows 0 .. offsets[E]-1 written (each
- * row accumulated in fp32 and stored once, rounded to dtype: an expert's
- * output is a tensor of the layer's storage type, as in the Quick Start's
- * expert_output).  The hidden activation H is kept in the workspace in
- * dtype.
+ * Output: y_perm [T*k, d] fp32, rows 0 .. offsets[E]-1 written.
+ * The hidden activation H is kept in the workspace in dtype.
  * Workspace: moe_workspace_size(MOE_WS_EXPERT_FFN).
  */
 moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets,
                             const void *w1, const void *b1, const void *w3, const void *w2,
-                            const void *b2, void *y_perm, void *ws, size_t ws_bytes,
+                            const void *b2, float *y_perm, void *ws, size_t ws_bytes,
                             moe_stream_t stream);
 
 /*
  * The always-on shared expert (DeepSeek V3 page: shared experts) on every
  * token: z = FFN_shared(x), same activation as the routed experts, no
  * biases.  x [T,d] dtype; shared_w1/w3 [F,d]; shared_w2 [d,F].
- * Output: z [T,d] dtype.  Workspace: moe_workspace_size(MOE_WS_SHARED_FFN).
+ * Output: z [T,d] fp32.  Workspace: moe_workspace_size(MOE_WS_SHARED_FFN).
  */
 moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *shared_w1,
-                            const void *shared_w3, const void *shared_w2, void *z, void *ws,
+                            const void *shared_w3, const void *shared_w2, float *z, void *ws,
                             size_t ws_bytes, moe_stream_t stream);
 
 /*
@@ -294,11 +291,11 @@ moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *
  *   out_t = sum_{j : inv[t*k+j] >= 0} topk_w[t,j] y_perm[inv[t*k+j]]
  *           + shared_out[t] (if not NULL) + x[t] (if cfg->residual)
  * summed in fp32 in that order (j ascending), stored in dtype.
- *   y_perm [T*k, d] dtype; inv [T*k]; topk_w [T*k]; shared_out [T,d] dtype
+ *   y_perm [T*k, d] fp32; inv [T*k]; topk_w [T*k]; shared_out [T,d] fp32
  *   or NULL; x [T,d] dtype (required when residual); out [T,d] dtype.
  */
-moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int32_t *inv,
-                         const float *topk_w, const void *shared_out, const void *x, void *out,
+moe_status_t moe_combine(const moe_config_t *cfg, const float *y_perm, const int32_t *inv,
+                         const float *topk_w, const float *shared_out, const void *x, void *out,
                          moe_stream_t stream);
 
 /*
@@ -447,7 +444,7 @@ typedef struct {
     const void *x_perm;
     const void *pre_act;
     const void *hidden;
-    const void *y_perm;
+    const float *y_perm;
     const void *shared_pre_act;
     const void *shared_hidden;
 } moe_saved_t;

@@ -14,12 +14,9 @@
  *   - the sigmoid selection key of DeepSeek-V3-style routing is an fp32
  *     value (see orc_exp32 / orc_sigmoid32 below);
  *   - the aux-loss-free bias b_i is an fp32 parameter updated in place.
- * For bf16 layers the activation output H and each expert's output y are
- * rounded to bf16, because that is their storage precision: a bf16 Linear ->
- * activation -> Linear chain keeps H in bf16, and the expert's result is a
- * bf16 tensor before it is gate-weighted ("MoE Training: Mixture of
- * Experts", Quick Start MoELayer: expert_output = expert(x) is added as
- * score * expert_output).  The gate-weighted sum itself is fp64.
+ * For bf16 layers the activation output H is rounded to bf16, because that
+ * is the storage precision of the layer's intermediate (a bf16 Linear ->
+ * activation -> Linear chain keeps H in bf16).
  *
  * Functions and the passages they follow:
  *   orc_router_logits    "MoE Training: Mixture of Experts", Quick Start
@@ -486,7 +483,7 @@ static void expert_row(const orc_cfg *c, const void *W1, const void *B1, const v
     for (int64_t n = 0; n < d; ++n) {
         double acc = dot_row(W2, dt, e * d * F + n * F, h, F);
         if (c->activation != 2 && B2) acc += elem(B2, dt, e * d + n);
-        y[n] = (dt == 1) ? orc_round_bf16(acc) : acc;
+        y[n] = acc;
     }
 }
 
@@ -687,11 +684,11 @@ void orc_param_counts(int64_t d, int64_t F, int64_t E, int64_t k, int gated, int
  *   dW_r += dl x^T,  db_r += dl,  dx_t += W_r^T dl.
  *   The selection bias b_i enters only the choice, so it gets no gradient.
  * For bf16 layers the values the backward reads from bf16 storage are
- * rounded to bf16 at the points where they are stored: H and y (as in the
- * forward; dgate reads the stored y), the pre-activations a1 / a3 / a the
- * forward keeps for the backward (used by the activation derivative; H
- * itself is formed from the unrounded ones, as in the forward), dy and
- * da1 / da3 / da; everything else is fp64.
+ * rounded to bf16 at the points where they are stored: H (as in the
+ * forward), the pre-activations a1 / a3 / a the forward keeps for the
+ * backward (used by the activation derivative; H itself is formed from the
+ * unrounded ones, as in the forward), dy and da1 / da3 / da; everything
+ * else is fp64.
  *
  * Outputs (fp64, overwritten): dx [T,d], dw_router [E,d], db_router [E],
  * dw1 [E,F,d], db1 [E,F], dw3 [E,F,d], dw2 [E,d,F], db2 [E,d], dsw1 / dsw3
@@ -746,7 +743,7 @@ static void expert_backward_row(const orc_cfg *c, const void *W1, const void *B1
     for (int64_t n = 0; n < d; ++n) {
         double acc = dot_row(W2, dt, e * d * F + n * F, h, F);
         if (c->activation != 2 && B2) acc += elem(B2, dt, e * d + n);
-        y[n] = rnd(c, acc);
+        y[n] = acc;
     }
     for (int64_t f = 0; f < F; ++f) {
         double dh = 0.0;

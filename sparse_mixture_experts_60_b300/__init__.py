@@ -397,7 +397,7 @@ class TrainingLayer(MoELayer):
         self.io.update(x_perm=torch.empty(R, d, dtype=dt, device=dev),
                        pre_act=torch.empty(R, nF, dtype=torch.bfloat16, device=dev),
                        hidden=torch.empty(R, F, dtype=dt, device=dev),
-                       y_perm=torch.empty(R, d, dtype=dt, device=dev))
+                       y_perm=torch.empty(R, d, dtype=torch.float32, device=dev))
         if cfg.num_shared:
             self.io.update(shared_pre_act=torch.empty(max(T, 1), nF, dtype=torch.bfloat16, device=dev),
                            shared_hidden=torch.empty(max(T, 1), F, dtype=dt, device=dev))

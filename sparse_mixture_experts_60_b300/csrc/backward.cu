@@ -1,6 +1,5 @@
 // Backward of the layer, the kernels around the tensor-core GEMMs:
 //   combine backward  dy = gate * dout into the expert rows, dgate = <dout, y>
-//                     (y the stored bf16 expert outputs)
 //   router backward   dlogits from the gate Jacobian, L_aux and z-loss
 //   dx assembly       sum of the expert rows' dx, residual, shared expert,
 //                     and the router term dlogits W_r
@@ -59,7 +58,7 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t T, int d, int k, const bf16 *__restrict__ dout,
                                                           const float *__restrict__ topk_w,
                                                           const int32_t *__restrict__ inv,
-                                                          const bf16 *__restrict__ y, bf16 *__restrict__ dy,
+                                                          const float *__restrict__ y, bf16 *__restrict__ dy,
                                                           float *__restrict__ dgate) {
     PDL_ENTER();
     const int lane = threadIdx.x & 31;
@@ -74,13 +73,14 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(int64_t T, int d, int 
             continue;
         }
         const float g = __ldg(topk_w + t * k + j);
-        const uint4 *yr = reinterpret_cast<const uint4 *>(y + (int64_t)row * d);
+        const float4 *yr = reinterpret_cast<const float4 *>(y + (int64_t)row * d);
         uint4 *dyr = reinterpret_cast<uint4 *>(dy + (int64_t)row * d);
         float dot = 0.0f;
         for (int c = lane; c < nv; c += 32) {
-            float o[8], gy[8], yy[8];
+            float o[8], gy[8];
             unpack8(__ldg(go + c), o);
-            unpack8(__ldg(yr + c), yy);
+            const float4 y0 = __ldg(yr + 2 * c), y1 = __ldg(yr + 2 * c + 1);
+            const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 dot = fmaf(o[i], yy[i], dot);
@@ -463,7 +463,7 @@ cudaError_t launch_fill_range(int32_t *seg, int n, cudaStream_t s) {
 }
 
 cudaError_t launch_combine_bwd(int64_t T, int d, int k, const bf16 *dout, const float *topk_w, const int32_t *inv,
-                               const bf16 *y, bf16 *dy, float *dgate, cudaStream_t s) {
+                               const float *y, bf16 *dy, float *dgate, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     return launch_pdl(combine_bwd_kernel, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, T, d, k, dout, topk_w,
                       inv, y, dy, dgate);

@@ -19,143 +19,98 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// 16 bytes of a row as fp32: 8 bf16 values or 4 fp32 values.
-template <bool BF16>
-struct Chunk {
-    static constexpr int V = BF16 ? 8 : 4;
-    __device__ __forceinline__ static void load(const void *base, int64_t elem, float (&f)[V]) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(base) +
-                                                              elem * (BF16 ? 2 : 4)));
-        if constexpr (BF16) {
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                f[2 * h] = __uint_as_float(w[h] << 16);
-                f[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
-            }
-        } else {
-            f[0] = __uint_as_float(u.x);
-            f[1] = __uint_as_float(u.y);
-            f[2] = __uint_as_float(u.z);
-            f[3] = __uint_as_float(u.w);
-        }
-    }
-    __device__ __forceinline__ static void store(void *base, int64_t elem, const float (&f)[V]) {
-        uint4 u;
-        if constexpr (BF16) {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * h], f[2 * h + 1]);
-                w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-            }
-            u = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-            u = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                           __float_as_uint(f[3]));
-        }
-        *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(base) + elem * (BF16 ? 2 : 4)) = u;
-    }
-};
-
-// Gate-weighted combine, one warp per (token, span of columns):
+// One warp per token; each lane owns V consecutive output columns per step.
 //   out = sum_j w_j * y[inv_j]  (j ascending, dropped slots skipped)
 //         + z (shared expert) + x (residual), in fp32, stored in dtype.
-// y, z, x and out are all in the layer dtype.  A warp's span is U chunks of
-// 16 bytes per lane (U * 32 * V columns); every load of the span (the kept
-// rows, z, x) is issued before the first add, so a warp keeps
-// U * (k + 2) 16-byte loads in flight.  KC = k when it is 1, 2, 4 or 8
-// (loops unrolled), 0 for any other k <= kMaxTopK.
-template <bool BF16, int KC, int U>
-__global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, int64_t spans,
-                                                      const void *__restrict__ y, const int32_t *__restrict__ inv,
+// PRE: the rows already hold w_j * y (+ x for the token's first kept slot,
+// CombinePrep): out = sum_j y[inv_j] + z, + x only if no slot was kept.
+template <bool BF16, bool PRE = false>
+__global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, const float *__restrict__ y,
+                                                      const int32_t *__restrict__ inv,
                                                       const float *__restrict__ topk_w,
-                                                      const void *__restrict__ z, const void *__restrict__ x,
+                                                      const float *__restrict__ z, const void *__restrict__ x,
                                                       void *__restrict__ out) {
     PDL_ENTER();
-    using Ck = Chunk<BF16>;
-    constexpr int V = Ck::V;
-    constexpr int KM = KC > 0 ? KC : kMaxTopK;
+    constexpr int V = BF16 ? 8 : 4;
     const int lane = threadIdx.x & 31;
-    const int64_t unit = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int64_t t = unit / spans;
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int kk = KC > 0 ? KC : k;
-    const int c0 = (int)(unit - t * spans) * (U * 32 * V) + lane * V;   // first column of this lane
-    const int my_r = lane < kk ? __ldg(inv + t * kk + lane) : -1;
-    const float my_w = lane < kk ? __ldg(topk_w + t * kk + lane) : 0.0f;
-    int rows[KM];
-    float wts[KM];
+    const int my_r = lane < k ? inv[t * k + lane] : -1;
+    const float my_w = (!PRE && lane < k) ? topk_w[t * k + lane] : 1.0f;
+    int rows[kMaxTopK];
+    float wts[kMaxTopK];
 #pragma unroll
-    for (int j = 0; j < KM; ++j) {
+    for (int j = 0; j < kMaxTopK; ++j) {
         rows[j] = __shfl_sync(kFull, my_r, j);
         wts[j] = __shfl_sync(kFull, my_w, j);
     }
-    float acc[U][V];
+    // with prepared rows x is already in the first kept row
+    if (PRE && __any_sync(kFull, lane < k && my_r >= 0)) x = nullptr;
+    const int nchunk = d / V;
+    for (int c = lane; c < nchunk; c += 32) {
+        float acc[V];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
+        for (int i = 0; i < V; ++i) acc[i] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[u][i] = 0.0f;
-    if constexpr (KC > 0) {
-        float yv[KC][U][V];
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k && rows[j] >= 0) {
+                const float4 *src = reinterpret_cast<const float4 *>(y + (int64_t)rows[j] * d) + c * (V / 4);
 #pragma unroll
-        for (int j = 0; j < KC; ++j)
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int c = c0 + u * 32 * V;
-                if (rows[j] >= 0 && c < d) {
-                    Ck::load(y, (int64_t)rows[j] * d + c, yv[j][u]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < V; ++i) yv[j][u][i] = 0.0f;
-                }
-            }
-#pragma unroll
-        for (int j = 0; j < KC; ++j)
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (rows[j] >= 0)
-#pragma unroll
-                    for (int i = 0; i < V; ++i) acc[u][i] = fmaf(wts[j], yv[j][u][i], acc[u][i]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < KM; ++j) {
-            if (j < kk && rows[j] >= 0) {
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + u * 32 * V;
-                    if (c < d) {
-                        float v[V];
-                        Ck::load(y, (int64_t)rows[j] * d + c, v);
-#pragma unroll
-                        for (int i = 0; i < V; ++i) acc[u][i] = fmaf(wts[j], v[i], acc[u][i]);
+                for (int h = 0; h < V / 4; ++h) {
+                    const float4 u = __ldg(src + h);
+                    if (PRE) {
+                        acc[4 * h + 0] += u.x;
+                        acc[4 * h + 1] += u.y;
+                        acc[4 * h + 2] += u.z;
+                        acc[4 * h + 3] += u.w;
+                    } else {
+                        acc[4 * h + 0] = fmaf(wts[j], u.x, acc[4 * h + 0]);
+                        acc[4 * h + 1] = fmaf(wts[j], u.y, acc[4 * h + 1]);
+                        acc[4 * h + 2] = fmaf(wts[j], u.z, acc[4 * h + 2]);
+                        acc[4 * h + 3] = fmaf(wts[j], u.w, acc[4 * h + 3]);
                     }
                 }
             }
         }
-    }
-    float zv[U][V], xv[U][V];
+        if (z) {
+            const float4 *src = reinterpret_cast<const float4 *>(z + t * d) + c * (V / 4);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * 32 * V;
-#pragma unroll
-        for (int i = 0; i < V; ++i) zv[u][i] = xv[u][i] = 0.0f;
-        if (c < d) {
-            if (z) Ck::load(z, t * d + c, zv[u]);
-            if (x) Ck::load(x, t * d + c, xv[u]);
+            for (int h = 0; h < V / 4; ++h) {
+                const float4 u = __ldg(src + h);
+                acc[4 * h + 0] += u.x;
+                acc[4 * h + 1] += u.y;
+                acc[4 * h + 2] += u.z;
+                acc[4 * h + 3] += u.w;
+            }
         }
-    }
+        if (BF16) {
+            if (x) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(x) + t * d) + c);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * 32 * V;
-        if (c >= d) continue;
-        if (z)
+                for (int h = 0; h < 4; ++h) {
+                    acc[2 * h] += __uint_as_float(w[h] << 16);
+                    acc[2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                }
+            }
+            uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[u][i] += zv[u][i];
-        if (x)
-#pragma unroll
-            for (int i = 0; i < V; ++i) acc[u][i] += xv[u][i];
-        Ck::store(out, t * d + c, acc[u]);
+            for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+                o[h] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + t * d)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            if (x) {
+                const float4 u = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + t * d) + c);
+                acc[0] += u.x;
+                acc[1] += u.y;
+                acc[2] += u.z;
+                acc[3] += u.w;
+            }
+            reinterpret_cast<float4 *>(static_cast<float *>(out) + t * d)[c] =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
     }
 }
 
@@ -164,15 +119,14 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, i
 // first compacted into a per-warp shared list in slot order (ballots over 32
 // slots at a time), then summed in that order like the narrow kernel.
 template <bool BF16>
-__global__ void __launch_bounds__(256) combine_wide_kernel(int64_t T, int d, int k, const void *__restrict__ y,
+__global__ void __launch_bounds__(256) combine_wide_kernel(int64_t T, int d, int k, const float *__restrict__ y,
                                                            const int32_t *__restrict__ inv,
                                                            const float *__restrict__ topk_w,
-                                                           const void *__restrict__ z, const void *__restrict__ x,
+                                                           const float *__restrict__ z, const void *__restrict__ x,
                                                            void *__restrict__ out) {
     PDL_ENTER();
     extern __shared__ int wlist[];                       // [8 warps][k] rows, then [8][k] gates
-    using Ck = Chunk<BF16>;
-    constexpr int V = Ck::V;
+    constexpr int V = BF16 ? 8 : 4;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t t = (int64_t)blockIdx.x * 8 + warp;
     if (t >= T) return;
@@ -191,27 +145,60 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(int64_t T, int d, int
         n += __popc(b);
     }
     __syncwarp();
-    for (int c = lane * V; c < d; c += 32 * V) {
-        float acc[V], v[V];
+    for (int c = lane; c < d / V; c += 32) {
+        float acc[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] = 0.0f;
         for (int i = 0; i < n; ++i) {
-            Ck::load(y, (int64_t)rows[i] * d + c, v);
+            const float4 *src = reinterpret_cast<const float4 *>(y + (int64_t)rows[i] * d) + c * (V / 4);
             const float wv = wts[i];
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[q] = fmaf(wv, v[q], acc[q]);
+            for (int h = 0; h < V / 4; ++h) {
+                const float4 u = __ldg(src + h);
+                acc[4 * h + 0] = fmaf(wv, u.x, acc[4 * h + 0]);
+                acc[4 * h + 1] = fmaf(wv, u.y, acc[4 * h + 1]);
+                acc[4 * h + 2] = fmaf(wv, u.z, acc[4 * h + 2]);
+                acc[4 * h + 3] = fmaf(wv, u.w, acc[4 * h + 3]);
+            }
         }
         if (z) {
-            Ck::load(z, t * d + c, v);
+            const float4 *src = reinterpret_cast<const float4 *>(z + t * d) + c * (V / 4);
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[q] += v[q];
+            for (int h = 0; h < V / 4; ++h) {
+                const float4 u = __ldg(src + h);
+                acc[4 * h + 0] += u.x;
+                acc[4 * h + 1] += u.y;
+                acc[4 * h + 2] += u.z;
+                acc[4 * h + 3] += u.w;
+            }
         }
-        if (x) {
-            Ck::load(x, t * d + c, v);
+        if (BF16) {
+            if (x) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const bf16 *>(x) + t * d) + c);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int q = 0; q < V; ++q) acc[q] += v[q];
+                for (int h = 0; h < 4; ++h) {
+                    acc[2 * h] += __uint_as_float(w[h] << 16);
+                    acc[2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+                o[h] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            reinterpret_cast<uint4 *>(static_cast<bf16 *>(out) + t * d)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            if (x) {
+                const float4 u = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + t * d) + c);
+                acc[0] += u.x;
+                acc[1] += u.y;
+                acc[2] += u.z;
+                acc[3] += u.w;
+            }
+            reinterpret_cast<float4 *>(static_cast<float *>(out) + t * d)[c] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
-        Ck::store(out, t * d + c, acc);
     }
 }
 
@@ -335,32 +322,12 @@ __global__ void bias_update_kernel(int64_t S, int E, const int32_t *counts, floa
 
 }  // namespace
 
-template <bool BF16>
-cudaError_t launch_combine_t(int64_t T, int d, int k, const void *y, const int32_t *inv, const float *w,
-                             const void *z, const void *x, void *out, cudaStream_t s) {
-    // span per warp: U chunks of 16 bytes per lane, U = 4 for k <= 2, 2 for
-    // k <= 4, else 1 (registers hold U * (k + 2) chunks)
-    auto go = [&](auto kern, int U) {
-        const int64_t span_cols = (int64_t)U * 32 * Chunk<BF16>::V;
-        const int64_t spans = ceil_div(d, span_cols);
-        const unsigned grid = (unsigned)ceil_div(T * spans, 8);
-        return launch_pdl(kern, dim3(grid), dim3(256), 0, s, T, d, k, spans, y, inv, w, z, x, out);
-    };
-    switch (k) {
-        case 1: return go(combine_kernel<BF16, 1, 4>, 4);
-        case 2: return go(combine_kernel<BF16, 2, 4>, 4);
-        case 4: return go(combine_kernel<BF16, 4, 2>, 2);
-        case 8: return go(combine_kernel<BF16, 8, 1>, 1);
-        default: return go(combine_kernel<BF16, 0, 1>, 1);
-    }
-}
-
-cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const void *y_perm, const int32_t *inv,
-                           const float *topk_w, const void *shared_out, const void *x_res, void *out,
+cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_perm, const int32_t *inv,
+                           const float *topk_w, const float *shared_out, const void *x_res, void *out,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)ceil_div(T, 8);
     if (k > kMaxTopK) {
-        const unsigned grid = (unsigned)ceil_div(T, 8);
         const size_t smem = (size_t)16 * k * sizeof(int);
         auto kern = dtype == 1 ? combine_wide_kernel<true> : combine_wide_kernel<false>;
         if (smem > 48 * 1024) {
@@ -370,8 +337,17 @@ cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const void *y_per
         return launch_pdl(kern, dim3(grid), dim3(256), smem, s, T, d, k, y_perm, inv, topk_w, shared_out, x_res,
                           out);
     }
-    return dtype == 1 ? launch_combine_t<true>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out, s)
-                      : launch_combine_t<false>(T, d, k, y_perm, inv, topk_w, shared_out, x_res, out, s);
+    auto kern = dtype == 1 ? combine_kernel<true> : combine_kernel<false>;
+    return launch_pdl(kern, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, inv, topk_w, shared_out, x_res, out);
+}
+
+cudaError_t launch_combine_prepped(int64_t T, int d, int k, int dtype, const float *y_perm, const int32_t *inv,
+                                   const float *shared_out, const void *x_res, void *out, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    if (k > kMaxTopK) return cudaErrorInvalidValue;
+    auto kern = dtype == 1 ? combine_kernel<true, true> : combine_kernel<false, true>;
+    return launch_pdl(kern, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, T, d, k, y_perm, inv,
+                      static_cast<const float *>(nullptr), shared_out, x_res, out);
 }
 
 cudaError_t launch_stats(const StatsParams &p, cudaStream_t s) {

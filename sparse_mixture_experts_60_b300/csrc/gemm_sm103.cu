@@ -342,6 +342,9 @@ struct Args {
     int k_split;           // MN-major B: K below k_split from tmB, the rest from tmB2
     int n_inner;           // K-grouped: consecutive tiles walk N (else M) inside a group
     uint64_t wait_ns;      // bound of every mbarrier wait (ns); a wait that runs out aborts the kernel
+    // second expert GEMM of the layer forward: rows scaled by their gate,
+    // plus x for a token's first kept slot (GemmProblem::comb)
+    CombinePrep comb;
 };
 
 struct Tile {
@@ -519,13 +522,6 @@ __device__ __forceinline__ KRange k_range(const Args &args, const Tile &tl, cons
     return {0, num_kb};
 }
 
-// Part `split` of ks of a K range: blocks kb0 + n*split/ks .. kb0 + n*(split+1)/ks - 1.
-__device__ __forceinline__ KRange split_range(KRange kr, int split, int ks) {
-    if (ks == 1) return kr;
-    const int n = kr.kb1 - kr.kb0;
-    return {kr.kb0 + n * split / ks, kr.kb0 + n * (split + 1) / ks};
-}
-
 // Epilogue modes beyond the forward FFN: the activation backward of the
 // first expert GEMM, fused into the GEMM that produces dh = dy W2.
 constexpr int kEpiBwdGated = 100;   // SwiGLU: da1 = dh a3 silu'(a1), da3 = dh silu(a1)
@@ -544,6 +540,25 @@ __device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, 
                                               uint32_t tbase, int half, int lane, uint8_t *stg, bool zero_acc) {
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
     const int row = row_base + lane;
+    // combine preparation (fp32 output of a plain GEMM): this row's gate,
+    // and the token whose x it adds when it is the token's first kept slot
+    constexpr bool kComb = !GATED && OUT_F32 && EPI == 0;
+    bool comb = false;
+    float cgate = 1.0f;
+    int64_t ctok = -1;
+    if constexpr (kComb) {
+        const CombinePrep &cp = args.comb;
+        if (cp.perm && row < tl.seg_end) {
+            comb = true;
+            const int32_t sl = __ldg(cp.perm + row);
+            const int64_t t = sl / cp.k;
+            const int j = sl - (int)(t * cp.k);
+            cgate = __ldg(cp.gate + sl);
+            bool first = cp.x != nullptr;
+            for (int jj = 0; jj < j && first; ++jj) first = __ldg(cp.inv + t * cp.k + jj) < 0;
+            if (first) ctok = t;
+        }
+    }
 #pragma unroll 1
     for (int c = 32 * half; c < BN_OUT; c += 64) {
         const int col = tl.n0 + c;
@@ -617,6 +632,19 @@ __device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, 
                     for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
                 }
             }
+            if constexpr (kComb) {
+                if (comb) {
+                    if (ctok >= 0) {
+                        float xv[32];
+                        load_row32_bf16(args.comb.x, args.N, (int)ctok, (int)ctok + 1, col, xv);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = fmaf(cgate, v[i], xv[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= cgate;
+                    }
+                }
+            }
             store_chunk<OUT_F32>(v, out, args.ldo, col, args.N, row_base, tl.seg_end, stg, lane);
         }
     }
@@ -672,57 +700,6 @@ __device__ __forceinline__ void route_epilogue(const Args &args, const Tile &tl,
     if (lane == 0 && re.part_z) re.part_z[blk] = z;
 }
 
-__device__ __forceinline__ void epi_bar_sync() {
-    // named barrier 1: the four epilogue warps that hold the TMEM lane
-    // quadrants of a routing tile (warps 2-5)
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// One work unit of the router GEMM split along K (ks units per 128-token
-// tile; unit `split` summed K blocks split*nkb/ks .. (split+1)*nkb/ks-1).
-// Thread = token row r of the tile, v = its accumulator row.  With ks > 1
-// every unit stores its E partial logits per row to kpart[tile][split]
-// [128][E], and the unit that arrives last on the tile's counter (the
-// counters are zeroed before the launch) adds the ks partials in split
-// order, p0 + p1 + ... (the same bits whichever unit arrives last), and
-// runs the routing epilogue on the sums.  No unit waits for another.
-template <int EP>
-__device__ __forceinline__ void route_unit(const Args &args, const Tile &tl, int row_base, float (&v)[32],
-                                           int lane, int q, int tile, int split, int ks,
-                                           volatile int *last_flag) {
-    const RouteEpilogue &re = args.route;
-    const int E = args.N;
-    if (ks > 1) {
-        const int r = q * 32 + lane;
-        float *mine = re.kpart + (((int64_t)tile * ks + split) * BM + r) * E;
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-            if (e < E) mine[e] = v[e];
-        __threadfence();
-        epi_bar_sync();
-        if (q == 0 && lane == 0) *last_flag = atomicAdd(re.kcount + tile, 1) == ks - 1;
-        epi_bar_sync();
-        if (!*last_flag) return;
-        __threadfence();
-        float sum[EP];
-#pragma unroll
-        for (int e = 0; e < EP; ++e) sum[e] = 0.0f;
-        for (int j = 0; j < ks; ++j) {
-            const float *src = re.kpart + (((int64_t)tile * ks + j) * BM + r) * E;
-#pragma unroll
-            for (int e = 0; e < EP; ++e) {
-                if (e < E) {
-                    const float pj = j == split ? v[e] : __ldcg(src + e);
-                    sum[e] = j == 0 ? pj : sum[e] + pj;
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < EP; ++e) v[e] = sum[e];
-    }
-    route_epilogue<EP>(args, tl, row_base, v, lane);
-}
-
 // EPI: 0 forward FFN epilogue; 8 / 16 / 32 routing epilogue (router GEMM,
 // E <= EPI); kEpiBwdGated / kEpiBwdAct activation backward.
 // KG_MN: K-grouped with both operands MN-major, read in place from the
@@ -752,7 +729,6 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *consumed = abort_flag + 1;
-    volatile int *route_last = consumed + 2;   // after seg_bad: routing units, "this unit arrived last"
     // KG_MN: [STAGES] stage ready for the MMA, after drain and the flags
     uint64_t *fixed = bars + 2 * STAGES + 8;
     static_assert(!KG_MN || (3 * STAGES + 8) * 8 <= C::BAR_BYTES, "barrier area too small");
@@ -830,20 +806,16 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
     // segments must be monotone and inside A; otherwise the kernel does nothing
     const int total = *seg_bad ? 0 : pre_s[G];
     const int num_kb = (args.K + BK - 1) / BK;
-    // the router GEMM splits every tile's K range into ks work units
-    const int ks = (EPI > 0 && EPI <= 32) ? args.route.ksplit : 1;
-    const int units = total * ks;
     int issued = 0;  // producer: TMA stages issued
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t ph = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int tile = u / ks;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
             const int brow = args.kgroup ? tl.n0 : tl.g * args.b_group_rows + tl.n0;
-            const KRange kr = split_range(k_range<KG_MN>(args, tl, seg_s, num_kb), u - tile * ks, ks);
+            const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
             bool ok = true;
             for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, args.err, args.wait_ns)) {
@@ -897,13 +869,12 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
         int acc = 0;
         uint32_t aph = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, args.err, args.wait_ns)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            const int tile = u / ks;
             const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
-            const KRange kr = split_range(k_range<KG_MN>(args, tl, seg_s, num_kb), u - tile * ks, ks);
+            const KRange kr = k_range<KG_MN>(args, tl, seg_s, num_kb);
             const int kb0 = kr.kb0, kb1 = kr.kb1;
             // KG_MN: a group's partial last block waits for the fixer, the rest for TMA
             const int kg_rows = KG_MN ? seg_s[tl.g + 1] - seg_s[tl.g] : 0;
@@ -998,8 +969,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
         uint8_t *stg = sEpi + (warp - 2) * (32 * 64);
         int acc = 0;
         uint32_t aph = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int tile = u / ks;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile tl = tile_of(args, tile, seg_s, pre_s, G, BN_OUT, kg_tiles);
             // tcgen05.ld below is warp-collective: leave only as a whole warp
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], aph, abort_flag, args.err, args.wait_ns))) break;
@@ -1007,16 +977,11 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
             const int row_base = tl.row0 + q * 32;          // first row of this warp's 32
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI > 0 && EPI <= 32) {
-                // the accumulator row goes to registers and TMEM is released
-                // at once, so the next unit's MMAs need not wait for routing
-                float v[32];
-                if (half == 0) tmem_ld32(tbase, v);
-                tc_fence_before();
-                mbar_arrive(&tempty[acc]);
-                acc ^= 1;
-                if (acc == 0) aph ^= 1u;
-                if (half == 0) route_unit<EPI>(args, tl, row_base, v, lane, q, tile, u - tile * ks, ks, route_last);
-                continue;
+                if (half == 0) {
+                    float v[32];
+                    tmem_ld32(tbase, v);
+                    route_epilogue<EPI>(args, tl, row_base, v, lane);
+                }
             } else {
                 void *out = args.out;
                 bool zero_acc = false;
@@ -1434,8 +1399,8 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     a.err = device_error_flag();
     if (!a.err) return cudaErrorUnknown;
     a.wait_ns = wait_limit_ns();
+    a.comb = p.comb;
     a.route = p.route ? *p.route : RouteEpilogue{};
-    if (a.route.ksplit < 1 || !a.route.kpart || !a.route.kcount) a.route.ksplit = 1;
     a.pre = p.pre;
     a.ld_pre = p.ld_pre;
     a.kgroup = p.kgroup;
@@ -1491,6 +1456,7 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     a.err = device_error_flag();
     if (!a.err) return cudaErrorUnknown;
     a.wait_ns = wait_limit_ns();
+    a.comb = p.comb;
     const size_t smem = C::smem_bytes(a.G);
     auto kern = grouped_gemm_pair_kernel<BN, GATED, OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1516,42 +1482,21 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
 
 // CTA pairs pay off when groups are tall (a pair tile covers 256 rows, so
 // short expert segments would waste most of it).  Measured on B300: they
-// lose for the gated first expert GEMM; for the second (no activation) they
-// won with K = 4096 (Quick Start shape: 0.112 vs 0.125 ms) and lost with
-// K = 14336 (Mixtral shape: 3.12 vs 3.07 ms), so they run only the second
-// GEMM of tall groups with K <= 8192 by default.  The MOE_OPT_GEMM_PAIR
-// option forces the choice (the tests run both kernels on the same shapes).
+// lose for the gated first expert GEMM (Mixtral shape: 6.29 vs 5.97 ms);
+// for the second (no activation) they win (Quick Start shape, K = 4096:
+// 0.112 vs 0.125 ms; Mixtral shape, K = 14336: 3.12 vs 3.23 and 3.17 vs
+// 3.22 ms in two runs), so they run the second GEMM of tall groups.  The
+// MOE_OPT_GEMM_PAIR option forces the choice (the tests run both kernels
+// on the same shapes).
 bool use_pair(const GemmProblem &p) {
     const int opt = gemm_pair_option();
     if (opt == 0 || opt == 1) return opt == 1;
     const int groups = p.seg ? p.G : 1;
     const int64_t rows_per_group = p.a_rows / (groups > 0 ? groups : 1);
-    return rows_per_group >= 1024 && p.act == 0 && !p.gated && !p.route && p.K <= 8192;
+    return rows_per_group >= 1024 && p.act == 0 && !p.gated && !p.route;
 }
 
 }  // namespace
-
-// K splits of the router GEMM: enough work units that every SM takes
-// several (so that a unit's routing epilogue overlaps the next unit's
-// loads), each unit at least two K blocks, at most kRouteMaxSplit; among
-// the candidates the one whose busiest SM holds the least K work.
-int route_ksplit(int64_t T, int d, int sms) {
-    const int64_t tiles = (T + BM - 1) / BM;
-    const int nkb = (d + BK - 1) / BK;
-    if (tiles <= 0 || tiles >= 2 * (int64_t)sms) return 1;
-    const int hi = std::max(1, std::min(kRouteMaxSplit, nkb / 2));
-    const int want = (int)std::min<int64_t>(hi, std::max<int64_t>(1, (6 * (int64_t)sms + tiles - 1) / tiles));
-    int best = 1;
-    double best_cost = 1e30;
-    for (int k = std::max(1, want - 2); k <= hi; ++k) {
-        const double cost = (double)((tiles * k + sms - 1) / sms) / k;   // K work of the busiest SM, in tiles
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = k;
-        }
-    }
-    return best;
-}
 
 // Columns are written in 16-byte units: N % 4 == 0 for fp32 output, N % 8
 // for bf16; a bias needs whole 32-column chunks.  K % 8 == 0 keeps the TMA

@@ -75,21 +75,19 @@ int64_t route_blocks(const moe_config_t *c) { return ceil_div(c->num_tokens, kRo
 int64_t perm_chunks(const moe_config_t *c) { return ceil_div(c->num_tokens * c->top_k, kPermChunk); }
 
 // The bf16 router of at most 32 experts runs as one tensor-core GEMM with
-// the routing in its epilogue, its K range split over several CTAs.
+// the routing in its epilogue.
 bool fused_router(const moe_config_t *c) {
     return c->dtype == MOE_DTYPE_BF16 && c->num_experts <= 32 &&
            grouped_gemm_supported(c->num_experts, c->d_model, 0, 1, 0);
 }
-int64_t route_tiles(const moe_config_t *c) { return ceil_div(c->num_tokens, 128); }
 
 size_t route_ws(const moe_config_t *c) {
-    size_t n = 2 * align256((size_t)route_blocks(c) * c->num_experts * 4) + align256((size_t)route_blocks(c) * 4);
-    if (fused_router(c))   // split-K partial logits and the per-tile unit counters
-        n += align256((size_t)route_tiles(c) * kRouteMaxSplit * 128 * c->num_experts * 4) +
-             align256((size_t)route_tiles(c) * 4);
-    return n;
+    return 2 * align256((size_t)route_blocks(c) * c->num_experts * 4) + align256((size_t)route_blocks(c) * 4);
 }
-size_t permute_ws(const moe_config_t *c) { return 2 * align256((size_t)perm_chunks(c) * c->num_experts * 4); }
+size_t permute_ws(const moe_config_t *c) {
+    return 2 * align256((size_t)perm_chunks(c) * c->num_experts * 4) +
+           align256((size_t)c->num_tokens * c->top_k * 4);
+}
 size_t ffn_ws(const moe_config_t *c) {
     return align256((size_t)c->num_tokens * c->top_k * c->d_ff * elem_bytes(c));
 }
@@ -114,8 +112,8 @@ size_t forward_ws(const moe_config_t *c) {
     const size_t d = (size_t)c->d_model;
     size_t n = route_ws(c) + permute_ws(c) + ffn_ws(c) + shared_ws(c);
     n += align256(S * d * elem_bytes(c));                         // x_perm
-    n += align256(S * d * elem_bytes(c));                         // y_perm
-    if (c->num_shared) n += align256(T * d * elem_bytes(c));      // z
+    n += align256(S * d * 4);                                     // y_perm
+    if (c->num_shared) n += align256(T * d * 4);                  // z
     n += align256(T * E * 4) + 4 * align256(S * 4) + align256(T * 4);  // logits, idx, w, perm, inv, lse
     n += 4 * align256(E * 4) + align256((E + 1) * 4) + align256(sizeof(moe_stats_t));
     return n;
@@ -133,8 +131,8 @@ size_t ec_ws(const moe_config_t *c) {
     const size_t T = (size_t)c->num_tokens, E = (size_t)c->num_experts, d = (size_t)c->d_model;
     const size_t R = E * (size_t)ec_capacity_of(c), F = (size_t)c->d_ff;
     size_t n = align256(T * E * 4) * 3 + align256(R * 4) + align256((E + 1) * 4);   // logits, tok_row, gate, ...
-    n += align256(R * d * elem_bytes(c)) + align256(R * F * elem_bytes(c)) + align256(R * d * elem_bytes(c));
-    if (c->num_shared) n += shared_ws(c) + align256(T * d * elem_bytes(c));
+    n += align256(R * d * elem_bytes(c)) + align256(R * F * elem_bytes(c)) + align256(R * d * 4);
+    if (c->num_shared) n += shared_ws(c) + align256(T * d * 4);
     return n;
 }
 
@@ -222,8 +220,6 @@ struct RoutePartials {
     int32_t *cnt;      // [E, nblk]
     float *z;          // [nblk]
     int64_t nblk;
-    float *kpart;      // fused router: [tiles, kRouteMaxSplit, 128, E] split-K partial logits
-    int32_t *kcount;   // fused router: [tiles] units finished per tile
 };
 RoutePartials route_partials(const moe_config_t *c, void *ws) {
     Carve cv{static_cast<uint8_t *>(ws)};
@@ -232,12 +228,6 @@ RoutePartials route_partials(const moe_config_t *c, void *ws) {
     r.prob = cv.take<float>((size_t)r.nblk * c->num_experts * 4);
     r.cnt = cv.take<int32_t>((size_t)r.nblk * c->num_experts * 4);
     r.z = cv.take<float>((size_t)r.nblk * 4);
-    r.kpart = nullptr;
-    r.kcount = nullptr;
-    if (fused_router(c)) {
-        r.kpart = cv.take<float>((size_t)route_tiles(c) * kRouteMaxSplit * 128 * c->num_experts * 4);
-        r.kcount = cv.take<int32_t>((size_t)route_tiles(c) * 4);
-    }
     return r;
 }
 
@@ -272,16 +262,9 @@ moe_status_t route_impl(const moe_config_t *c, const void *x, const void *w_rout
     const bool fused_gemm = !logits_in && fused_router(c);
     if (fused_gemm) {
         // bf16, E <= 32: logits on the tensor cores with the routing in the
-        // GEMM's epilogue (one launch after the counters are zeroed)
+        // GEMM's epilogue (one launch)
         if (c->num_tokens > 0) {
             RouteEpilogue re{};
-            re.ksplit = route_ksplit(c->num_tokens, c->d_model, num_sms());
-            re.kpart = rp.kpart;
-            re.kcount = rp.kcount;
-            if (re.ksplit > 1) {
-                e = cudaMemsetAsync(rp.kcount, 0, (size_t)route_tiles(c) * 4, s);
-                if (e != cudaSuccess) return cuda_status(e, "router counters");
-            }
             re.b_router = b_router;
             re.sel_bias = sel_bias;
             re.k = c->top_k;
@@ -372,13 +355,15 @@ moe_status_t permute_impl(const moe_config_t *c, const void *x, const int32_t *t
     p.x_perm = x_perm;
     p.hist = cv.take<int32_t>((size_t)nch * c->num_experts * 4);
     p.base = cv.take<int32_t>((size_t)nch * c->num_experts * 4);
+    p.lrank = cv.take<int32_t>((size_t)c->num_tokens * c->top_k * 4);
     return cuda_status(launch_permute(p, s), "moe_permute launch");
 }
 
 // Two-layer FFN over row groups (routed: seg = offsets, G = E; shared: seg = null).
 moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, const int32_t *seg, int G, int M,
                       const void *w1, const void *b1, const void *w3, const void *w2, const void *b2, void *H,
-                      void *y, cudaStream_t s, void *mid_event = nullptr, void *pre = nullptr) {
+                      float *y, cudaStream_t s, void *mid_event = nullptr, void *pre = nullptr,
+                      const CombinePrep *comb = nullptr) {
     const int d = c->d_model, F = c->d_ff;
     const int gated = c->activation == MOE_ACT_SWIGLU;
     const int act = c->activation == MOE_ACT_GELU ? 1 : (c->activation == MOE_ACT_RELU ? 2 : 0);
@@ -422,11 +407,12 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
         g2.K = F;
         g2.out = y;
         g2.ldo = d;
-        g2.out_f32 = 0;          // y in the layer dtype
+        g2.out_f32 = 1;
         g2.bias = gated ? nullptr : static_cast<const bf16 *>(b2);
         g2.bias_stride = d;
         g2.act = 0;
         g2.gated = 0;
+        if (comb) g2.comb = *comb;
         e = launch_grouped_gemm(g2, s);
         return cuda_status(e, "expert FFN2 launch");
     }
@@ -459,7 +445,7 @@ moe_status_t ffn_impl(const moe_config_t *c, const void *A, int64_t a_rows, cons
     p2.max_rows = a_rows;
     p2.N = d;
     p2.K = F;
-    p2.out = static_cast<float *>(y);
+    p2.out = y;
     p2.ldo = d;
     p2.bias = gated ? nullptr : static_cast<const float *>(b2);
     p2.bias_stride = d;
@@ -637,7 +623,7 @@ moe_status_t moe_permute_noalloc(const moe_config_t *cfg, const void *x, const i
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
-                            const void *b1, const void *w3, const void *w2, const void *b2, void *y_perm,
+                            const void *b1, const void *w3, const void *w2, const void *b2, float *y_perm,
                             void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     const int64_t S = cfg->num_tokens * cfg->top_k;
@@ -653,7 +639,7 @@ moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *x_perm, const i
 }
 
 moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *shared_w1, const void *shared_w3,
-                            const void *shared_w2, void *z, void *ws, size_t ws_bytes, moe_stream_t stream) {
+                            const void *shared_w2, float *z, void *ws, size_t ws_bytes, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     if (cfg->num_shared != 1) return fail(MOE_ERR_INVALID_ARG, "moe_shared_ffn needs num_shared = 1");
     TRY(need16(x, "x", cfg->num_tokens));
@@ -664,8 +650,8 @@ moe_status_t moe_shared_ffn(const moe_config_t *cfg, const void *x, const void *
                     shared_w2, nullptr, ws, z, static_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int32_t *inv, const float *topk_w,
-                         const void *shared_out, const void *x, void *out, moe_stream_t stream) {
+moe_status_t moe_combine(const moe_config_t *cfg, const float *y_perm, const int32_t *inv, const float *topk_w,
+                         const float *shared_out, const void *x, void *out, moe_stream_t stream) {
     TRY(check_cfg(cfg));
     const int64_t T = cfg->num_tokens, S = T * cfg->top_k;
     TRY(need16(y_perm, "y_perm", S));
@@ -740,8 +726,8 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
     void *ws_ffn = cv.take<uint8_t>(ffn_ws(c));
     void *ws_shared = cv.take<uint8_t>(shared_ws(c));
     void *x_perm = cv.take<uint8_t>(S * d * elem_bytes(c));
-    void *y_perm = cv.take<uint8_t>(S * d * elem_bytes(c));
-    void *z = c->num_shared ? cv.take<uint8_t>(T * d * elem_bytes(c)) : nullptr;
+    float *y_perm = cv.take<float>(S * d * 4);
+    float *z = c->num_shared ? cv.take<float>(T * d * 4) : nullptr;
     moe_forward_io_t o{};
     if (io) o = *io;
     float *logits_ws = cv.take<float>(T * E * 4);
@@ -790,16 +776,34 @@ moe_status_t forward_impl(const moe_config_t *cfg, const moe_weights_t *w, const
     mark(1);
     TRY(permute_impl(c, x, o.topk_idx, o.counts, o.kept, o.offsets, o.perm, o.inv, x_perm, ws_perm, s));
     mark(2);
+    // bf16 layer without saved expert outputs (not a training forward, y_perm
+    // not requested): the second expert GEMM's epilogue applies the gates and
+    // adds the residual to each token's first kept row, so the combine reads
+    // no x and multiplies nothing
+    const bool prep = c->dtype == MOE_DTYPE_BF16 && !o.pre_act && !(io && io->y_perm);
+    CombinePrep cp{};
+    if (prep) {
+        cp.perm = o.perm;
+        cp.gate = o.topk_w;
+        cp.inv = o.inv;
+        cp.x = c->residual ? static_cast<const bf16 *>(x) : nullptr;
+        cp.k = c->top_k;
+    }
     TRY(ffn_impl(c, x_perm, (int64_t)S, o.offsets, c->num_experts, 0, w->w1, w->b1, w->w3, w->w2, w->b2, ws_ffn,
-                 y_perm, s, ev ? ev[3] : nullptr, o.pre_act));
+                 y_perm, s, ev ? ev[3] : nullptr, o.pre_act, prep ? &cp : nullptr));
     mark(4);
     if (c->num_shared)
         TRY(ffn_impl(c, x, (int64_t)T, nullptr, 1, (int)T, w->shared_w1, nullptr, w->shared_w3, w->shared_w2,
                      nullptr, ws_shared, z, s, nullptr, o.shared_pre_act));
     mark(5);
-    TRY(cuda_status(launch_combine(c->num_tokens, c->d_model, c->top_k, c->dtype, y_perm, o.inv, o.topk_w, z,
-                                   c->residual ? x : nullptr, out, s),
-                    "combine launch"));
+    if (prep)
+        TRY(cuda_status(launch_combine_prepped(c->num_tokens, c->d_model, c->top_k, c->dtype, y_perm, o.inv, z,
+                                               c->residual ? x : nullptr, out, s),
+                        "combine launch"));
+    else
+        TRY(cuda_status(launch_combine(c->num_tokens, c->d_model, c->top_k, c->dtype, y_perm, o.inv, o.topk_w, z,
+                                       c->residual ? x : nullptr, out, s),
+                        "combine launch"));
     mark(6);
     StatsParams sp{};
     sp.T = c->num_tokens;
@@ -936,9 +940,7 @@ moe_status_t backward_impl(const moe_config_t *c, const moe_weights_t *w, const 
 #define CU(call, what) TRY(cuda_status((call), what))
     mark(0);
     // combine and router backward
-    CU(launch_combine_bwd(b.T, d, (int)b.k, go, sv->topk_w, sv->inv, static_cast<const bf16 *>(sv->y_perm), dy,
-                          dgate, s),
-       "combine backward");
+    CU(launch_combine_bwd(b.T, d, (int)b.k, go, sv->topk_w, sv->inv, sv->y_perm, dy, dgate, s), "combine backward");
     CU(launch_router_bwd(b.T, E, (int)b.k, c->score_fn, c->renormalize, sv->logits, sv->topk_idx, dgate, sv->counts,
                          aux_coef, z_coef, dl, dl_hi, dl_lo, s),
        "router backward");
@@ -1147,9 +1149,9 @@ moe_status_t moe_forward_expert_choice(const moe_config_t *cfg, const moe_weight
     int32_t *off_ws = cv.take<int32_t>((E + 1) * 4);
     void *x_perm = cv.take<uint8_t>(R * d * elem_bytes(c));
     void *H = cv.take<uint8_t>(R * (size_t)c->d_ff * elem_bytes(c));
-    void *y_perm = cv.take<uint8_t>(R * d * elem_bytes(c));
+    float *y_perm = cv.take<float>(R * d * 4);
     void *ws_shared = c->num_shared ? cv.take<uint8_t>(shared_ws(c)) : nullptr;
-    void *z = c->num_shared ? cv.take<uint8_t>(T * d * elem_bytes(c)) : nullptr;
+    float *z = c->num_shared ? cv.take<float>(T * d * 4) : nullptr;
     if (!o.logits) o.logits = logits_ws;
     if (!o.tok_row) o.tok_row = tok_row_ws;
     if (!o.tok_gate) o.tok_gate = gate_ws;

@@ -120,6 +120,7 @@ struct PermuteParams {
     void *x_perm;
     int32_t *hist;         // [nchunk, E] scratch
     int32_t *base;         // [nchunk, E] scratch
+    int32_t *lrank;        // [T*k] scratch: rank of each slot within its chunk (two-launch dispatch)
     int chunked;           // 1: always the chunked kernels (which use hist/base)
 };
 // Layers up to this many slots and experts dispatch in one CTA without
@@ -127,12 +128,12 @@ struct PermuteParams {
 // kernels, which spread the integer work over many SMs.
 constexpr int64_t kSmallSlots = 8192;
 constexpr int kSmallExperts = 256;
-// Up to this many chunks (kPermChunk slots each) the dispatch runs as one
-// kernel in which every CTA recounts the expert ids before its chunk
-// (no scratch, one launch for the whole integer dispatch); above it the
-// chunked kernels with the workspace tables (the recount would grow with
-// the square of the chunk count).
-constexpr int64_t kFusedChunks = 64;
+// Layers whose chunk table (chunks of kPermChunk slots x experts) has at
+// most this many entries dispatch in two launches: per-chunk histograms and
+// ranks, then the row copy, each of whose CTAs rebuilds the chunk bases and
+// offsets from the table in shared memory; larger tables use the separate
+// histogram, scan and rank kernels.
+constexpr int64_t kTwoPassTable = 8192;
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s);
 // Device address of the file-scope scratch of the allocation-free dispatch
 // (looked up once per device, on first use, with that device current).
@@ -172,17 +173,19 @@ struct RouteEpilogue {
     int32_t *part_cnt;     // [E, nblk]
     float *part_z;         // [nblk]
     int64_t nblk;          // ceil(T / kRouteTokPerCta)
-    // K split: every 128-token tile's K range is cut into ksplit units that
-    // run on different CTAs; kpart [tiles, ksplit, 128, E] holds their
-    // partial logits and kcount [tiles] (zeroed before the launch) counts
-    // the units that finished a tile
-    int ksplit;
-    float *kpart;
-    int32_t *kcount;
 };
-constexpr int kRouteMaxSplit = 8;
-// K splits of the router GEMM for T tokens and d_model d on sms SMs
-int route_ksplit(int64_t T, int d, int sms);
+
+// Combine preparation in the epilogue of the second expert GEMM (fp32
+// output, layer forward): row r of slot s = perm[r] (token t = s / k, rank
+// j = s % k) stores gate[s] * y + x[t] when no slot of t before j was kept
+// (x: the residual, [T, N] bf16), else gate[s] * y.  perm null: off.
+struct CombinePrep {
+    const int32_t *perm;
+    const float *gate;
+    const int32_t *inv;
+    const bf16 *x;          // null without residual
+    int k;
+};
 
 struct GemmProblem {
     const bf16 *A; int64_t a_rows;           // A [a_rows, K]
@@ -209,6 +212,7 @@ struct GemmProblem {
     // cols] (row stride lda), B [K rows, N cols] (ldb); seg[g] .. seg[g+1]-1
     // are group g's rows (any offsets), K the total rows
     int kg_mn; int64_t lda, ldb;
+    CombinePrep comb;                        // second expert GEMM of the forward, or zeros
 };
 cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s);
 bool grouped_gemm_supported(int N, int K, int gated, int out_f32, int has_bias);
@@ -223,10 +227,14 @@ struct SimtProblem {
 cudaError_t launch_ffn_simt(const SimtProblem &p, cudaStream_t s);
 
 // ----------------------------------------------------------------- combine / stats
-// y_perm and shared_out in the layer dtype (bf16 when dtype == 1, else fp32)
-cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const void *y_perm,
-                           const int32_t *inv, const float *topk_w, const void *shared_out,
+cudaError_t launch_combine(int64_t T, int d, int k, int dtype, const float *y_perm,
+                           const int32_t *inv, const float *topk_w, const float *shared_out,
                            const void *x_res, void *out, cudaStream_t s);
+// The combine after a second expert GEMM with CombinePrep: y_perm rows hold
+// gate * y (+ x for a token's first kept slot); out = sum of the token's
+// kept rows (j ascending) + shared_out, + x only when no slot was kept.
+cudaError_t launch_combine_prepped(int64_t T, int d, int k, int dtype, const float *y_perm, const int32_t *inv,
+                                   const float *shared_out, const void *x_res, void *out, cudaStream_t s);
 struct StatsParams {
     int64_t T; int E, k; int64_t cap; int drop;
     const int32_t *counts, *kept; const float *prob_mean, *lse;
@@ -242,7 +250,7 @@ cudaError_t launch_bias_update(int64_t T, int E, int k, const int32_t *counts, f
 
 // ----------------------------------------------------------------- backward
 cudaError_t launch_combine_bwd(int64_t T, int d, int k, const bf16 *dout, const float *topk_w, const int32_t *inv,
-                               const bf16 *y, bf16 *dy, float *dgate, cudaStream_t s);
+                               const float *y, bf16 *dy, float *dgate, cudaStream_t s);
 cudaError_t launch_router_bwd(int64_t T, int E, int k, int score_fn, int renormalize, const float *logits,
                               const int32_t *topk_idx, const float *dgate, const int32_t *counts, float aux_coef,
                               float z_coef, float *dl, bf16 *dl_hi, bf16 *dl_lo, cudaStream_t s);

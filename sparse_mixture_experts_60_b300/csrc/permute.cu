@@ -11,7 +11,11 @@
 // all rank-0 slots in token order, then rank-1, ...).
 //
 // Priority index of slot (t, j) is p = j*T + t.  Chunks of kPermChunk
-// consecutive priorities are the unit of parallel work:
+// consecutive priorities are the unit of parallel work.  Layers up to
+// kSmallSlots slots dispatch in one CTA (perm_small_kernel); up to a chunk
+// table of kTwoPassTable entries in two launches (perm_local_kernel,
+// perm_copy_rank_kernel, below); larger ones, and the allocation-free
+// entry point, with four:
 //   perm_hist  : per-chunk expert histogram                    [nchunk, E]
 //   perm_scan  : exclusive scan over chunks per expert (chunk bases),
 //                counts, kept = min(counts, C), offsets = scan(kept)
@@ -41,7 +45,7 @@ __device__ __forceinline__ int slot_expert(const int32_t *idx, int64_t p, int64_
     *slot_out = s;
     const int e = idx[s];
     if (e < 0 || e >= E) {
-        atomicExch(err, 1);  // MOE_ERR_INVALID_ARG
+        if (err) atomicExch(err, 1);  // MOE_ERR_INVALID_ARG
         return -2;
     }
     return e;
@@ -166,134 +170,168 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *
     }
 }
 
-// Whole integer dispatch in one launch of nchunk CTAs and no scratch, for
-// layers of at most kFusedChunks chunks.  CTA c owns priorities
-// [c*kPermChunk, (c+1)*kPermChunk).  Every CTA first reads all S expert ids
-// (slot order, 16-byte loads) and counts, per expert, all slots (-> counts,
-// kept, offsets, the same in every CTA) and the slots of priority below its
-// chunk (-> its chunk's base per expert): the prefix over the chunks is
-// recomputed by each CTA instead of being exchanged, so no CTA waits for
-// another and nothing is written between launches.  Then the chunk's ranks
-// as in perm_rank_kernel.  CTA 0 writes counts, kept and offsets.
-__device__ __forceinline__ void count_slot(int e, int *h) {
-    // e >= 0: one more slot for expert e, summed over the warp's equal ids
-    const unsigned peers = __match_any_sync(kFull, e);
-    if (e >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[e], __popc(peers));
-}
-
-__global__ void __launch_bounds__(kPermThreads) perm_fused_kernel(const int32_t *idx, int64_t T, int k, int E,
-                                                                  int64_t cap, int32_t *counts, int32_t *kept,
-                                                                  int32_t *offsets, int32_t *perm, int32_t *inv,
-                                                                  int32_t *err) {
+// Dispatch in two launches (layers with nchunk * E <= kTwoPassTable):
+//   perm_local_kernel      chunk c (priorities c*kPermChunk ..): the chunk's
+//                          expert histogram -> hist[c][E], and every slot's
+//                          rank among the chunk's slots of its expert ->
+//                          lrank[slot] (8 warps x 256 priorities, warp bases
+//                          from a scan of the warp histograms, match-any
+//                          ranks 32 slots at a time)
+//   perm_copy_rank_kernel  every CTA first turns the small hist table into
+//                          chunk bases, counts, kept and offsets in shared
+//                          memory (recomputed per CTA instead of a third
+//                          launch); then warp per token: rank = base[chunk of
+//                          the slot][e] + lrank[slot], the capacity clamp,
+//                          perm / inv, and the row copy of x.
+__global__ void __launch_bounds__(kPermThreads) perm_local_kernel(const int32_t *idx, int64_t T, int k, int E,
+                                                                  int32_t *hist, int32_t *lrank, int32_t *err) {
     PDL_ENTER();
-    extern __shared__ int sm[];
-    int *tot = sm;                       // [E] all slots per expert
-    int *bef = tot + E;                  // [E] slots of priority below this chunk
-    int *off_s = bef + E;                // [E + 1] offsets
-    int *wh = off_s + E + 1;             // [8][E] warp histograms, then warp running bases
-    __shared__ int scan_s[kPermThreads];
+    extern __shared__ int wh[];          // [8][E] warp histograms, then warp running bases
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int nw = kPermThreads / 32;
-    for (int i = threadIdx.x; i < 2 * E + (E + 1) + nw * E; i += blockDim.x) sm[i] = 0;
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wh[i] = 0;
     __syncthreads();
     const int64_t S = T * k;
-    const int64_t p0 = (int64_t)blockIdx.x * kPermChunk;
-    // A: histograms over every slot
-    auto classify = [&](int64_t s, int e) {
-        const bool ok = e >= 0 && e < E;
-        if (!ok && s < S) atomicExch(err, 1);  // MOE_ERR_INVALID_ARG
-        const int64_t t = s / k, j = s - t * k;
-        const bool before = ok && s < S && j * T + t < p0;
-        count_slot(ok && s < S ? e : -1, tot);
-        count_slot(before ? e : -1, bef);
-    };
-    const bool vec = (S & 3) == 0 && (reinterpret_cast<uintptr_t>(idx) & 15) == 0;
-    if (vec) {
-        const int64_t nvec = S / 4;
-        for (int64_t b0 = 0; b0 < nvec; b0 += blockDim.x) {
-            const int64_t v = b0 + threadIdx.x;
-            int4 q = make_int4(-1, -1, -1, -1);
-            if (v < nvec) q = __ldg(reinterpret_cast<const int4 *>(idx) + v);
-            const int a4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) classify(v < nvec ? 4 * v + h : S, a4[h]);
-        }
-    } else {
-        for (int64_t b0 = 0; b0 < S; b0 += blockDim.x) {
-            const int64_t sl = b0 + threadIdx.x;
-            classify(sl < S ? sl : S, sl < S ? __ldg(idx + sl) : -1);
-        }
-    }
-    __syncthreads();
-    // B: kept and offsets (exclusive scan of kept over the experts), each
-    // thread a contiguous run of experts
-    const int per = (E + kPermThreads - 1) / kPermThreads;
-    const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
-    int run = 0;
-    for (int e = e0; e < e1; ++e) run += (int)min((int64_t)tot[e], cap);
-    scan_s[threadIdx.x] = run;
-    __syncthreads();
-    for (int o = 1; o < kPermThreads; o <<= 1) {
-        const int add = threadIdx.x >= o ? scan_s[threadIdx.x - o] : 0;
-        __syncthreads();
-        scan_s[threadIdx.x] += add;
-        __syncthreads();
-    }
-    int before_run = scan_s[threadIdx.x] - run;
-    for (int e = e0; e < e1; ++e) {
-        const int kp = (int)min((int64_t)tot[e], cap);
-        off_s[e] = before_run;
-        if (blockIdx.x == 0) {
-            counts[e] = tot[e];
-            kept[e] = kp;
-            offsets[e] = before_run;
-        }
-        before_run += kp;
-    }
-    if (threadIdx.x == kPermThreads - 1) {
-        off_s[E] = scan_s[kPermThreads - 1];
-        if (blockIdx.x == 0) offsets[E] = scan_s[kPermThreads - 1];
-    }
-    __syncthreads();
-    // C: this chunk's ranks (warp w: priorities p0 + 256 w ..), as perm_rank_kernel
-    const int64_t pw = p0 + (int64_t)warp * kWarpSpan;
+    const int64_t p0 = (int64_t)blockIdx.x * kPermChunk + (int64_t)warp * kWarpSpan;
     int *my = wh + warp * E;
     for (int g = 0; g < kWarpSpan; g += 32) {
         int64_t sl;
-        const int e = slot_expert(idx, pw + g + lane, T, k, E, S, &sl, err);
+        const int e = slot_expert(idx, p0 + g + lane, T, k, E, S, &sl, err);
         if (e >= 0) atomicAdd(&my[e], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int r = bef[e];
+        int run = 0;
         for (int w = 0; w < nw; ++w) {
             const int c = wh[w * E + e];
-            wh[w * E + e] = r;
-            r += c;
+            wh[w * E + e] = run;
+            run += c;
         }
+        hist[(int64_t)blockIdx.x * E + e] = run;
     }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
     for (int g = 0; g < kWarpSpan; g += 32) {
         int64_t sl = -1;
-        const int e = slot_expert(idx, pw + g + lane, T, k, E, S, &sl, err);
+        const int e = slot_expert(idx, p0 + g + lane, T, k, E, S, &sl, nullptr);
         const unsigned peers = __match_any_sync(kFull, e);
         int rank = 0;
         if (e >= 0) rank = my[e] + __popc(peers & lt);
         __syncwarp();
         if (e >= 0 && (peers & lt) == 0) my[e] += __popc(peers);
         __syncwarp();
-        if (e >= 0) {
-            if ((int64_t)rank < cap) {
-                const int row = off_s[e] + rank;
-                perm[row] = (int32_t)sl;
-                inv[sl] = row;
-            } else {
-                inv[sl] = -1;
-            }
-        } else if (e == -2) {
-            inv[sl] = -1;
+        if (e >= 0) lrank[sl] = rank;
+    }
+}
+
+__global__ void __launch_bounds__(256) perm_copy_rank_kernel(const uint4 *x, int64_t T, int k, int64_t nvec,
+                                                             const int32_t *idx, int E, int64_t cap,
+                                                             int64_t nchunk, const int32_t *hist,
+                                                             const int32_t *lrank, int32_t *counts, int32_t *kept,
+                                                             int32_t *offsets, int32_t *perm, int32_t *inv,
+                                                             uint4 *x_perm) {
+    PDL_ENTER();
+    extern __shared__ int tab[];         // [nchunk][E] chunk bases, then [E + 1] offsets
+    __shared__ int scan_s[256];
+    int *off_s = tab + nchunk * E;
+    const int lane = threadIdx.x & 31;
+    const int64_t S = T * k;
+    // the chunk table into shared memory in one coalesced pass, then chunk
+    // bases (exclusive prefix over chunks) and per-expert totals
+    const int64_t ntab = nchunk * E;
+    const bool vec = (ntab & 3) == 0 && (reinterpret_cast<uintptr_t>(hist) & 15) == 0;
+    if (vec) {
+        for (int64_t i = threadIdx.x; i < ntab / 4; i += blockDim.x)
+            reinterpret_cast<int4 *>(tab)[i] = __ldg(reinterpret_cast<const int4 *>(hist) + i);
+    } else {
+        for (int64_t i = threadIdx.x; i < ntab; i += blockDim.x) tab[i] = __ldg(hist + i);
+    }
+    __syncthreads();
+    const int per = (E + 255) / 256;
+    const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+    int run_kept = 0;
+    for (int e = e0; e < e1; ++e) {
+        int run = 0;
+        for (int64_t c = 0; c < nchunk; ++c) {
+            const int h = tab[c * E + e];
+            tab[c * E + e] = run;
+            run += h;
         }
+        off_s[e] = run;                  // the count, for now
+        run_kept += (int)min((int64_t)run, cap);
+    }
+    scan_s[threadIdx.x] = run_kept;
+    __syncthreads();
+    for (int o = 1; o < 256; o <<= 1) {
+        const int add = threadIdx.x >= o ? scan_s[threadIdx.x - o] : 0;
+        __syncthreads();
+        scan_s[threadIdx.x] += add;
+        __syncthreads();
+    }
+    int before = scan_s[threadIdx.x] - run_kept;
+    for (int e = e0; e < e1; ++e) {
+        const int cnt = off_s[e];
+        const int kp = (int)min((int64_t)cnt, cap);
+        if (blockIdx.x == 0) {
+            counts[e] = cnt;
+            kept[e] = kp;
+            offsets[e] = before;
+        }
+        off_s[e] = before;
+        before += kp;
+    }
+    if (threadIdx.x == 255) {
+        off_s[E] = scan_s[255];
+        if (blockIdx.x == 0) offsets[E] = scan_s[255];
+    }
+    __syncthreads();
+    // unused tail of perm -> -1
+    {
+        const int64_t used = off_s[E];
+        const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        const int64_t gsz = (int64_t)gridDim.x * blockDim.x;
+        for (int64_t i = used + gtid; i < S; i += gsz) perm[i] = -1;
+    }
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_row = -1;
+    if (lane < k) {
+        const int64_t sl = t * k + lane;
+        const int e = __ldg(idx + sl);
+        if (e >= 0 && e < E) {
+            const int64_t pr = (int64_t)lane * T + t;           // priority of slot (t, lane)
+            const int rank = tab[(pr / kPermChunk) * E + e] + __ldg(lrank + sl);
+            if ((int64_t)rank < cap) {
+                my_row = off_s[e] + rank;
+                perm[my_row] = (int32_t)sl;
+            }
+        }
+        inv[sl] = my_row;                                        // -1: dropped or invalid (flagged earlier)
+    }
+    int rows[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(kFull, my_row, j);
+    const uint4 *src = x + t * nvec;
+    int64_t v = lane;
+    for (; v + 96 < nvec; v += 128) {
+        uint4 a0 = __ldg(src + v), a1 = __ldg(src + v + 32), a2 = __ldg(src + v + 64),
+              a3 = __ldg(src + v + 96);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k && rows[j] >= 0) {
+                uint4 *dst = x_perm + (int64_t)rows[j] * nvec;
+                dst[v] = a0;
+                dst[v + 32] = a1;
+                dst[v + 64] = a2;
+                dst[v + 96] = a3;
+            }
+        }
+    }
+    for (; v < nvec; v += 32) {
+        const uint4 a = __ldg(src + v);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k && rows[j] >= 0) x_perm[(int64_t)rows[j] * nvec + v] = a;
     }
 }
 
@@ -493,17 +531,23 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
         return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k,
                           nvec, p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
     }
-    if (!p.chunked && nchunk > 0 && nchunk <= kFusedChunks) {
-        const size_t smem = (size_t)(2 * p.E + p.E + 1 + (kPermThreads / 32) * p.E) * sizeof(int);
-        if (smem > 48 * 1024) {
-            e = cudaFuncSetAttribute(perm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (!p.chunked && nchunk > 0 && nchunk * p.E <= kTwoPassTable) {
+        const size_t smem1 = (size_t)(kPermThreads / 32) * p.E * sizeof(int);
+        if (smem1 > 48 * 1024) {
+            e = cudaFuncSetAttribute(perm_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
             if (e != cudaSuccess) return e;
         }
-        e = launch_pdl(perm_fused_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), smem, s, p.topk_idx, p.T, p.k,
-                       p.E, p.cap, p.counts, p.kept, p.offsets, p.perm, p.inv, err);
+        e = launch_pdl(perm_local_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), smem1, s, p.topk_idx, p.T,
+                       p.k, p.E, p.hist, p.lrank, err);
         if (e != cudaSuccess) return e;
-        return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k,
-                          nvec, p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
+        const size_t smem2 = (size_t)(nchunk * p.E + p.E + 1) * sizeof(int);
+        if (smem2 > 48 * 1024) {
+            e = cudaFuncSetAttribute(perm_copy_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_pdl(perm_copy_rank_kernel, copy_grid, dim3(256), smem2, s, static_cast<const uint4 *>(p.x), p.T,
+                          p.k, nvec, p.topk_idx, p.E, p.cap, nchunk, p.hist, p.lrank, p.counts, p.kept, p.offsets,
+                          p.perm, p.inv, static_cast<uint4 *>(p.x_perm));
     }
     if (nchunk > 0) {
         e = launch_pdl(perm_hist_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), p.E * sizeof(int), s,

@@ -77,13 +77,10 @@ def _ws_expect(w):
     nblk = -(-T // 32)
     nch = -(-S // 2048)
     route = 2 * a(nblk * E * 4) + a(nblk * 4)
-    if w.dtype == wl.BF16 and E <= 32:          # router GEMM split along K: partial logits, unit counters
-        tiles = -(-T // 128)
-        route += a(tiles * 8 * 128 * E * 4) + a(tiles * 4)
-    perm = 2 * a(nch * E * 4)
+    perm = 2 * a(nch * E * 4) + a(S * 4)
     ffn = a(S * F * eb)
     shared = a(T * F * eb) if w.num_shared else 0
-    fwd = route + perm + ffn + shared + a(S * d * eb) + a(S * d * eb) + (a(T * d * eb) if w.num_shared else 0)
+    fwd = route + perm + ffn + shared + a(S * d * eb) + a(S * d * 4) + (a(T * d * 4) if w.num_shared else 0)
     fwd += a(T * E * 4) + 4 * a(S * 4) + a(T * 4) + 4 * a(E * 4) + a((E + 1) * 4) + a(32)
     return dict(route=route, perm=perm, ffn=ffn, shared=shared, fwd=fwd)
 

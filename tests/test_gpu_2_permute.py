@@ -62,7 +62,7 @@ def test_permute_bit_exact_full_size(name):
 
 
 @pytest.mark.parametrize("case", ["one_expert_capacity", "k_equals_E", "single_token", "ragged_many_chunks",
-                                  "empty_experts", "e1024_drop", "fp32_k3_drop", "fused_80k_slots",
+                                  "empty_experts", "e1024_drop", "fp32_k3_drop", "two_pass_80k_slots",
                                   "chunked_160k_slots"])
 def test_permute_edge_cases(case):
     g = np.random.default_rng(len(case))
@@ -96,16 +96,17 @@ def test_permute_edge_cases(case):
                         capacity_factor=2.0, min_capacity=4)
         pop = np.exp(g.standard_normal(w.E) * 1.5)
         idx = np.stack([g.choice(w.E, 4, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
-    elif case == "fused_80k_slots":
-        # far above the one-CTA dispatch limit: 40 chunks, the one-launch dispatch
+    elif case == "two_pass_80k_slots":
+        # far above the one-CTA dispatch limit: 40 chunks x 64 experts, the two-launch dispatch
         w = wl.Workload(case, 48, T=40000, d=64, E=64, k=2, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                         dtype=wl.BF16, router_bias=False, expert_bias=False, drop_tokens=True,
                         capacity_factor=1.1, min_capacity=4)
         pop = np.exp(g.standard_normal(w.E))
         idx = np.stack([g.choice(w.E, 2, replace=False, p=pop / pop.sum()) for _ in range(w.T)]).astype(np.int32)
     elif case == "chunked_160k_slots":
-        # above the one-launch limit (64 chunks): the chunked kernels with the workspace tables
-        w = wl.Workload(case, 51, T=40000, d=64, E=64, k=4, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
+        # a chunk table of 79 x 128 entries, above the two-launch limit: the
+        # histogram, scan and rank kernels with the workspace tables
+        w = wl.Workload(case, 51, T=40000, d=64, E=128, k=4, F=64, activation=wl.GELU, score_fn=wl.SOFTMAX,
                         dtype=wl.BF16, router_bias=False, expert_bias=False, drop_tokens=True,
                         capacity_factor=1.1, min_capacity=4)
         pop = np.exp(g.standard_normal(w.E))
@@ -125,7 +126,7 @@ def test_permute_empty_batch():
     assert got["counts"].tolist() == [0] * w.E and got["offsets"].tolist() == [0] * (w.E + 1)
 
 
-@pytest.mark.parametrize("T", [100, 6000], ids=["one_cta", "one_launch"])
+@pytest.mark.parametrize("T", [100, 6000], ids=["one_cta", "two_launch"])
 def test_permute_flags_out_of_range_expert(T):
     """An index outside [0, E) is skipped (slot dropped) and raises the
     library's device error flag, read back as MOE_ERR_INVALID_ARG."""
@@ -142,7 +143,7 @@ def test_permute_flags_out_of_range_expert(T):
     assert moe.moe_check_device_error() == 0   # read clears the flag
 
 
-@pytest.mark.parametrize("T", [3001, 5001], ids=["one_cta", "one_launch"])
+@pytest.mark.parametrize("T", [3001, 5001], ids=["one_cta", "two_launch"])
 def test_permute_unaligned_topk_idx(T):
     """topk_idx need not be 16-byte aligned: a view starting 4 bytes into a
     buffer gives the same dispatch."""

@@ -38,8 +38,7 @@ def run_expert_ffn(w, inp, d_ref, expect_flag=0):
     xp = np.zeros((max(S, 1), d), X.dtype)
     xp[:nk] = X[d_ref["perm"][:nk] // w.k]             # host-side gather of the rows
     W = weights(inp)
-    ydt = torch.float32 if w.dtype == wl.F32 else torch.bfloat16      # expert outputs in the layer dtype
-    y = torch.full((max(S, 1), d), float("nan"), dtype=ydt, device="cuda")
+    y = torch.full((max(S, 1), d), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(max(moe.moe_workspace_size(cfg, moe.MOE_WS_EXPERT_FFN), 1), dtype=torch.uint8, device="cuda")
     moe.moe_expert_ffn(cfg, dev(xp), dev(d_ref["offsets"]), W["w1"], W.get("b1"), W.get("w3"), W["w2"],
                        W.get("b2"), y, ws)
@@ -108,7 +107,7 @@ def test_shared_ffn(gemm_kernel):
     inp = wl.make_inputs(w)
     cfg = moe.config_for(w)
     W = weights(inp)
-    z = torch.full((w.T, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    z = torch.full((w.T, w.d), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(moe.moe_workspace_size(cfg, moe.MOE_WS_SHARED_FFN), dtype=torch.uint8, device="cuda")
     moe.moe_shared_ffn(cfg, dev(inp["x"]), W["shared_w1"], W["shared_w3"], W["shared_w2"], z, ws)
     torch.cuda.synchronize()

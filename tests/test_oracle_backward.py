@@ -189,8 +189,8 @@ def test_backward_bf16_rounding_points_worked_by_hand(act):
     from the chain rule of the "MoE Training: Mixture of Experts" objective
     (loss = <dout, out>; L = main + coef * aux with coef 0), with the bf16
     rounding at each point where a bf16 layer stores a value: the forward's
-    H and expert output y, the stored pre-activations the activation
-    derivative reads, dy = gate * dout, and da.  Each rounding changes some
+    H, the stored pre-activations the activation derivative reads,
+    dy = gate * dout, and da (the expert output y is kept in fp32).  Each rounding changes some
     of its values here (checked), and with 24 rounded pre-activations per
     point a change that large moves some rounded da, so moving or dropping
     any one rounding in the oracle changes a gradient far beyond the 1e-12
@@ -225,7 +225,7 @@ def test_backward_bf16_rounding_points_worked_by_hand(act):
     dx = np.zeros((T, d))
     dW1, dW3, dW2 = np.zeros((E, F, d)), np.zeros((E, F, d)), np.zeros((E, d, F))
     db1, db2, dWr = np.zeros((E, F)), np.zeros((E, d)), np.zeros((E, d))
-    points = {k: [] for k in ("h", "y", "dy", "a1", "a3", "da1", "da3")}
+    points = {k: [] for k in ("h", "dy", "a1", "a3", "da1", "da3")}
     for t in range(T):
         X, D = f64(x[t]), f64(dout[t])
         lg = f64(base["logits"][t])                      # fp32 router logits of the forward
@@ -243,8 +243,7 @@ def test_backward_bf16_rounding_points_worked_by_hand(act):
             a1 = a1 + f64(b1[e])
             hv = gelu(a1)
         h = bfv(hv)
-        yv = W2 @ h + (f64(b2[e]) if act != wl.SWIGLU else 0.0)
-        y = bfv(yv)
+        y = W2 @ h + (f64(b2[e]) if act != wl.SWIGLU else 0.0)
         dyv = gate * D
         dy = bfv(dyv)
         dh = W2.T @ dy
@@ -260,9 +259,9 @@ def test_backward_bf16_rounding_points_worked_by_hand(act):
         else:
             da1v = dh * dgelu(a1s)
         da1 = bfv(da1v)
-        for k_, v in (("h", hv), ("y", yv), ("dy", dyv), ("a1", a1), ("da1", da1v)):
+        for k_, v in (("h", hv), ("dy", dyv), ("a1", a1), ("da1", da1v)):
             points[k_].append(v)
-        dgate = float(D @ y)                             # the gate reads the stored y
+        dgate = float(D @ y)
         assert gr["dgate"][t, 0] == pytest.approx(dgate, rel=1e-12, abs=1e-15)
         dl = -p * p[e] * dgate                           # raw softmax: dl_c = p_c (dg [c = e] - p_e dg)
         dl[e] += p[e] * dgate
