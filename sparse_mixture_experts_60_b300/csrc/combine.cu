@@ -114,6 +114,92 @@ __global__ void __launch_bounds__(256) combine_kernel(int64_t T, int d, int k, c
     }
 }
 
+// The combine of prepared rows (CombinePrep) for k = KC in {1, 2, 4, 8},
+// bf16 layers: warp per token, each lane H 8-column chunks per step (two for
+// k <= 2, columns c and c + 256; one for larger k, to bound the registers)
+// with every row load of the step issued before the first add; out = sum_j y[inv_j] (j ascending) + z, + x only if no slot of
+// the token was kept, as combine_kernel<true, true>.
+template <int KC, int H = (KC <= 2 ? 2 : 1)>
+__global__ void __launch_bounds__(256) combine_pre_kernel(int64_t T, int d, const float *__restrict__ y,
+                                                          const int32_t *__restrict__ inv,
+                                                          const float *__restrict__ z, const bf16 *__restrict__ x,
+                                                          bf16 *__restrict__ out) {
+    PDL_ENTER();
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int my_r = lane < KC ? __ldg(inv + t * KC + lane) : -1;
+    int rows[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) rows[j] = __shfl_sync(kFull, my_r, j);
+    if (__any_sync(kFull, lane < KC && my_r >= 0)) x = nullptr;
+    const int nchunk = d / 8;
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * H) {
+        float4 u[KC][H][2];
+#pragma unroll
+        for (int j = 0; j < KC; ++j)
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const int c = c0 + 32 * h;
+                const bool ok = rows[j] >= 0 && c < nchunk;
+                const float4 *src = reinterpret_cast<const float4 *>(y + (int64_t)(ok ? rows[j] : 0) * d) + 2 * c;
+                u[j][h][0] = ok ? __ldg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+                u[j][h][1] = ok ? __ldg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        float4 zz[H][2];
+        uint4 xx[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const int c = c0 + 32 * h;
+            const bool ok = c < nchunk;
+            zz[h][0] = zz[h][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            xx[h] = make_uint4(0, 0, 0, 0);
+            if (ok && z) {
+                zz[h][0] = __ldg(reinterpret_cast<const float4 *>(z + t * d) + 2 * c);
+                zz[h][1] = __ldg(reinterpret_cast<const float4 *>(z + t * d) + 2 * c + 1);
+            }
+            if (ok && x) xx[h] = __ldg(reinterpret_cast<const uint4 *>(x + t * d) + c);
+        }
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const int c = c0 + 32 * h;
+            if (c >= nchunk) continue;
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+                if (rows[j] < 0) continue;
+                const float v[8] = {u[j][h][0].x, u[j][h][0].y, u[j][h][0].z, u[j][h][0].w,
+                                    u[j][h][1].x, u[j][h][1].y, u[j][h][1].z, u[j][h][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += v[i];
+            }
+            if (z) {
+                const float v[8] = {zz[h][0].x, zz[h][0].y, zz[h][0].z, zz[h][0].w,
+                                    zz[h][1].x, zz[h][1].y, zz[h][1].z, zz[h][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += v[i];
+            }
+            if (x) {
+                const uint32_t w[4] = {xx[h].x, xx[h].y, xx[h].z, xx[h].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] += __uint_as_float(w[q] << 16);
+                    acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+                o[q] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            reinterpret_cast<uint4 *>(out + t * d)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 // Combine for more than kMaxTopK slots per token (expert-choice routing on
 // many experts).  Warp per token: the token's kept (row, gate) pairs are
 // first compacted into a per-warp shared list in slot order (ballots over 32
@@ -345,6 +431,12 @@ cudaError_t launch_combine_prepped(int64_t T, int d, int k, int dtype, const flo
                                    const float *shared_out, const void *x_res, void *out, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (k > kMaxTopK) return cudaErrorInvalidValue;
+    if (dtype == 1 && (k == 1 || k == 2 || k == 4 || k == 8)) {
+        auto kern = k == 1 ? combine_pre_kernel<1>
+                           : (k == 2 ? combine_pre_kernel<2> : (k == 4 ? combine_pre_kernel<4> : combine_pre_kernel<8>));
+        return launch_pdl(kern, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, T, d, y_perm, inv, shared_out,
+                          static_cast<const bf16 *>(x_res), static_cast<bf16 *>(out));
+    }
     auto kern = dtype == 1 ? combine_kernel<true, true> : combine_kernel<false, true>;
     return launch_pdl(kern, dim3((unsigned)ceil_div(T, 8)), dim3(256), 0, s, T, d, k, y_perm, inv,
                       static_cast<const float *>(nullptr), shared_out, x_res, out);

@@ -147,18 +147,22 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;                 // one 128-byte swizzle atom of bf16
 constexpr int UMMA_K = 16;
-constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant (default)
 constexpr int kThreads = 64 + 32 * kEpiWarps;       // producer, MMA, epilogue
+// The plain bf16-output kernel of GELU / ReLU layers takes 16 epilogue
+// warps (four per quadrant): at d_model 1024 its activation math, not the
+// tensor cores, bounds a tile.
+constexpr int kEpiWarpsWide = 16;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;  // teardown waits: 2 s, whatever the wait limit
 
-template <int BN>
+template <int BN, int EW = kEpiWarps>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : (BN >= 64 ? 8 : 10));
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr int EPI_BYTES = kEpiWarps * 32 * 64;   // per epilogue warp: 32 rows x 64 B
+    static constexpr int EPI_BYTES = EW * 32 * 64;   // per epilogue warp: 32 rows x 64 B
     static constexpr int BAR_BYTES = 256;
     static size_t smem_bytes(int G) {
         return 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
@@ -528,16 +532,16 @@ constexpr int kEpiBwdGated = 100;   // SwiGLU: da1 = dh a3 silu'(a1), da3 = dh s
 constexpr int kEpiBwdAct = 101;     // GELU / ReLU: da = dh act'(a)
 
 // Epilogue of one accumulator tile for one warp: rows row_base .. +31 (the
-// warp's TMEM lane quadrant q), alternate 32-column chunks starting at
-// 32 * half.  `out` is this tile's output base (the group's, for K-grouped
+// warp's TMEM lane quadrant q), every PARTS-th 32-column chunk starting at
+// 32 * part (PARTS warps share a quadrant).  `out` is this tile's output base (the group's, for K-grouped
 // problems); zero_acc: the tile had no K blocks, so its result is zero.
 // Shared by the single-CTA and the CTA-pair kernels.
 //   forward:  [bias], [pre-activations stored], activation or SwiGLU gating
 //   kEpiBwdGated / kEpiBwdAct: the activation backward from the stored
 //             pre-activations (args.pre), dh being the accumulator.
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0>
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, int PARTS = 2>
 __device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, void *out, int row_base,
-                                              uint32_t tbase, int half, int lane, uint8_t *stg, bool zero_acc) {
+                                              uint32_t tbase, int part, int lane, uint8_t *stg, bool zero_acc) {
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
     const int row = row_base + lane;
     // combine preparation (fp32 output of a plain GEMM): this row's gate,
@@ -560,7 +564,7 @@ __device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, 
         }
     }
 #pragma unroll 1
-    for (int c = 32 * half; c < BN_OUT; c += 64) {
+    for (int c = 32 * part; c < BN_OUT; c += 32 * PARTS) {
         const int col = tl.n0 + c;
         float v[32];
         if (zero_acc) {
@@ -706,11 +710,11 @@ __device__ __forceinline__ void route_epilogue(const Args &args, const Tile &tl,
 // row-major token tensors (A [rows, M], B [rows, N]); the group's rows are
 // its K range in blocks of 64 from seg[g], and a fixer warp zeroes the K
 // rows of a group's last block that belong to the next group.
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false>
-__global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false, int EW = kEpiWarps>
+__global__ void __launch_bounds__(64 + 32 * EW + (KG_MN ? 32 : 0), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const Args args) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, EW>;
     constexpr int STAGES = C::STAGES;
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
     constexpr uint32_t IDESC = IDesc<BM, BN, B_MN || KG_MN, KG_MN>::value;
@@ -747,7 +751,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 32 * kEpiWarps);
+            mbar_init(&tempty[i], 32 * EW);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -912,7 +916,7 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
-    } else if (KG_MN && warp == 2 + kEpiWarps) {
+    } else if (KG_MN && warp == 2 + EW) {
         // ------------------------------------------------ K-tail fixer
         // A group's last K block may reach into the next group's rows: those
         // K rows of A are zeroed (whole 128-byte lines of each 64-column box;
@@ -958,14 +962,14 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
                 }
             }
         }
-    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+    } else if (warp >= 2 && warp < 2 + EW) {
         // ------------------------------------------------ epilogue
-        // Thread = accumulator row.  Warps w and w+4 share a TMEM lane
-        // quadrant and take alternate 32-column chunks.  Output leaves through
-        // a per-warp 2 KB shared-memory buffer (store_chunk): row-contiguous
-        // 64-byte segments of bf16, whole 128-byte lines of fp32.
+        // Thread = accumulator row.  Warps w, w+4, ... share a TMEM lane
+        // quadrant and take every (EW/4)-th 32-column chunk.  Output leaves
+        // through a per-warp 2 KB shared-memory buffer (store_chunk):
+        // row-contiguous 64-byte segments of bf16, whole 128-byte lines of fp32.
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = (warp - 2) >> 2;       // which alternate chunks
+        const int half = (warp - 2) >> 2;       // which chunks: half, half + EW/4, ...
         uint8_t *stg = sEpi + (warp - 2) * (32 * 64);
         int acc = 0;
         uint32_t aph = 0;
@@ -990,7 +994,8 @@ __global__ void __launch_bounds__(KG_MN ? kThreads + 32 : kThreads, 1)
                           tl.g * args.out_group_stride * (int64_t)(OUT_F32 ? 4 : 2);
                     zero_acc = seg_s[tl.g + 1] == seg_s[tl.g];
                 }
-                epilogue_tile<BN, GATED, OUT_F32, EPI>(args, tl, out, row_base, tbase, half, lane, stg, zero_acc);
+                epilogue_tile<BN, GATED, OUT_F32, EPI, EW / 4>(args, tl, out, row_base, tbase, half, lane, stg,
+                                                                 zero_acc);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -1354,9 +1359,9 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false>
+template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false, int EW = kEpiWarps>
 cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, EW>;
     constexpr int BN_B = GATED ? BN / 2 : BN;   // rows per TMA box of B
     CUtensorMap ta, tb, tb2;
     if (KG_MN) {
@@ -1422,10 +1427,10 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     // CTA's allocation
     const size_t smem = (B_MN || KG_MN) ? (size_t)232448 : C::smem_bytes(a.G);
     if ((B_MN || KG_MN) && C::smem_bytes(a.G) > smem) return cudaErrorInvalidValue;
-    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI, B_MN, KG_MN>;
+    auto kern = grouped_gemm_kernel<BN, GATED, OUT_F32, EPI, B_MN, KG_MN, EW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(num_sms()), dim3(KG_MN ? kThreads + 32 : kThreads), smem, s, ta, tb, tb2, a);
+    return launch_pdl(kern, dim3(num_sms()), dim3(64 + 32 * EW + (KG_MN ? 32 : 0)), smem, s, ta, tb, tb2, a);
 }
 
 template <int BN, bool GATED, bool OUT_F32>
@@ -1559,6 +1564,10 @@ cudaError_t launch_grouped_gemm(const GemmProblem &p, cudaStream_t s) {
         return launch_t<256, false, true>(p, s);
     }
     if (use_pair(p)) return launch_pair_t<256, false, false>(p, s);
+    // GELU / ReLU first GEMM: 16 epilogue warps while their staging and the
+    // segment tables fit in shared memory (up to a few hundred experts)
+    if (p.act != 0 && Cfg<256, kEpiWarpsWide>::smem_bytes(p.seg ? p.G : 1) <= (size_t)232448)
+        return launch_t<256, false, false, 0, false, false, kEpiWarpsWide>(p, s);
     return launch_t<256, false, false>(p, s);
 }
 
