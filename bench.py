@@ -218,10 +218,13 @@ def launches_per_step(w, routing="topk"):
         n = 1                                 # hash routing
     else:
         n = 1 if w.E <= 32 else 2             # fused router (GEMM epilogue / CUDA-core kernel), else logits + routing
+    nchunk = -(-S // 2048)                    # the two-launch dispatch's largest chunk
     if S == 0:
         n += 1
     elif S <= 8192 and w.E <= 256:
         n += 2                                # one-CTA dispatch, row copy
+    elif nchunk * w.E <= 8192:
+        n += 2                                # chunk ranks, row copy with the chunk bases
     else:
         n += 4                                # histogram, scan, rank, row copy
     n += 2 + (2 if w.num_shared else 0)       # expert GEMMs (+ shared expert)
@@ -462,6 +465,8 @@ def run_ours(args, w, rank, world, local):
     torch.cuda.set_device(local)
     if args.gemm_pair != "auto":
         moe.moe_set_option(moe.MOE_OPT_GEMM_PAIR, int(args.gemm_pair))
+    if args.gemm_band != -1:
+        moe.moe_set_option(moe.MOE_OPT_GEMM_BAND, args.gemm_band)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -798,6 +803,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--gemm-pair", default="auto", choices=["auto", "0", "1"],
                     help="expert GEMM kernel: chosen by shape (auto), one-CTA (0) or CTA-pair (1) tiles")
+    ap.add_argument("--gemm-band", type=int, default=-1,
+                    help="expert GEMM raster band in M tiles: -1 chosen by shape, 0 whole experts, n > 0 n tiles")
     ap.add_argument("--extra-steps", type=int, default=20,
                     help="timed steps of each of the other workloads added to the headline (Mixtral) line; 0: none")
     ap.add_argument("--train", action="store_true",

@@ -505,10 +505,17 @@ moe_status_t moe_check_device_error(int32_t *code);
  *                          the outputs of that call are then undefined.
  *                          A limit far below a kernel's run time (a few
  *                          microseconds) forces this path on purpose.
+ *   MOE_OPT_GEMM_BAND      -1 (default): an expert GEMM whose experts' rows
+ *                          do not fit in L2 walks each expert's tiles in
+ *                          bands of M tiles sized from the SM count and the
+ *                          operand shapes (N outer, M inner within a band),
+ *                          others M fastest over the whole expert; 0: always
+ *                          M fastest; n > 0: bands of n M tiles.
  * moe_set_option returns MOE_ERR_INVALID_ARG for an unknown option or a
- * value out of range (PDL 0/1, GEMM_PAIR -1/0/1, WAIT_LIMIT_NS >= 0).
+ * value out of range (PDL 0/1, GEMM_PAIR -1/0/1, WAIT_LIMIT_NS >= 0,
+ * GEMM_BAND -1..65536).
  */
-enum { MOE_OPT_PDL = 0, MOE_OPT_GEMM_PAIR = 1, MOE_OPT_WAIT_LIMIT_NS = 2 };
+enum { MOE_OPT_PDL = 0, MOE_OPT_GEMM_PAIR = 1, MOE_OPT_WAIT_LIMIT_NS = 2, MOE_OPT_GEMM_BAND = 3 };
 moe_status_t moe_set_option(int32_t option, int64_t value);
 /* Current value of an option (host output). */
 moe_status_t moe_get_option(int32_t option, int64_t *value);

@@ -16,7 +16,7 @@ from __future__ import annotations
 import ctypes as C
 from typing import Dict, Optional
 
-from ._lib import (MOE_OPT_GEMM_PAIR, MOE_OPT_PDL, MOE_OPT_WAIT_LIMIT_NS,  # noqa: F401
+from ._lib import (MOE_OPT_GEMM_BAND, MOE_OPT_GEMM_PAIR, MOE_OPT_PDL, MOE_OPT_WAIT_LIMIT_NS,  # noqa: F401
                    MOE_BWD_STAGE_EVENTS, MOE_STAGE_EVENTS, MOE_WS_BACKWARD, MoEBackwardOpts, MOE_WS_EXPERT_CHOICE, MOE_WS_EXPERT_FFN,  # noqa: F401
                    MOE_WS_FORWARD, MOE_WS_PERMUTE, MOE_WS_ROUTE, MOE_WS_SHARED_FFN, MoEConfig, MoEECIO, MoEGrads,
                    MoESaved, MoEError, MoEForwardIO, MoEStats, MoEWeights, check,
@@ -249,7 +249,7 @@ def moe_check_device_error() -> int:
 
 
 def moe_set_option(option: int, value: int) -> None:
-    """Process-wide switch (MOE_OPT_PDL, MOE_OPT_GEMM_PAIR, MOE_OPT_WAIT_LIMIT_NS)."""
+    """Process-wide switch (MOE_OPT_PDL, MOE_OPT_GEMM_PAIR, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_GEMM_BAND)."""
     check(lib().moe_set_option(int(option), int(value)))
 
 

@@ -16,7 +16,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_BAD_ALIGNMENT", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
                 6: "MOE_ERR_DEVICE_TIMEOUT"}
-MOE_OPT_PDL, MOE_OPT_GEMM_PAIR, MOE_OPT_WAIT_LIMIT_NS = 0, 1, 2
+MOE_OPT_PDL, MOE_OPT_GEMM_PAIR, MOE_OPT_WAIT_LIMIT_NS, MOE_OPT_GEMM_BAND = 0, 1, 2, 3
 (MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_SHARED_FFN, MOE_WS_EXPERT_CHOICE,
  MOE_WS_BACKWARD) = range(7)
 

@@ -39,6 +39,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <mutex>
 #include <math.h>
@@ -97,11 +98,13 @@ namespace {
 std::atomic<int64_t> g_opt_pdl{1};
 std::atomic<int64_t> g_opt_gemm_pair{-1};
 std::atomic<int64_t> g_opt_wait_ns{2000000000ll};
+std::atomic<int64_t> g_opt_gemm_band{-1};
 }  // namespace
 
 bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
 int gemm_pair_option() { return (int)g_opt_gemm_pair.load(std::memory_order_relaxed); }
 uint64_t wait_limit_ns() { return (uint64_t)g_opt_wait_ns.load(std::memory_order_relaxed); }
+int64_t gemm_band_option() { return g_opt_gemm_band.load(std::memory_order_relaxed); }
 
 bool set_option(int option, int64_t value) {
     switch (option) {
@@ -117,6 +120,10 @@ bool set_option(int option, int64_t value) {
             if (value < 0) return false;
             g_opt_wait_ns.store(value);
             return true;
+        case 3:   // MOE_OPT_GEMM_BAND
+            if (value < -1 || value > 65536) return false;
+            g_opt_gemm_band.store(value);
+            return true;
         default:
             return false;
     }
@@ -126,6 +133,7 @@ bool get_option(int option, int64_t *value) {
         case 0: *value = g_opt_pdl.load(); return true;
         case 1: *value = g_opt_gemm_pair.load(); return true;
         case 2: *value = g_opt_wait_ns.load(); return true;
+        case 3: *value = g_opt_gemm_band.load(); return true;
         default: return false;
     }
 }
@@ -349,14 +357,19 @@ struct Args {
     // second expert GEMM of the layer forward: rows scaled by their gate,
     // plus x for a token's first kept slot (GemmProblem::comb)
     CombinePrep comb;
+    int band;              // M-grouped: M tiles per raster band (0: whole group)
 };
 
 struct Tile {
     int g, row0, seg_end, n0;
 };
 
+// Tile `tile` of an M-grouped problem: group by binary search over the
+// tile prefix, then inside the group bands of `band` M tiles (0: one band
+// of the whole group), N block outer and M tile inner within a band, so
+// that the tiles in flight share a band's A rows and B columns in L2.
 __device__ __forceinline__ Tile decode_tile_m(int tile, const int *seg_s, const int *pre_s, int G, int bn_out,
-                                              int tile_m) {
+                                              int tile_m, int band = 0) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -366,7 +379,19 @@ __device__ __forceinline__ Tile decode_tile_m(int tile, const int *seg_s, const 
     const int rows = seg_s[lo + 1] - seg_s[lo];
     const int mt = (rows + tile_m - 1) / tile_m;
     const int local = tile - pre_s[lo];
-    const int nb = local / mt, mb = local - nb * mt;
+    int nb, mb;
+    if (band <= 0 || band >= mt) {
+        nb = local / mt;
+        mb = local - nb * mt;
+    } else {
+        const int nt = (pre_s[lo + 1] - pre_s[lo]) / mt;
+        const int per_band = band * nt;
+        const int b = local / per_band;
+        const int in_rows = min(band, mt - b * band);
+        const int in = local - b * per_band;
+        nb = in / in_rows;
+        mb = b * band + (in - nb * in_rows);
+    }
     Tile t;
     t.g = lo;
     t.row0 = seg_s[lo] + mb * tile_m;
@@ -374,8 +399,9 @@ __device__ __forceinline__ Tile decode_tile_m(int tile, const int *seg_s, const 
     t.n0 = nb * bn_out;
     return t;
 }
-__device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const int *pre_s, int G, int bn_out) {
-    return decode_tile_m(tile, seg_s, pre_s, G, bn_out, BM);
+__device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const int *pre_s, int G, int bn_out,
+                                            int band = 0) {
+    return decode_tile_m(tile, seg_s, pre_s, G, bn_out, BM, band);
 }
 
 // Gaussian CDF for the GELU epilogues, from the rational approximation of
@@ -492,7 +518,7 @@ __device__ __forceinline__ float gelu_erf_grad(float a) {
 // K range; tiles group-major, then N block, then M block).
 __device__ __forceinline__ Tile tile_of(const Args &args, int tile, const int *seg_s, const int *pre_s, int G,
                                         int bn_out, int kg_tiles) {
-    if (!args.kgroup) return decode_tile(tile, seg_s, pre_s, G, bn_out);
+    if (!args.kgroup) return decode_tile(tile, seg_s, pre_s, G, bn_out, args.band);
     const int mt = (args.M + BM - 1) / BM;
     Tile t;
     t.g = tile / kg_tiles;
@@ -843,7 +869,14 @@ __global__ void __launch_bounds__(64 + 32 * EW + (KG_MN ? 32 : 0), 1)
                     }
                     continue;
                 }
-                tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * BK, tl.row0);
+                // the router GEMM (one tile per CTA, all of them streaming at
+                // once) starts every tile at its own K block and wraps around,
+                // so that concurrent tiles read different column ranges of
+                // their rows instead of the same one
+                const int kbl = (EPI > 0 && EPI <= 32)
+                                    ? kr.kb0 + (kb - kr.kb0 + tile * 13) % (kr.kb1 - kr.kb0)
+                                    : kb;
+                tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kbl * BK, tl.row0);
                 if (B_MN) {
                     // B[n][k] = W[g rows + k][n]: 64 x 64 boxes along N
                     const bool lo = kb * BK < args.k_split;
@@ -856,7 +889,7 @@ __global__ void __launch_bounds__(64 + 32 * EW + (KG_MN ? 32 : 0), 1)
                     tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * BK, brow);
                     tma_load_2d(sB + stage * C::B_BYTES + (BN / 2) * BK * 2, &tmB2, &full[stage], kb * BK, brow);
                 } else {
-                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * BK, brow);
+                    tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kbl * BK, brow);
                 }
                 ++issued;
                 if (++stage == STAGES) {
@@ -1229,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t ph = 0;
         for (int tile = cid; tile < total; tile += ncl) {
-            const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M);
+            const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M, args.band);
             const int arow = tl.row0 + BM * (int)rank;
             const int brow = GATED ? tl.g * args.b_group_rows + tl.n0
                                    : tl.g * args.b_group_rows + tl.n0 + (BN / 2) * (int)rank;
@@ -1293,7 +1326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = cid; tile < total; tile += ncl) {
-            const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M);
+            const Tile tl = decode_tile_m(tile, seg_s, pre_s, G, BN_OUT, TILE_M, args.band);
             if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tfull[acc], aph, abort_flag, args.err, args.wait_ns))) break;
             tc_fence_after();
             const int row_base = tl.row0 + BM * (int)rank + q * 32;
@@ -1359,6 +1392,23 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, 
     return r == CUDA_SUCCESS;
 }
 
+// Raster band of an M-grouped problem: W tiles run at once, each reading an
+// A strip (tile_m rows) and a B strip (b_rows rows) over the whole K.
+// While a group's A rows fit in a third of L2 (42 MB), M-fastest over the
+// whole group reads every operand once (measured, Mixtral first GEMM: 2.2
+// GB read with whole groups, 4.0 GB with bands).  Above that, a band of m
+// M tiles puts m A strips and W/m B strips in flight, least bytes at
+// m = sqrt(W * b_rows / tile_m) (Mixtral second GEMM: 4.6 GB read instead
+// of 5.2).  The MOE_OPT_GEMM_BAND option overrides the choice.
+int raster_band(const GemmProblem &p, int W, int tile_m, int b_rows) {
+    const int64_t opt = gemm_band_option();
+    if (opt >= 0) return (int)opt;
+    const int groups = p.seg ? p.G : 1;
+    const int64_t group_a_bytes = p.a_rows / std::max(1, groups) * (int64_t)p.K * 2;
+    if (group_a_bytes <= (int64_t)42 << 20) return 0;
+    return std::max(1, (int)lround(std::sqrt((double)W * b_rows / tile_m)));
+}
+
 template <int BN, bool GATED, bool OUT_F32, int EPI = 0, bool B_MN = false, bool KG_MN = false, int EW = kEpiWarps>
 cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     using C = Cfg<BN, EW>;
@@ -1405,6 +1455,7 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     if (!a.err) return cudaErrorUnknown;
     a.wait_ns = wait_limit_ns();
     a.comb = p.comb;
+    a.band = (p.kgroup || p.route) ? 0 : raster_band(p, num_sms(), BM, BN);
     a.route = p.route ? *p.route : RouteEpilogue{};
     a.pre = p.pre;
     a.ld_pre = p.ld_pre;
@@ -1462,6 +1513,9 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     if (!a.err) return cudaErrorUnknown;
     a.wait_ns = wait_limit_ns();
     a.comb = p.comb;
+    // (bands measured no better for CTA pairs: Mixtral second GEMM 6.7 GB
+    // read with bands of 9 pair tiles, 6.4 GB M-fastest)
+    a.band = gemm_band_option() > 0 ? (int)gemm_band_option() : 0;
     const size_t smem = C::smem_bytes(a.G);
     auto kern = grouped_gemm_pair_kernel<BN, GATED, OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

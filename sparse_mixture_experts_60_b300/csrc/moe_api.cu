@@ -2,6 +2,7 @@
 // the launch sequence.  Every step of the layer runs in this library's own
 // kernels; the host code only checks arguments, carves the caller's
 // workspace, encodes TMA descriptors and launches on the caller's stream.
+#include <algorithm>
 #include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
@@ -84,9 +85,12 @@ bool fused_router(const moe_config_t *c) {
 size_t route_ws(const moe_config_t *c) {
     return 2 * align256((size_t)route_blocks(c) * c->num_experts * 4) + align256((size_t)route_blocks(c) * 4);
 }
+// chunk histogram and base tables of the chunked dispatch (the two-launch
+// dispatch keeps its chunk table, at most kTwoPassTable entries, in the
+// first), and the slots' ranks within their chunk
 size_t permute_ws(const moe_config_t *c) {
-    return 2 * align256((size_t)perm_chunks(c) * c->num_experts * 4) +
-           align256((size_t)c->num_tokens * c->top_k * 4);
+    const size_t tab = std::max<size_t>((size_t)perm_chunks(c) * c->num_experts, (size_t)kTwoPassTable);
+    return 2 * align256(tab * 4) + align256((size_t)c->num_tokens * c->top_k * 4);
 }
 size_t ffn_ws(const moe_config_t *c) {
     return align256((size_t)c->num_tokens * c->top_k * c->d_ff * elem_bytes(c));
@@ -353,8 +357,9 @@ moe_status_t permute_impl(const moe_config_t *c, const void *x, const int32_t *t
     p.perm = perm;
     p.inv = inv;
     p.x_perm = x_perm;
-    p.hist = cv.take<int32_t>((size_t)nch * c->num_experts * 4);
-    p.base = cv.take<int32_t>((size_t)nch * c->num_experts * 4);
+    const size_t tab = std::max<size_t>((size_t)nch * c->num_experts, (size_t)kTwoPassTable);
+    p.hist = cv.take<int32_t>(tab * 4);
+    p.base = cv.take<int32_t>(tab * 4);
     p.lrank = cv.take<int32_t>((size_t)c->num_tokens * c->top_k * 4);
     return cuda_status(launch_permute(p, s), "moe_permute launch");
 }

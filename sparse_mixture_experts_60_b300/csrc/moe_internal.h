@@ -128,9 +128,9 @@ struct PermuteParams {
 // kernels, which spread the integer work over many SMs.
 constexpr int64_t kSmallSlots = 8192;
 constexpr int kSmallExperts = 256;
-// Layers whose chunk table (chunks of kPermChunk slots x experts) has at
-// most this many entries dispatch in two launches: per-chunk histograms and
-// ranks, then the row copy, each of whose CTAs rebuilds the chunk bases and
+// Layers whose chunk table (chunks of 512, 1024 or 2048 slots x experts)
+// has at most this many entries dispatch in two launches: per-chunk histograms and ranks,
+// then the row copy, each of whose CTAs rebuilds the chunk bases and
 // offsets from the table in shared memory; larger tables use the separate
 // histogram, scan and rank kernels.
 constexpr int64_t kTwoPassTable = 8192;

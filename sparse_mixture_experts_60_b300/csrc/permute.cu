@@ -36,6 +36,9 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kPermThreads = 256;
 constexpr int kWarpSpan = kPermChunk / (kPermThreads / 32);  // 256 priorities per warp
+// two-launch dispatch: chunks of 512, 1024 or 2048 priorities (the
+// smallest whose table fits), an eighth of a chunk per warp
+constexpr int kLocalChunkMin = 512;
 
 __device__ __forceinline__ int slot_expert(const int32_t *idx, int64_t p, int64_t T, int k, int E,
                                            int64_t S, int64_t *slot_out, int32_t *err) {
@@ -171,10 +174,11 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *
 }
 
 // Dispatch in two launches (layers with nchunk * E <= kTwoPassTable):
-//   perm_local_kernel      chunk c (priorities c*kPermChunk ..): the chunk's
+//   perm_local_kernel      chunk c (priorities c*lchunk .., lchunk = 512,
+//                          1024 or 2048, the smallest whose table fits): the chunk's
 //                          expert histogram -> hist[c][E], and every slot's
 //                          rank among the chunk's slots of its expert ->
-//                          lrank[slot] (8 warps x 256 priorities, warp bases
+//                          lrank[slot] (8 warps x lchunk/8 priorities, warp bases
 //                          from a scan of the warp histograms, match-any
 //                          ranks 32 slots at a time)
 //   perm_copy_rank_kernel  every CTA first turns the small hist table into
@@ -184,7 +188,8 @@ __global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *
 //                          the slot][e] + lrank[slot], the capacity clamp,
 //                          perm / inv, and the row copy of x.
 __global__ void __launch_bounds__(kPermThreads) perm_local_kernel(const int32_t *idx, int64_t T, int k, int E,
-                                                                  int32_t *hist, int32_t *lrank, int32_t *err) {
+                                                                  int lchunk, int32_t *hist, int32_t *lrank,
+                                                                  int32_t *err) {
     PDL_ENTER();
     extern __shared__ int wh[];          // [8][E] warp histograms, then warp running bases
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -192,9 +197,10 @@ __global__ void __launch_bounds__(kPermThreads) perm_local_kernel(const int32_t 
     for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wh[i] = 0;
     __syncthreads();
     const int64_t S = T * k;
-    const int64_t p0 = (int64_t)blockIdx.x * kPermChunk + (int64_t)warp * kWarpSpan;
+    const int span = lchunk / nw;
+    const int64_t p0 = (int64_t)blockIdx.x * lchunk + (int64_t)warp * span;
     int *my = wh + warp * E;
-    for (int g = 0; g < kWarpSpan; g += 32) {
+    for (int g = 0; g < span; g += 32) {
         int64_t sl;
         const int e = slot_expert(idx, p0 + g + lane, T, k, E, S, &sl, err);
         if (e >= 0) atomicAdd(&my[e], 1);
@@ -211,7 +217,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_local_kernel(const int32_t 
     }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
-    for (int g = 0; g < kWarpSpan; g += 32) {
+    for (int g = 0; g < span; g += 32) {
         int64_t sl = -1;
         const int e = slot_expert(idx, p0 + g + lane, T, k, E, S, &sl, nullptr);
         const unsigned peers = __match_any_sync(kFull, e);
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_local_kernel(const int32_t 
 }
 
 __global__ void __launch_bounds__(256) perm_copy_rank_kernel(const uint4 *x, int64_t T, int k, int64_t nvec,
-                                                             const int32_t *idx, int E, int64_t cap,
+                                                             const int32_t *idx, int E, int64_t cap, int lchunk,
                                                              int64_t nchunk, const int32_t *hist,
                                                              const int32_t *lrank, int32_t *counts, int32_t *kept,
                                                              int32_t *offsets, int32_t *perm, int32_t *inv,
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(256) perm_copy_rank_kernel(const uint4 *x, int
         const int e = __ldg(idx + sl);
         if (e >= 0 && e < E) {
             const int64_t pr = (int64_t)lane * T + t;           // priority of slot (t, lane)
-            const int rank = tab[(pr / kPermChunk) * E + e] + __ldg(lrank + sl);
+            const int rank = tab[(pr / lchunk) * E + e] + __ldg(lrank + sl);
             if ((int64_t)rank < cap) {
                 my_row = off_s[e] + rank;
                 perm[my_row] = (int32_t)sl;
@@ -531,22 +537,26 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t s) {
         return launch_pdl(perm_copy_kernel, copy_grid, dim3(256), 0, s, static_cast<const uint4 *>(p.x), p.T, p.k,
                           nvec, p.inv, p.offsets, p.E, p.perm, S, static_cast<uint4 *>(p.x_perm));
     }
-    if (!p.chunked && nchunk > 0 && nchunk * p.E <= kTwoPassTable) {
+    int lchunk = kLocalChunkMin;
+    while (lchunk < kPermChunk && ceil_div(S, lchunk) * p.E > kTwoPassTable) lchunk *= 2;
+    const int64_t nlocal = ceil_div(S, lchunk);
+    if (!p.chunked && nlocal > 0 && nlocal * p.E <= kTwoPassTable) {
         const size_t smem1 = (size_t)(kPermThreads / 32) * p.E * sizeof(int);
         if (smem1 > 48 * 1024) {
             e = cudaFuncSetAttribute(perm_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
             if (e != cudaSuccess) return e;
         }
-        e = launch_pdl(perm_local_kernel, dim3((unsigned)nchunk), dim3(kPermThreads), smem1, s, p.topk_idx, p.T,
-                       p.k, p.E, p.hist, p.lrank, err);
+        e = launch_pdl(perm_local_kernel, dim3((unsigned)nlocal), dim3(kPermThreads), smem1, s, p.topk_idx, p.T,
+                       p.k, p.E, lchunk, p.hist, p.lrank, err);
         if (e != cudaSuccess) return e;
-        const size_t smem2 = (size_t)(nchunk * p.E + p.E + 1) * sizeof(int);
+        const size_t smem2 = (size_t)(nlocal * p.E + p.E + 1) * sizeof(int);
         if (smem2 > 48 * 1024) {
             e = cudaFuncSetAttribute(perm_copy_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
             if (e != cudaSuccess) return e;
         }
         return launch_pdl(perm_copy_rank_kernel, copy_grid, dim3(256), smem2, s, static_cast<const uint4 *>(p.x), p.T,
-                          p.k, nvec, p.topk_idx, p.E, p.cap, nchunk, p.hist, p.lrank, p.counts, p.kept, p.offsets,
+                          p.k, nvec, p.topk_idx, p.E, p.cap, lchunk, nlocal, p.hist, p.lrank, p.counts, p.kept,
+                          p.offsets,
                           p.perm, p.inv, static_cast<uint4 *>(p.x_perm));
     }
     if (nchunk > 0) {

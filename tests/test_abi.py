@@ -77,7 +77,7 @@ def _ws_expect(w):
     nblk = -(-T // 32)
     nch = -(-S // 2048)
     route = 2 * a(nblk * E * 4) + a(nblk * 4)
-    perm = 2 * a(nch * E * 4) + a(S * 4)
+    perm = 2 * a(max(nch * E, 8192) * 4) + a(S * 4)
     ffn = a(S * F * eb)
     shared = a(T * F * eb) if w.num_shared else 0
     fwd = route + perm + ffn + shared + a(S * d * eb) + a(S * d * 4) + (a(T * d * 4) if w.num_shared else 0)
@@ -220,6 +220,9 @@ def test_options_are_checked_on_host(L):
     assert moe.moe_get_option(moe.MOE_OPT_PDL) == 1
     assert moe.moe_get_option(moe.MOE_OPT_GEMM_PAIR) == -1
     assert moe.moe_get_option(moe.MOE_OPT_WAIT_LIMIT_NS) == 2_000_000_000
+    assert moe.moe_get_option(moe.MOE_OPT_GEMM_BAND) == -1
+    with pytest.raises(moe.MoEError, match="out of range"):
+        moe.moe_set_option(moe.MOE_OPT_GEMM_BAND, -2)
     with pytest.raises(moe.MoEError, match="out of range"):
         moe.moe_set_option(moe.MOE_OPT_WAIT_LIMIT_NS, -1)
     with pytest.raises(moe.MoEError, match="out of range"):

@@ -118,3 +118,19 @@ def test_train_line(name):
         {"dh_gemm": "tensor", "dx_gemm": "tensor", "dw2_gemm": "tensor", "dw13_gemm": "tensor"} if name == "mixtral"
         else {"dh_gemm": "tensor", "dx_gemm": "tensor", "dw2_gemm": "hbm", "dw13_gemm": "hbm"})
     assert line["gpu_launches"] == (bench.launches_per_step(w) + bench.bwd_launches(w)) * 30
+
+
+def test_launch_counts_follow_the_forward_sequence():
+    """Kernels of one moe_forward per workload, counted from its launch
+    sequence: router (one fused GEMM with the routing epilogue for bf16
+    E <= 32 or the fp32 CUDA-core router; logits GEMM + routing kernel for
+    wider routers), dispatch (one CTA for <= 8192 slots, else two launches
+    while a table of chunks (512 to 2048 slots) x experts fits in 8192
+    entries, else four), the two expert GEMMs (+ two for the shared expert), combine,
+    statistics."""
+    expect = {"tiny_fp32": 1 + 2 + 2 + 2, "quickstart_bf16": 1 + 2 + 2 + 2, "capacity_e128": 2 + 2 + 2 + 2,
+              "mixtral": 1 + 2 + 2 + 2, "deepseek_v3": 2 + 2 + 4 + 2}
+    for name, n in expect.items():
+        assert bench.launches_per_step(wl.WORKLOADS[name]) == n, name
+    big = wl.WORKLOADS["mixtral"].with_(T=150000, E=64)          # 147 2048-slot chunks x 64: four launches
+    assert bench.launches_per_step(big) == 2 + 4 + 2 + 2                 # router of 64 experts: two launches
