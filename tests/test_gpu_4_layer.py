@@ -1,6 +1,8 @@
 """Whole-layer parity on the GPU through moe_forward (the call the benchmark
 times): output, intermediates, statistics, the bias update, determinism and
 the empty batch."""
+import ctypes as C
+
 import numpy as np
 import pytest
 import torch
@@ -175,3 +177,62 @@ def test_host_batches_pipeline_matches_forward():
     assert torch.equal(outs[0], ref0)                 # step 4 used batch 0
     assert torch.equal(outs[1], ref1)                 # step 3 used batch 1
     np.testing.assert_array_equal(host(ref0), got["out"])
+
+
+def run_steps(w, inp):
+    """The layer as the separate calls of the C ABI, each with its own
+    workspace: moe_route -> moe_permute -> moe_expert_ffn (-> moe_shared_ffn)
+    -> moe_combine -> moe_stats (raw expert outputs, gates applied in the
+    combine)."""
+    cfg = moe.config_for(w)
+    T, E, k, d = w.T, w.E, w.k, w.d
+    S = T * k
+    W = weights(inp)
+    f32, i32 = dict(dtype=torch.float32, device="cuda"), dict(dtype=torch.int32, device="cuda")
+    ws = lambda which: torch.empty(max(moe.moe_workspace_size(cfg, which), 1), dtype=torch.uint8, device="cuda")
+    x = dev(inp["x"])
+    sb = dev(inp["sel_bias"]) if "sel_bias" in inp else None
+    o = dict(logits=torch.empty(T, E, **f32), topk_idx=torch.empty(T, k, **i32), topk_w=torch.empty(T, k, **f32),
+             lse=torch.empty(T, **f32), prob_mean=torch.empty(E, **f32), counts=torch.empty(E, **i32),
+             counts2=torch.empty(E, **i32), kept=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+             perm=torch.empty(S, **i32), inv=torch.empty(S, **i32), f=torch.empty(E, **f32))
+    moe.moe_route(cfg, x, W["w_router"], W.get("b_router"), sb, o["logits"], o["topk_idx"], o["topk_w"], o["lse"],
+                  o["prob_mean"], o["counts"], ws(moe.MOE_WS_ROUTE))
+    x_perm = torch.empty(S, d, dtype=x.dtype, device="cuda")
+    moe.moe_permute(cfg, x, o["topk_idx"], o["counts2"], o["kept"], o["offsets"], o["perm"], o["inv"], x_perm,
+                    ws(moe.MOE_WS_PERMUTE))
+    y = torch.empty(S, d, **f32)
+    moe.moe_expert_ffn(cfg, x_perm, o["offsets"], W["w1"], W.get("b1"), W.get("w3"), W["w2"], W.get("b2"), y,
+                       ws(moe.MOE_WS_EXPERT_FFN))
+    z = None
+    if w.num_shared:
+        z = torch.empty(T, d, **f32)
+        moe.moe_shared_ffn(cfg, x, W["shared_w1"], W.get("shared_w3"), W["shared_w2"], z, ws(moe.MOE_WS_SHARED_FFN))
+    out = torch.empty(T, d, dtype=x.dtype, device="cuda")
+    moe.moe_combine(cfg, y, o["inv"], o["topk_w"], z, x, out)
+    st = torch.empty(C.sizeof(moe.MoEStats), dtype=torch.uint8, device="cuda")
+    moe.moe_stats(cfg, o["counts2"], o["kept"], o["prob_mean"], o["lse"], o["f"], st)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == 0
+    got = {k2: host(v) for k2, v in o.items()}
+    got["out"] = host(out)
+    got["stats"] = moe.stats_from_buffer(st)
+    return got
+
+
+@pytest.mark.parametrize("name,T,ntok", [c for c in LAYER_CASES if c[0] != "tiny_fp32"] + [("tiny_fp32", 64, None)])
+def test_step_by_step_calls_match_oracle_and_forward(name, T, ntok):
+    """Every call of the boundary chained by hand gives the oracle's layer,
+    and the same routing, dispatch and statistics as moe_forward."""
+    w = wl.WORKLOADS[name].scaled(T)
+    inp = wl.make_inputs(w)
+    got = run_steps(w, inp)
+    np.testing.assert_array_equal(got["counts"], got["counts2"])     # router and dispatch agree
+    tokens = np.arange(T) if ntok is None else wl.sample_tokens(w, ntok)
+    check_layer(w, inp, got, tokens)
+    _, fwd = run_layer(w, inp)
+    for key in ("logits", "topk_idx", "topk_w", "lse", "counts", "kept", "offsets", "perm", "inv", "f"):
+        np.testing.assert_array_equal(got[key], fwd[key], err_msg=key)
+    assert got["stats"]["total_kept"] == fwd["stats"]["total_kept"]
+    # the two combines add the same terms in a different fp32 order
+    float_check(got["out"], fwd["out"], w, f"{name} steps vs forward")
