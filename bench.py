@@ -108,6 +108,13 @@ def hbm_bytes(w, kept_rows, routing="topk"):
     (expert outputs y and the shared expert's z in the layer dtype)."""
     eb = w.elem_bytes
     T, d, E, S = w.T, w.d, w.E, w.T * w.k
+    if routing == "hash":
+        # hash routing: token ids in, expert ids and gates out
+        route = T * 4 + S * 8
+        permute = T * d * eb + kept_rows * d * eb + S * 4 * 3 + T * w.k * 4
+        combine = kept_rows * d * eb + T * d * eb + (T * d * eb if w.residual else 0) + \
+            (T * d * eb if w.num_shared else 0) + S * 8
+        return route, permute, combine
     if routing == "expert_choice":
         R = kept_rows
         # logits GEMM (x, w_r in; logits out), selection (logits in; tok_row,
@@ -523,7 +530,13 @@ def run_ours(args, w, rank, world, local):
         with ClockSampler(uuid) as cs:
             t0.record(stream)
             for i in range(args.steps):
-                fwd(x, out, stage_events=handles[i])
+                if args.routing == "hash":
+                    # the hash routing runs before moe_forward_from_routing:
+                    # the route stage starts before it
+                    evs[i][0].record(stream)
+                    fwd(x, out, stage_events=[0] + list(handles[i][1:]))
+                else:
+                    fwd(x, out, stage_events=handles[i])
             t1.record(stream)
             barrier()
         return t0.elapsed_time(t1), evs, cs.summary()
