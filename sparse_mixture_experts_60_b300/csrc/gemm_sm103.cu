@@ -155,8 +155,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;                 // one 128-byte swizzle atom of bf16
 constexpr int UMMA_K = 16;
-constexpr int kEpiWarps = 8;                       // two per TMEM lane quadrant (default)
-constexpr int kThreads = 64 + 32 * kEpiWarps;       // producer, MMA, epilogue
+constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant (default); a CTA is 64 + 32 EW threads
 // The plain bf16-output kernel of GELU / ReLU layers takes 16 epilogue
 // warps (four per quadrant): at d_model 1024 its activation math, not the
 // tensor cores, bounds a tile.
@@ -412,19 +411,72 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *seg_s, const in
 // 1 - erfc(x) / 2 otherwise; exp(-x^2) = exp(-a^2 / 2) is returned in `e`
 // for the density term of GELU'.  One exponential and one reciprocal per
 // element, where erff and expf cost the backward epilogue twice as much.
+struct ErfcAS7126 {
+    static constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
+                           a4 = -1.453152027f, a5 = 1.061405429f;
+};
 __device__ __forceinline__ float gauss_cdf(float a, float &e) {
-    constexpr float p = 0.3275911f, a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f,
-                    a4 = -1.453152027f, a5 = 1.061405429f;
+    using K = ErfcAS7126;
     const float x = fabsf(a) * 0.70710678118654752f;
-    const float t = __fdividef(1.0f, fmaf(p, x, 1.0f));
+    const float t = __fdividef(1.0f, fmaf(K::p, x, 1.0f));
     e = __expf(-x * x);
-    const float half_erfc = 0.5f * t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1) * e;
+    const float half_erfc = 0.5f * t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, K::a5, K::a4), K::a3), K::a2), K::a1) * e;
     return a >= 0.0f ? 1.0f - half_erfc : half_erfc;
 }
-// GELU(a) = a Phi(a)
-__device__ __forceinline__ float gelu_erf(float v) {
-    float e;
-    return v * gauss_cdf(v, e);
+
+// Paired fp32 arithmetic (f32x2: two lanes of a 64-bit register per
+// instruction), for the activation math of the epilogues.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_splat(float v) { return f2_pack(v, v); }
+__device__ __forceinline__ float rcp_approx(float v) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float exp2_approx(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// GELU(a) = a Phi(a) of two values: the A&S 7.1.26 evaluation of gauss_cdf
+// with the multiplies and the polynomial on paired lanes, Phi(a) from half
+// erfc(|a| / sqrt 2) = t (a1 + t (a2 + ...)) exp(-x^2) / 2, where
+// exp(-x^2) = 2^(-x^2 log2 e).
+__device__ __forceinline__ void gelu_erf2(float &v0, float &v1) {
+    using K = ErfcAS7126;
+    const uint64_t x = f2_mul(f2_pack(fabsf(v0), fabsf(v1)), f2_splat(0.70710678118654752f));
+    float d0, d1;
+    f2_unpack(f2_fma(f2_splat(K::p), x, f2_splat(1.0f)), d0, d1);
+    const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+    float q0, q1;
+    f2_unpack(f2_mul(f2_mul(x, x), f2_splat(-1.4426950408889634f)), q0, q1);   // -x^2 log2 e
+    const uint64_t e = f2_pack(exp2_approx(q0), exp2_approx(q1));
+    uint64_t poly = f2_fma(t, f2_splat(K::a5), f2_splat(K::a4));
+    poly = f2_fma(poly, t, f2_splat(K::a3));
+    poly = f2_fma(poly, t, f2_splat(K::a2));
+    poly = f2_fma(poly, t, f2_splat(K::a1));
+    float h0, h1;
+    f2_unpack(f2_mul(f2_mul(t, poly), f2_mul(e, f2_splat(0.5f))), h0, h1);
+    const float c0 = v0 >= 0.0f ? 1.0f - h0 : h0, c1 = v1 >= 0.0f ? 1.0f - h1 : h1;
+    f2_unpack(f2_mul(f2_pack(v0, v1), f2_pack(c0, c1)), v0, v1);
 }
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 
@@ -656,7 +708,7 @@ __device__ __forceinline__ void epilogue_tile(const Args &args, const Tile &tl, 
                     store_chunk<false>(v, args.pre, args.ld_pre, col, args.N, row_base, tl.seg_end, stg, lane);
                 if (args.act == 1) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+                    for (int i = 0; i < 32; i += 2) gelu_erf2(v[i], v[i + 1]);
                 } else if (args.act == 2) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
@@ -1156,25 +1208,26 @@ __device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, v
     }
 }
 
-template <int BN>
+template <int BN, int EW = kEpiWarps>
 struct PairCfg {
     static constexpr int A_BYTES = BM * BK * 2;              // 128 rows of A
     static constexpr int B_BYTES = (BN / 2) * BK * 2;        // BN/2 rows of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // per CTA
     static constexpr int STAGES = 6;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int EPI_BYTES = kEpiWarps * 32 * 64;
+    static constexpr int EPI_BYTES = EW * 32 * 64;
     static constexpr int BAR_BYTES = 256;
+    static constexpr int THREADS = 64 + 32 * EW;
     static size_t smem_bytes(int G) {
         return 1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + (size_t)2 * (G + 1) * sizeof(int);
     }
 };
 
-template <int BN, bool GATED, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, bool GATED, bool OUT_F32, int EW = kEpiWarps>
+__global__ void __launch_bounds__(64 + 32 * EW, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmB2, const Args args) {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, EW>;
     constexpr int STAGES = C::STAGES;
     constexpr int BN_OUT = GATED ? BN / 2 : BN;
     constexpr int TILE_M = 2 * BM;
@@ -1209,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 2 * kEpiWarps);   // one arrival per epilogue warp of both CTAs
+            mbar_init(&tempty[i], 2 * EW);   // one arrival per epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -1220,7 +1273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
     PDL_ENTER();   // the segment offsets and A are the previous kernel's output
-    for (int i = threadIdx.x; i <= G; i += kThreads)
+    for (int i = threadIdx.x; i <= G; i += C::THREADS)
         seg_s[i] = args.seg ? args.seg[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
     const int n_tiles = (args.N + BN_OUT - 1) / BN_OUT;
@@ -1331,7 +1384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int row_base = tl.row0 + BM * (int)rank + q * 32;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN, GATED, OUT_F32>(args, tl, args.out, row_base, tbase, half, lane, stg, false);
+            epilogue_tile<BN, GATED, OUT_F32, 0, EW / 4>(args, tl, args.out, row_base, tbase, half, lane, stg, false);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
@@ -1484,9 +1537,9 @@ cudaError_t launch_t(const GemmProblem &p, cudaStream_t s) {
     return launch_pdl(kern, dim3(num_sms()), dim3(64 + 32 * EW + (KG_MN ? 32 : 0)), smem, s, ta, tb, tb2, a);
 }
 
-template <int BN, bool GATED, bool OUT_F32>
+template <int BN, bool GATED, bool OUT_F32, int EW = kEpiWarps>
 cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, EW>;
     constexpr int BOX_B = BN / 2;   // rows of B per CTA
     CUtensorMap ta, tb, tb2;
     if (!make_tmap(&ta, p.A, (uint64_t)p.K, (uint64_t)p.a_rows, BM)) return cudaErrorInvalidValue;
@@ -1517,12 +1570,12 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
     // read with bands of 9 pair tiles, 6.4 GB M-fastest)
     a.band = gemm_band_option() > 0 ? (int)gemm_band_option() : 0;
     const size_t smem = C::smem_bytes(a.G);
-    auto kern = grouped_gemm_pair_kernel<BN, GATED, OUT_F32>;
+    auto kern = grouped_gemm_pair_kernel<BN, GATED, OUT_F32, EW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -1544,8 +1597,10 @@ cudaError_t launch_pair_t(const GemmProblem &p, cudaStream_t s) {
 // lose for the gated first expert GEMM (Mixtral shape: 6.29 vs 5.97 ms);
 // for the second (no activation) they win (Quick Start shape, K = 4096:
 // 0.112 vs 0.125 ms; Mixtral shape, K = 14336: 3.12 vs 3.23 and 3.17 vs
-// 3.22 ms in two runs), so they run the second GEMM of tall groups.  The
-// MOE_OPT_GEMM_PAIR option forces the choice (the tests run both kernels
+// 3.22 ms in two runs), so they run the second GEMM of tall groups.  For
+// the GELU / ReLU first GEMM (Quick Start shape) pairs with 8 or 16
+// epilogue warps measured no faster than one CTA with 16 (0.125-0.128 ms
+// each).  The MOE_OPT_GEMM_PAIR option forces the choice (the tests run both kernels
 // on the same shapes).
 bool use_pair(const GemmProblem &p) {
     const int opt = gemm_pair_option();

@@ -15,8 +15,8 @@ SRC = os.path.join(os.path.dirname(__file__), "..", "sparse_mixture_experts_60_b
 
 def _constants():
     src = open(SRC).read()
-    body = src[src.index("float gauss_cdf(float a, float &e)"):]
-    body = body[:body.index("}")]
+    body = src[src.index("struct ErfcAS7126 {"):]
+    body = body[:body.index("};")]
     vals = dict(re.findall(r"\b(p|a[1-5])\s*=\s*(-?[0-9.]+)f", body))
     assert set(vals) == {"p", "a1", "a2", "a3", "a4", "a5"}, vals
     return {k: float(v) for k, v in vals.items()}
