@@ -72,7 +72,8 @@ def test_forward_line(name, steps, capsys):
     frac, bound2 = expected_frac(w, stages[2], kept, active, steps, ms)
     assert bound2 == bound
     x = torch.empty(w.T, w.d, dtype=torch.bfloat16)
-    bench.finish(_args(steps=steps), w, 0, 1, None, None, x, x, ms, stages, None, kept, CLOCKS, ms * 1.01, active)
+    bench.finish(_args(steps=steps), w, 0, 1, None, None, x, x, ms, stages, None, kept, CLOCKS, (ms * 1.01, 50),
+                 active)
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert KEYS <= set(line)
     assert line["n_gpus"] == 1 and line["scaling"] == "weak" and line["higher_is_better"] is True
@@ -85,6 +86,7 @@ def test_forward_line(name, steps, capsys):
     assert r["unit"] == ("TFLOP/s" if bound == "tensor" else "GB/s")
     e2e = line["e2e"]
     assert e2e["h2d_bytes_per_step"] == e2e["d2h_bytes_per_step"] == w.T * w.d * 2
+    assert e2e["steps"] == 50 and e2e["value"] == pytest.approx(w.T / (ms * 1.01e-3))
     assert line["gpu_launches"] == bench.launches_per_step(w) * steps
     if bound == "tensor":
         assert r["peak"] == (PEAKS["bf16_tflops"] if steps * ms < 1000.0 else PEAKS["bf16_tflops_sustained"])
