@@ -124,11 +124,11 @@ __device__ __forceinline__ void route_group(const RouteParams &p, const float (&
 }
 
 // Per-CTA partials: psum is summed over the groups of a warp (xor
-// butterfly), then over the 8 warps in warp order.
-template <int G, int VPL>
+// butterfly), then over the NW warps in warp order.
+template <int G, int VPL, int NW = 8>
 __device__ __forceinline__ void write_partials(const RouteParams &p, float (&psum)[VPL], float zsum, int r,
                                                int grp, float *s_prob, const int *s_cnt) {
-    __shared__ float s_z[8];
+    __shared__ float s_z[NW];
     const int warp = threadIdx.x >> 5;
     const int EP = G * VPL;
 #pragma unroll
@@ -143,13 +143,13 @@ __device__ __forceinline__ void write_partials(const RouteParams &p, float (&psu
     __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
         float acc = 0.0f;
-        for (int w = 0; w < 8; ++w) acc += s_prob[w * EP + e];
+        for (int w = 0; w < NW; ++w) acc += s_prob[w * EP + e];
         p.part_prob[(int64_t)e * gridDim.x + blockIdx.x] = acc;   // [E][blocks]
         p.part_cnt[(int64_t)e * gridDim.x + blockIdx.x] = s_cnt[e];
     }
     if (threadIdx.x == 0 && p.part_z) {
         float z = 0.0f;
-        for (int w = 0; w < 8; ++w) z += s_z[w];
+        for (int w = 0; w < NW; ++w) z += s_z[w];
         p.part_z[blockIdx.x] = z;
     }
 }
@@ -253,14 +253,19 @@ __global__ void __launch_bounds__(256, EP <= 16 ? 2 : 1) router_fused_kernel(Rou
 }
 
 // Routing from logits in memory (optionally adding the router bias and
-// writing the biased logits back).
-template <int G, int VPL>
-__global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
+// writing the biased logits back).  NW warps share a CTA's 32 tokens: a
+// token's routing is a chain of dependent shuffles (k arg-max rounds), so
+// the wide routers take a warp per token (up to 32 warps) to keep more
+// tokens in flight per SM.
+template <int G, int VPL, int NW>
+__global__ void __launch_bounds__(NW * 32) route_logits_kernel(RouteParams p) {
     PDL_ENTER();
-    constexpr int TPR = 32 / G;             // tokens per warp per round
+    constexpr int TPR = 32 / G;                       // tokens per warp per round
+    constexpr int TPW = kRouteTokPerCta / NW;         // tokens per warp
+    static_assert(TPW % TPR == 0 && TPW >= TPR, "tokens per warp");
     extern __shared__ float dyn[];
-    float *s_prob = dyn;                                  // [8][G*VPL]
-    int *s_cnt = reinterpret_cast<int *>(dyn + 8 * G * VPL);  // [G*VPL]
+    float *s_prob = dyn;                                   // [NW][G*VPL]
+    int *s_cnt = reinterpret_cast<int *>(dyn + NW * G * VPL);  // [G*VPL]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = lane % G, grp = lane / G;
     const int E = p.E;
@@ -272,8 +277,8 @@ __global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
     float zsum = 0.0f;
     const int64_t cta_t0 = (int64_t)blockIdx.x * kRouteTokPerCta;
 #pragma unroll 1
-    for (int round = 0; round < 4 / TPR; ++round) {
-        const int64_t t = cta_t0 + warp * 4 + round * TPR + grp;
+    for (int round = 0; round < TPW / TPR; ++round) {
+        const int64_t t = cta_t0 + warp * TPW + round * TPR + grp;
         const bool tok_ok = t < p.T;
         float l[VPL];
 #pragma unroll
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(RouteParams p) {
         route_group<G, VPL>(p, l, r, tok_ok, t, psum, zsum, s_cnt);
     }
     __syncthreads();
-    write_partials<G, VPL>(p, psum, zsum, r, grp, s_prob, s_cnt);
+    write_partials<G, VPL, NW>(p, psum, zsum, r, grp, s_prob, s_cnt);
 }
 
 // logits = x W^T on CUDA cores, 32x32 output tiles (no bias).
@@ -359,16 +364,18 @@ __global__ void __launch_bounds__(256) route_reduce_kernel(const float *part_pro
     }
 }
 
-template <int G, int VPL>
+// Warps per CTA: one token per warp while the registers allow (VPL <= 8:
+// 62 registers at 1024 threads), else 16 or 8 warps.
+template <int G, int VPL, int NW = (G == 32 ? (VPL <= 8 ? 32 : (VPL <= 16 ? 16 : 8)) : 8)>
 cudaError_t launch_route_logits_t(const RouteParams &p, cudaStream_t s) {
     const int64_t nblk = ceil_div(p.T, kRouteTokPerCta);
-    const size_t smem = (size_t)(8 * G * VPL) * sizeof(float) + (size_t)(G * VPL) * sizeof(int);
-    auto kern = route_logits_kernel<G, VPL>;
+    const size_t smem = (size_t)(NW * G * VPL) * sizeof(float) + (size_t)(G * VPL) * sizeof(int);
+    auto kern = route_logits_kernel<G, VPL, NW>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, dim3((unsigned)nblk), dim3(256), smem, s, p);
+    return launch_pdl(kern, dim3((unsigned)nblk), dim3(NW * 32), smem, s, p);
 }
 
 // Hash routing: one thread per token.  Choice j of a token is
