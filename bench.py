@@ -228,7 +228,7 @@ def launches_per_step(w, routing="topk"):
     nchunk = -(-S // 2048)                    # the two-launch dispatch's largest chunk
     if S == 0:
         n += 1
-    elif S <= 8192 and w.E <= 256:
+    elif S <= 2048 and w.E <= 256:
         n += 2                                # one-CTA dispatch, row copy
     elif nchunk * w.E <= 8192:
         n += 2                                # chunk ranks, row copy with the chunk bases

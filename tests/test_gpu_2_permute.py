@@ -143,7 +143,7 @@ def test_permute_flags_out_of_range_expert(T):
     assert moe.moe_check_device_error() == 0   # read clears the flag
 
 
-@pytest.mark.parametrize("T", [3001, 5001], ids=["one_cta", "two_launch"])
+@pytest.mark.parametrize("T", [1001, 5001], ids=["one_cta", "two_launch"])
 def test_permute_unaligned_topk_idx(T):
     """topk_idx need not be 16-byte aligned: a view starting 4 bytes into a
     buffer gives the same dispatch."""
