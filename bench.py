@@ -807,6 +807,50 @@ def finish(args, w, rank, world, dist, inp, x, out, ms, stage_ms, stats, kept, c
     return 0
 
 
+def run_dense_reference(args, w):
+    """The dense bf16 GEMMs of the same sizes as the workload's two expert
+    GEMMs, by the vendor library (torch.matmul): kept rows x d x nF and kept
+    rows x F x d with every row routed (T k rows), timed as a burst (10 calls)
+    and in a loop of about a second under the power cap, with the clocks
+    sampled.  A yardstick for the grouped expert GEMMs, not part of the
+    layer."""
+    import torch
+    torch.cuda.set_device(0)
+    uuid = str(torch.cuda.get_device_properties(0).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    rows = w.T * w.k
+    n1 = (2 if w.gated else 1) * w.F
+    out = {"metric": "dense bf16 GEMM of the expert GEMM sizes (torch.matmul)", "impl": "dense_gemm_reference",
+           "config": {"workload": w.name, "rows": rows, "d_model": w.d, "d_ff": w.F}, "gemms": {}}
+    g = torch.Generator(device="cuda").manual_seed(11)
+    for name, (M, K, N) in (("ffn1", (rows, w.d, n1)), ("ffn2", (rows, w.F, w.d))):
+        a = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+        b = (torch.randn(K, N, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+        c = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        flops = 2.0 * M * N * K
+        res = {"M": M, "K": K, "N": N}
+        for label, n in (("burst", 10), ("loop", None)):
+            if n is None:   # about one second of back-to-back calls
+                n = max(10, int(1.0 / max(res["burst"]["ms"] * 1e-3, 1e-6)))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with ClockSampler(uuid) as cs:
+                e0.record()
+                for _ in range(n):
+                    torch.matmul(a, b, out=c)
+                e1.record()
+                torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            res[label] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "calls": n, "clocks": cs.summary()}
+        out["gemms"][name] = res
+        del a, b, c
+        torch.cuda.empty_cache()
+    print(json.dumps(out))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -833,6 +877,8 @@ def main():
                     help="time the training step (forward keeping activations + backward) instead")
     ap.add_argument("--routing", default="topk", choices=["topk", "expert_choice", "hash"],
                     help="token-choice top-k (the headline), expert-choice or hash routing")
+    ap.add_argument("--dense-gemm-reference", action="store_true",
+                    help="time the vendor library's dense bf16 GEMMs of the expert GEMM sizes instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -849,6 +895,8 @@ def main():
                     f"_k{args.top_k or w.k}")
     if args.routing == "expert_choice":
         w = dataclasses.replace(w, capacity_factor=float(w.k))
+    if args.dense_gemm_reference:
+        return run_dense_reference(args, w)
     if args.impl == "reference":
         if args.routing != "topk":
             ap.error("--impl reference times the top-k layer only")
