@@ -355,6 +355,22 @@ class MoELayer(_HostPipeline):
         moe_forward(self.cfg, self.weights, x, self.sel_bias, out, self.io, self.ws, stream, stage_events)
         return out
 
+    def graphed(self, x, out):
+        """A CUDA graph of ``forward(x, out)`` on these two device buffers:
+        one eager forward first (it also sets up the library's per-device
+        state), then a capture on torch's capture stream.  ``g.replay()``
+        runs the whole layer with one launch from the host: copy new inputs
+        into ``x`` first, read the result from ``out``.  The graph is valid
+        while the layer, ``x`` and ``out`` live and the layer's weights keep
+        their addresses."""
+        import torch
+        self.forward(x, out)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            self.forward(x, out)
+        return g
+
     def forward_host(self, x_host, out_host, x_dev=None, out_dev=None, stream=None):
         """End-to-end call from host buffers (pinned for overlap): copy x in,
         run the layer, copy out back; asynchronous on the stream."""

@@ -179,6 +179,34 @@ def test_host_batches_pipeline_matches_forward():
     np.testing.assert_array_equal(host(ref0), got["out"])
 
 
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 64), ("quickstart_bf16", 1000), ("deepseek_v3", 200)])
+def test_graph_replay_matches_forward(name, T):
+    """MoELayer.graphed: replays of the captured forward, on new inputs
+    copied into the captured x buffer, give exactly the eager forward's
+    output, routing and statistics for those inputs."""
+    w = wl.WORKLOADS[name].scaled(T)
+    inp = wl.make_inputs(w)
+    layer, first = run_layer(w, inp)
+    x = dev(inp["x"])
+    out = torch.empty(w.T, w.d, dtype=layer.out_dtype(), device="cuda")
+    g = layer.graphed(x, out)
+    torch.cuda.synchronize()
+    x0 = x.clone()
+    x1 = (x0.flip(0) * 0.5).contiguous()             # a second, different batch
+    for xb in (x1, x0, x1):
+        x.copy_(xb)
+        g.replay()
+        torch.cuda.synchronize()
+        got_out, got_idx, got_stats = out.clone(), layer.io["topk_idx"].clone(), layer.stats()
+        ref = layer.forward(xb)
+        torch.cuda.synchronize()
+        assert torch.equal(got_out, ref), name
+        assert torch.equal(got_idx, layer.io["topk_idx"]), name
+        assert got_stats == layer.stats(), name
+    assert moe.moe_check_device_error() == 0
+    np.testing.assert_array_equal(host(layer.forward(x0)), first["out"])
+
+
 def run_steps(w, inp):
     """The layer as the separate calls of the C ABI, each with its own
     workspace: moe_route -> moe_permute -> moe_expert_ffn (-> moe_shared_ffn)
